@@ -1,0 +1,87 @@
+// kernels.h -- host-side launchers of the MSA kernels (internal to libmsa.so).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "msa.h"
+
+namespace msa {
+
+// Validated problem, with derived sizes.
+struct Shape {
+  int B, N, H_q, H_kv, d, d_idx, Bk, topk, causal;
+  float scale, scale_idx;
+  int G;   // H_q / H_kv
+  int nb;  // ceil(N / Bk)
+  int64_t rows_kv() const { return (int64_t)B * H_kv * N; }  // (b, g, i) rows
+  int64_t keys() const { return (int64_t)B * H_kv * nb; }    // (b, g, block) lists
+};
+
+// Per-call device context.
+struct Ctx {
+  int* status;      // device status word of the current device
+  uint64_t wait_ns; // bound of every device-side wait
+  int debug;        // msa_debug_set flags
+  int num_sms;
+};
+
+// Inverted lists ("plan"): for every (b, g, block c), the (query, slot) pairs
+// whose block set holds c, as a CSR over keys = (b*H_kv + g)*nb + c, and the
+// split of every list into tiles of `qpt` queries.
+struct Plan {
+  int* cnt;      // [keys]      counts, reused as fill cursors
+  int* off;      // [keys + 1]  CSR offsets into entries
+  int* toff;     // [keys + 1]  tile offsets; toff[keys] = number of tiles
+  int* entries;  // [rows_kv * topk]  (i << 5) | slot
+};
+
+size_t plan_bytes(const Shape& s);
+Plan plan_carve(const Shape& s, void* ws);
+cudaError_t launch_plan(const Shape& s, const int32_t* block_idx, int qpt, const Plan& pl,
+                        const Ctx& cx, cudaStream_t st);
+
+// Index branch: tcgen05 scoring + block max-pool + register top-k -> block_idx.
+cudaError_t launch_index_topk(const Shape& s, const void* q_idx, const void* k_idx,
+                              int32_t* block_idx, const Ctx& cx, cudaStream_t st);
+
+// Index LSE over the selected tokens (gathered, KV-outer) -> lse_idx.
+size_t index_lse_ws_bytes(const Shape& s);
+cudaError_t launch_index_lse(const Shape& s, const void* q_idx, const void* k_idx,
+                             const int32_t* block_idx, const Plan& pl, float* lse_part,
+                             float* lse_idx, const Ctx& cx, cudaStream_t st);
+
+// Main forward: gathered KV-outer partials, then the per-row combine.
+cudaError_t launch_attn_fwd(const Shape& s, const void* q, const void* k, const void* v,
+                            const int32_t* block_idx, const Plan& pl, __nv_bfloat16* o_part,
+                            float* lse_part, void* o, float* lse, const Ctx& cx,
+                            cudaStream_t st);
+
+// Backward pieces.
+struct BwdBufs {
+  float* D;          // [B][H_q][N]
+  float* dq_acc;     // [B][N][H_q][d]
+  float* dk_acc;     // [B][N][H_kv][d]
+  float* dv_acc;     // [B][N][H_kv][d]
+  float* dqi_acc;    // [B][N][H_kv][d_idx]
+  float* dki_acc;    // [B][N][d_idx]
+  double* kl_acc;    // 1
+};
+cudaError_t launch_attn_bwd(const Shape& s, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const void* dO, const void* q_idx,
+                            const void* k_idx, const int32_t* block_idx, const float* lse_idx,
+                            float kl_weight, const Plan& pl, const BwdBufs& bb, void* dq,
+                            void* dk, void* dv, void* dq_idx, void* dk_idx, float* kl_out,
+                            const Ctx& cx, cudaStream_t st);
+
+// TMA descriptor encoding through the driver entry point (no libcuda link).
+bool encode_tiled(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                  CUtensorMapSwizzle swz);
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace msa

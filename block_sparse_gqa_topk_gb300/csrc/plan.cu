@@ -1,0 +1,163 @@
+// plan.cu -- inverted lists of the block selection.
+//
+// The main branch runs KV-outer: for every (batch, group, key block c) it gathers
+// the queries whose block set holds c, packs them into 128-row tiles (queries x
+// group heads) and runs one dense tile per 128 rows.  This is the query-gather
+// reparameterisation of block-sparse attention described for both prior kernels:
+// the MoBA-style varlen view of Flash-MSA (tech.kuratif.com ¶7, deephorus.pages.dev
+// ¶4) and fmha_sm100's KV-outer query gather (7minutos.es, "El codiseño del
+// kernel", second idea).  This file builds the lists from block_idx:
+//   count  -> per-list sizes (one atomic per selected block),
+//   scan   -> CSR offsets and tile offsets (one CTA, decoupled chunks),
+//   fill   -> (query << 5 | slot) entries.
+// HBM-bound integer work: block_idx is read twice, entries written once.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace msa {
+namespace {
+
+__global__ void plan_count_kernel(const int32_t* __restrict__ block_idx, int64_t rows, int topk,
+                                  int N, int nb, int* __restrict__ cnt, int* status) {
+  const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (t >= rows * topk) return;
+  const int c = block_idx[t];
+  if (c < 0) return;
+  if (c >= nb) {  // not a block of this sequence: record it, touch nothing
+    set_status(status, MSA_ERR_ARG);
+    return;
+  }
+  const int64_t r = t / topk;  // (b*H_kv + g)*N + i
+  const int64_t bg = r / N;
+  atomicAdd(&cnt[bg * nb + c], 1);
+}
+
+// Exclusive scans of cnt (-> off) and of ceil(cnt / qpt) (-> toff) over all keys,
+// then zeroes cnt for use as the fill cursor.  One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) plan_scan_kernel(int* __restrict__ cnt,
+                                                         int* __restrict__ off,
+                                                         int* __restrict__ toff, int64_t keys,
+                                                         int qpt) {
+  __shared__ int s_a[32], s_b[32];
+  __shared__ int carry_a, carry_b;
+  if (threadIdx.x == 0) {
+    carry_a = 0;
+    carry_b = 0;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t base = 0; base < keys; base += 1024) {
+    const int64_t k = base + threadIdx.x;
+    const int a = k < keys ? cnt[k] : 0;
+    const int b = (a + qpt - 1) / qpt;
+    int ia = a, ib = b;  // inclusive warp scans
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int xa = __shfl_up_sync(0xffffffffu, ia, o);
+      const int xb = __shfl_up_sync(0xffffffffu, ib, o);
+      if (lane >= o) {
+        ia += xa;
+        ib += xb;
+      }
+    }
+    if (lane == 31) {
+      s_a[warp] = ia;
+      s_b[warp] = ib;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int wa = s_a[lane], wb = s_b[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int xa = __shfl_up_sync(0xffffffffu, wa, o);
+        const int xb = __shfl_up_sync(0xffffffffu, wb, o);
+        if (lane >= o) {
+          wa += xa;
+          wb += xb;
+        }
+      }
+      s_a[lane] = wa;  // inclusive over warps
+      s_b[lane] = wb;
+    }
+    __syncthreads();
+    const int pa = carry_a + (warp ? s_a[warp - 1] : 0) + ia - a;
+    const int pb = carry_b + (warp ? s_b[warp - 1] : 0) + ib - b;
+    if (k < keys) {
+      off[k] = pa;
+      toff[k] = pb;
+      cnt[k] = 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 1023) {
+      carry_a = pa + a;
+      carry_b = pb + b;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    off[keys] = carry_a;
+    toff[keys] = carry_b;
+  }
+}
+
+__global__ void plan_fill_kernel(const int32_t* __restrict__ block_idx, int64_t rows, int topk,
+                                 int N, int nb, const int* __restrict__ off,
+                                 int* __restrict__ cursor, int* __restrict__ entries) {
+  const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (t >= rows * topk) return;
+  const int c = block_idx[t];
+  if (c < 0 || c >= nb) return;
+  const int64_t r = t / topk;
+  const int slot = (int)(t - r * topk);
+  const int64_t bg = r / N;
+  const int i = (int)(r - bg * N);
+  const int64_t key = bg * nb + c;
+  const int pos = off[key] + atomicAdd(&cursor[key], 1);
+  entries[pos] = (i << 5) | slot;
+}
+
+}  // namespace
+
+size_t plan_bytes(const Shape& s) {
+  const size_t keys = (size_t)s.keys();
+  return align256(keys * 4) + 2 * align256((keys + 1) * 4) +
+         align256((size_t)s.rows_kv() * s.topk * 4);
+}
+
+Plan plan_carve(const Shape& s, void* ws) {
+  const size_t keys = (size_t)s.keys();
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  Plan pl;
+  pl.cnt = reinterpret_cast<int*>(p);
+  p += align256(keys * 4);
+  pl.off = reinterpret_cast<int*>(p);
+  p += align256((keys + 1) * 4);
+  pl.toff = reinterpret_cast<int*>(p);
+  p += align256((keys + 1) * 4);
+  pl.entries = reinterpret_cast<int*>(p);
+  return pl;
+}
+
+cudaError_t launch_plan(const Shape& s, const int32_t* block_idx, int qpt, const Plan& pl,
+                        const Ctx& cx, cudaStream_t st) {
+  const int64_t keys = s.keys();
+  const int64_t n = s.rows_kv() * s.topk;
+  cudaError_t e = cudaMemsetAsync(pl.cnt, 0, (size_t)keys * 4, st);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)((n + 255) / 256);
+  if (n > 0) {
+    plan_count_kernel<<<grid, 256, 0, st>>>(block_idx, s.rows_kv(), s.topk, s.N, s.nb, pl.cnt,
+                                            cx.status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  plan_scan_kernel<<<1, 1024, 0, st>>>(pl.cnt, pl.off, pl.toff, keys, qpt);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (n > 0) {
+    plan_fill_kernel<<<grid, 256, 0, st>>>(block_idx, s.rows_kv(), s.topk, s.N, s.nb, pl.off,
+                                           pl.cnt, pl.entries);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace msa

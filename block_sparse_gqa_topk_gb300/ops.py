@@ -1,0 +1,180 @@
+"""PyTorch-facing wrappers of the C ABI (device memory and streams only).
+
+Each function checks dtypes/shapes, allocates outputs and a workspace with torch,
+and calls the same-named entry point of libmsa.so on the current CUDA stream.
+There is no fallback: without the built library or a CUDA device these raise.
+
+Layouts (contiguous): q, o [B,N,H_q,d]; k, v [B,N,H_kv,d]; q_idx [B,N,H_kv,d_idx];
+k_idx [B,N,d_idx]; lse [B,H_q,N] f32; lse_idx [B,H_kv,N] f32;
+block_idx [B,H_kv,N,topk] int32.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+
+_WS = {}
+
+
+def _workspace(nbytes: int, device: torch.device) -> torch.Tensor:
+    """Per-device scratch buffer, grown on demand (256-byte aligned by torch)."""
+    key = (device.type, device.index)
+    buf = _WS.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _WS[key] = buf
+    return buf
+
+
+def release_workspace() -> None:
+    _WS.clear()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def make_problem(B, N, H_q, H_kv, d, d_idx, topk, Bk=128, causal=True, scale=None,
+                 scale_idx=None) -> _lib.Problem:
+    return _lib.Problem(B=B, N=N, H_q=H_q, H_kv=H_kv, d=d, d_idx=d_idx, Bk=Bk, topk=topk,
+                        causal=int(bool(causal)),
+                        scale=float(scale if scale is not None else 1.0 / math.sqrt(d)),
+                        scale_idx=float(scale_idx if scale_idx is not None else 0.0))
+
+
+def msa_index_topk(q_idx: torch.Tensor, k_idx: torch.Tensor, topk: int = 16, *, H_q=None, d=None,
+                   Bk: int = 128, causal: bool = True, scale_idx=None, with_lse: bool = True):
+    """Index branch: returns (block_idx [B,H_kv,N,topk] int32, lse_idx [B,H_kv,N] f32 or None)."""
+    _need(q_idx, "q_idx", ndim=4)
+    _need(k_idx, "k_idx", ndim=3)
+    B, N, H_kv, d_idx = q_idx.shape
+    if tuple(k_idx.shape) != (B, N, d_idx):
+        raise ValueError(f"k_idx must be {(B, N, d_idx)}, got {tuple(k_idx.shape)}")
+    prob = make_problem(B, N, H_q or H_kv, H_kv, d or 128, d_idx, topk, Bk, causal, None, scale_idx)
+    dev = q_idx.device
+    block_idx = torch.empty((B, H_kv, N, topk), dtype=torch.int32, device=dev)
+    lse_idx = torch.empty((B, H_kv, N), dtype=torch.float32, device=dev) if with_lse else None
+    nws = _lib.msa_workspace_size(prob, _lib.MSA_WS_INDEX) if with_lse else 0
+    ws = _workspace(nws, dev) if with_lse else None
+    rc = _lib.msa_index_topk(prob, _ptr(q_idx), _ptr(k_idx), _ptr(block_idx), _ptr(lse_idx),
+                             _ptr(ws), nws, _stream(dev))
+    _lib.check(rc, "msa_index_topk")
+    return block_idx, lse_idx
+
+
+def msa_fwd(q, k, v, block_idx, *, scale=None, Bk: int = 128, causal: bool = True, d_idx=64):
+    """Main branch forward: returns (o [B,N,H_q,d] bf16, lse [B,H_q,N] f32)."""
+    _need(q, "q", ndim=4)
+    _need(k, "k", ndim=4)
+    _need(v, "v", ndim=4)
+    _need(block_idx, "block_idx", torch.int32, ndim=4)
+    B, N, H_q, d = q.shape
+    H_kv = k.shape[2]
+    topk = block_idx.shape[3]
+    if tuple(k.shape) != (B, N, H_kv, d) or tuple(v.shape) != (B, N, H_kv, d):
+        raise ValueError("k, v must be [B,N,H_kv,d] matching q")
+    if tuple(block_idx.shape) != (B, H_kv, N, topk):
+        raise ValueError("block_idx must be [B,H_kv,N,topk]")
+    prob = make_problem(B, N, H_q, H_kv, d, d_idx, topk, Bk, causal, scale, None)
+    dev = q.device
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H_q, N), dtype=torch.float32, device=dev)
+    nws = _lib.msa_workspace_size(prob, _lib.MSA_WS_FWD)
+    ws = _workspace(nws, dev)
+    rc = _lib.msa_fwd(prob, _ptr(q), _ptr(k), _ptr(v), _ptr(block_idx), _ptr(o), _ptr(lse),
+                      _ptr(ws), nws, _stream(dev))
+    _lib.check(rc, "msa_fwd")
+    return o, lse
+
+
+def msa_bwd(q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx, kl_weight: float, *,
+            scale=None, scale_idx=None, Bk: int = 128, causal: bool = True):
+    """Fused backward: returns dict dq, dk, dv, dq_idx, dk_idx (bf16) and kl (f32 [1])."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (q_idx, "q_idx")):
+        _need(t, n, ndim=4)
+    _need(k_idx, "k_idx", ndim=3)
+    _need(lse, "lse", torch.float32, ndim=3)
+    _need(lse_idx, "lse_idx", torch.float32, ndim=3)
+    _need(block_idx, "block_idx", torch.int32, ndim=4)
+    B, N, H_q, d = q.shape
+    H_kv = k.shape[2]
+    d_idx = q_idx.shape[3]
+    topk = block_idx.shape[3]
+    prob = make_problem(B, N, H_q, H_kv, d, d_idx, topk, Bk, causal, scale, scale_idx)
+    dev = q.device
+    out = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+           "dq_idx": torch.empty_like(q_idx), "dk_idx": torch.empty_like(k_idx),
+           "kl": torch.empty(1, dtype=torch.float32, device=dev)}
+    nws = _lib.msa_workspace_size(prob, _lib.MSA_WS_BWD)
+    ws = _workspace(nws, dev)
+    rc = _lib.msa_bwd(prob, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(q_idx),
+                      _ptr(k_idx), _ptr(block_idx), _ptr(lse_idx), kl_weight, _ptr(out["dq"]),
+                      _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dq_idx"]), _ptr(out["dk_idx"]),
+                      _ptr(out["kl"]), _ptr(ws), nws, _stream(dev))
+    _lib.check(rc, "msa_bwd")
+    return out
+
+
+def device_status() -> int:
+    """Reads and clears the current device's status word (after syncing the stream)."""
+    return _lib.msa_get_device_status(_stream(torch.device("cuda", torch.cuda.current_device())))
+
+
+class MSAFunction(torch.autograd.Function):
+    """o = MSA(q, k, v, q_idx, k_idx).  Backward returns dq, dk, dv from dO and the
+    KL-alignment gradients for q_idx, k_idx (teacher detached).  The KL value of
+    the last backward is kept in ctx-free storage `MSAFunction.last_kl`."""
+
+    last_kl = None
+
+    @staticmethod
+    def forward(ctx, q, k, v, q_idx, k_idx, topk, Bk, scale, scale_idx, kl_coef):
+        B, N, H_q, d = q.shape
+        block_idx, lse_idx = msa_index_topk(q_idx, k_idx, topk, H_q=H_q, d=d, Bk=Bk,
+                                            scale_idx=scale_idx, with_lse=True)
+        o, lse = msa_fwd(q, k, v, block_idx, scale=scale, Bk=Bk, d_idx=q_idx.shape[3])
+        ctx.save_for_backward(q, k, v, q_idx, k_idx, o, lse, block_idx, lse_idx)
+        ctx.cfg = (Bk, scale, scale_idx, kl_coef)
+        ctx.mark_non_differentiable(block_idx)
+        return o, block_idx
+
+    @staticmethod
+    def backward(ctx, dO, _dblock):
+        q, k, v, q_idx, k_idx, o, lse, block_idx, lse_idx = ctx.saved_tensors
+        Bk, scale, scale_idx, kl_coef = ctx.cfg
+        B, N, H_q, _ = q.shape
+        H_kv = k.shape[2]
+        w = kl_coef / float(B * H_kv * N)
+        g = msa_bwd(q, k, v, o, lse, dO.contiguous(), q_idx, k_idx, block_idx, lse_idx, w,
+                    scale=scale, scale_idx=scale_idx, Bk=Bk)
+        MSAFunction.last_kl = g["kl"]
+        return g["dq"], g["dk"], g["dv"], g["dq_idx"], g["dk_idx"], None, None, None, None, None
+
+
+def attention(q, k, v, q_idx, k_idx, topk: int = 16, Bk: int = 128, scale=None, scale_idx=None,
+              kl_coef: float = 1.0):
+    """MSA attention for training: returns o; backward also trains the index heads.
+    Stopping the gradient at the index-branch input is the caller's job (feed the
+    projections a detached hidden state)."""
+    o, _ = MSAFunction.apply(q, k, v, q_idx, k_idx, topk, Bk, scale, scale_idx, kl_coef)
+    return o

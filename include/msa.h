@@ -1,0 +1,154 @@
+/*
+ * msa.h -- C ABI of the MSA (MiniMax Sparse Attention) training hot path on GB300.
+ *
+ * The method (MiniMax Sparse Attention summary, 7minutos.es, "¿Qué es MSA?" and
+ * "Cómo funcionan las dos ramas"): an index branch -- one index-query head per GQA
+ * group and one shared index-key head -- scores the causally visible keys,
+ * max-pools the scores to Bk-token blocks and keeps the k best blocks per query and
+ * group, the query's own block always included; a main branch runs exact softmax
+ * attention of every query head of the group over the tokens of those blocks.
+ * Training (same page, "Cómo se entrena MSA") adds a KL loss that pulls the index
+ * distribution over the selected tokens toward the group-averaged main
+ * distribution, with the teacher detached, so only the index projections get it.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are row-major and contiguous, bf16 unless stated:
+ *      q, o, dO, dq      [B][N][H_q][d]
+ *      k, v, dk, dv      [B][N][H_kv][d]
+ *      q_idx, dq_idx     [B][N][H_kv][d_idx]
+ *      k_idx, dk_idx     [B][N][d_idx]          (one index-key head for all groups)
+ *      lse               [B][H_q][N]   float32, natural log of sum exp(scale q.k)
+ *      lse_idx           [B][H_kv][N]  float32, natural log of sum exp(scale_idx z)
+ *      block_idx         [B][H_kv][N][topk] int32, ascending block ids, -1 padded
+ *    Query head h belongs to group h / (H_q / H_kv).
+ *  - Every pointer is a DEVICE pointer owned by the caller, 16-byte aligned.  The
+ *    library allocates nothing: each call gets a caller-owned device workspace of at
+ *    least msa_workspace_size() bytes (256-byte aligned), used as scratch only
+ *    during the call's kernels.
+ *  - Calls are asynchronous on `stream` and return after enqueueing.  A non-zero
+ *    return means nothing was enqueued (argument errors) or a launch failed.
+ *    Errors found by the kernels themselves (a bounded wait that ran out) are
+ *    recorded in a per-device status word, read with msa_get_device_status().
+ *  - No exception, trap or abort crosses this boundary.
+ *  - Supported (this build): causal = 1, Bk = 128, d in {64, 128},
+ *    d_idx in {32, 64}, 1 <= topk <= 32, H_q % H_kv == 0 with G = H_q / H_kv in
+ *    {1, 2, 4, 8, 16}, N <= 2^24.  N need not be a multiple of Bk.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return / status codes. */
+#define MSA_OK 0
+#define MSA_ERR_ARG (-1)            /* null pointer, misaligned pointer, bad count */
+#define MSA_ERR_SHAPE (-2)          /* inconsistent sizes (e.g. H_q % H_kv != 0) */
+#define MSA_ERR_UNSUPPORTED (-3)    /* valid problem outside this build's kernels */
+#define MSA_ERR_WORKSPACE (-4)      /* workspace NULL or smaller than required */
+#define MSA_ERR_CUDA (-5)           /* a CUDA launch or runtime call failed */
+#define MSA_ERR_DEVICE_TIMEOUT (-6) /* a kernel's bounded wait ran out (status word) */
+
+/* Problem description.  scale: main softmax scale (> 0; e.g. 1/sqrt(d)).
+ * scale_idx: index-logit scale sigma_I used by lse_idx, the KL and its gradients;
+ * <= 0 selects 1/sqrt(d_idx).  Block selection ranks raw index dot products and
+ * does not depend on scale_idx (softmax keeps the order: "El codiseño del kernel",
+ * first idea).  The local block counts inside the topk budget. */
+typedef struct msa_problem {
+  int32_t B, N, H_q, H_kv, d, d_idx, Bk, topk;
+  int32_t causal;
+  float scale;
+  float scale_idx;
+} msa_problem_t;
+
+/* Which call a workspace is sized for. */
+#define MSA_WS_INDEX 0
+#define MSA_WS_FWD 1
+#define MSA_WS_BWD 2
+
+/* Bytes of workspace the call `which` needs for problem p (0 if p is invalid). */
+size_t msa_workspace_size(const msa_problem_t* p, int which);
+
+/*
+ * Index branch forward.
+ *   Scores s[b,g,i,j] = q_idx[b,i,g,:] . k_idx[b,j,:] for every key j in a block
+ *   wholly before query i's own block, max-pools them per Bk-token block, and keeps
+ *   the topk-1 best such blocks plus the query's own block ("Cómo funcionan las dos
+ *   ramas" ¶1-2; Flash-MSA article, tech.kuratif.com, ¶3 and ¶6: max-pooled
+ *   128-token blocks, register top-k, local score forced to +inf).  Ranking uses
+ *   the raw scores, no exp ("El codiseño del kernel", first idea).  Ties rank the
+ *   lower block id first.  When fewer than topk blocks are visible all are taken
+ *   and the remaining slots are -1.
+ *   If lse_idx is not NULL it also writes the index log-sum-exp over the selected
+ *   tokens (the cheap recompute of "Accelerating Million-Token Training", ¶4):
+ *   lse_idx[b,g,i] = log sum_{j in T(b,g,i)} exp(scale_idx * s[b,g,i,j]), where
+ *   T is the set of tokens j <= i of the selected blocks.
+ * In:  q_idx, k_idx (bf16).  Out: block_idx (int32), lse_idx (float32, optional).
+ */
+int msa_index_topk(const msa_problem_t* p, const void* q_idx, const void* k_idx,
+                   int32_t* block_idx, float* lse_idx, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream);
+
+/*
+ * Main branch forward: exact block-sparse GQA softmax attention.
+ *   For query i, head h of group g: o[b,i,h] = sum_{j in T} P_j v[b,j,g] with
+ *   P = softmax_j(scale * q[b,i,h] . k[b,j,g]) over T(b,g,i) (the causally visible
+ *   tokens of the group's blocks, "Cómo funcionan las dos ramas" ¶3), and
+ *   lse[b,h,i] = log sum_{j in T} exp(scale q.k) kept for the backward (Flash-MSA
+ *   article ¶6).  block_idx is msa_index_topk's output (or any valid set: ascending
+ *   ids, own block included, -1 padding).
+ * In:  q, k, v (bf16), block_idx.  Out: o (bf16), lse (float32).
+ */
+int msa_fwd(const msa_problem_t* p, const void* q, const void* k, const void* v,
+            const int32_t* block_idx, void* o, float* lse, void* workspace,
+            size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Fused backward of the main branch and of the KL alignment loss, over the cached
+ * block indices (Flash-MSA article ¶7; "Cómo se entrena MSA" ¶1-2).
+ *   Main: dq, dk, dv of sum(dO * o), no KL term (the teacher is detached).
+ *   KL:   p_T[j] = mean over the group's heads of P_h[j];
+ *         p_I[j] = exp(scale_idx z_j - lse_idx), z_j = q_idx . k_idx[j];
+ *         KL = kl_weight * sum over (b, g, i) of sum_j p_T (log p_T - log p_I);
+ *         dq_idx, dk_idx are its gradients with p_T held fixed
+ *         (dz_j = kl_weight (p_I - p_T)); dk_idx sums over groups.
+ *   kl_weight is the per-row weight, e.g. coef / (B * H_kv * N) for a mean.
+ *   o, lse: msa_fwd's outputs; lse_idx: msa_index_topk's.
+ * In:  q, k, v, o, dO, q_idx, k_idx (bf16), lse, lse_idx (float32), block_idx.
+ * Out: dq, dk, dv, dq_idx, dk_idx (bf16, overwritten); kl_out (one float32 on the
+ *      device, overwritten with the KL value; may be NULL).
+ */
+int msa_bwd(const msa_problem_t* p, const void* q, const void* k, const void* v, const void* o,
+            const float* lse, const void* dO, const void* q_idx, const void* k_idx,
+            const int32_t* block_idx, const float* lse_idx, float kl_weight, void* dq, void* dk,
+            void* dv, void* dq_idx, void* dk_idx, float* kl_out, void* workspace,
+            size_t workspace_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's status word
+ * (MSA_OK or the first MSA_ERR_* a kernel recorded since the last read). */
+int msa_get_device_status(cudaStream_t stream, int* status);
+
+/* Human-readable text for a status code (static storage). */
+const char* msa_status_string(int code);
+
+/* Test knob for the failure path, per process: the bounded device waits give up
+ * after wait_limit_ns (0 restores the default of 2 s); flags bit 0 makes the next
+ * index-top-k launches withhold their first TMA load, so the consumer's wait runs
+ * out, the kernel records MSA_ERR_DEVICE_TIMEOUT and returns without hanging. */
+int msa_debug_set(uint64_t wait_limit_ns, int flags);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int msa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

@@ -111,17 +111,19 @@ def select(cfg, inputs, rows=None, pooled=False, n_threads=0, **over):
     return bi, kth, pl
 
 
-def forward(cfg, inputs, block_idx, rows=None, n_threads=0, **over):
-    """(o [R,H_q,d], lse [R,H_q], lse_idx [R,H_kv]) over the given block sets."""
+def forward(cfg, inputs, block_idx, rows=None, n_threads=0, main=True, index=True, **over):
+    """(o [R,H_q,d], lse [R,H_q], lse_idx [R,H_kv]) over the given block sets; main=False
+    skips o/lse (None), index=False skips lse_idx (None)."""
     p = problem(cfg, **over)
     rows, R = _rows(rows)
     if R is None:
         R = p.B * p.N
-    o = np.empty((R, p.H_q, p.d))
-    lse = np.empty((R, p.H_q))
-    lse_idx = np.empty((R, p.H_kv))
+    o = np.empty((R, p.H_q, p.d)) if main else None
+    lse = np.empty((R, p.H_q)) if main else None
+    lse_idx = np.empty((R, p.H_kv)) if index else None
     bi = np.ascontiguousarray(block_idx, dtype=np.int32).reshape(R, p.H_kv, p.topk)
-    ins = [_u16(inputs[n]) for n in ("q", "k", "v", "q_idx", "k_idx")]
+    want = (("q", "k", "v") if main else ()) + (("q_idx", "k_idx") if index else ())
+    ins = [_u16(inputs[n]) if n in want else None for n in ("q", "k", "v", "q_idx", "k_idx")]
     rc = _get().oracle_forward(ctypes.byref(p), *[_ptr(a) for a in ins], _ptr(rows), R,
                                _ptr(bi), _ptr(o), _ptr(lse), _ptr(lse_idx), n_threads)
     if rc:

@@ -329,7 +329,7 @@ static void fwd_task(void* vctx, int64_t t, void* scratch) {
   int64_t* toks = (int64_t*)scratch;
   double* s = (double*)(toks + (int64_t)p->topk * p->Bk);
   int nT = token_set(p, i, cx->block_idx + t * p->topk, toks);
-  for (int hh = 0; hh < G; ++hh) {
+  for (int hh = 0; hh < G && (cx->o || cx->lse); ++hh) {
     int h = g * G + hh;
     const uint16_t* qh = q_row(in, b, i, h);
     for (int n = 0; n < nT; ++n) s[n] = p->scale * dot_bb(qh, k_row(in, b, toks[n], g), p->d);
@@ -359,7 +359,8 @@ int oracle_forward(const oracle_problem_t* p, const uint16_t* q, const uint16_t*
                    const uint16_t* v, const uint16_t* q_idx, const uint16_t* k_idx,
                    const int64_t* rows, int64_t n_rows, const int32_t* block_idx, double* o,
                    double* lse, double* lse_idx, int n_threads) {
-  if (check_problem(p) || !q || !k || !v || !block_idx) return OR_EARG;
+  if (check_problem(p) || !block_idx) return OR_EARG;
+  if ((o || lse) && (!q || !k || !v)) return OR_EARG;
   if (lse_idx && (!q_idx || !k_idx)) return OR_EARG;
   if (!rows) n_rows = (int64_t)p->B * p->N;
   fwd_ctx_t cx = {{p, q, k, v, q_idx, k_idx, NULL}, rows, n_rows, block_idx, o, lse, lse_idx};

@@ -14,3 +14,10 @@ if HERE not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+
+
+def pytest_sessionstart(session):
+    import oracle
+    from block_sparse_gqa_topk_gb300 import build as _build
+    oracle.build()
+    _build.build()

@@ -1,0 +1,97 @@
+"""The C ABI library on the CPU: it loads, exports every entry point that
+include/msa.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_sparse_gqa_topk_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "msa.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(msa_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("msa_index_topk", "msa_fwd", "msa_bwd", "msa_workspace_size"):
+        assert want in names
+    assert set(names) == set(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def _prob(**kw):
+    base = dict(B=1, N=2048, H_q=8, H_kv=2, d=64, d_idx=32, Bk=128, topk=4, causal=1, scale=0.125,
+                scale_idx=0.0)
+    base.update(kw)
+    return _lib.Problem(**base)
+
+
+def test_status_strings_and_version():
+    for code in range(0, -7, -1):
+        assert _lib.status_string(code)
+    assert "unknown" in _lib.status_string(-99)
+    assert _lib.msa_version() >= 10000
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H_q=6, H_kv=4), _lib.MSA_ERR_SHAPE),
+    (dict(N=-1), _lib.MSA_ERR_SHAPE),
+    (dict(topk=0), _lib.MSA_ERR_SHAPE),
+    (dict(Bk=64), _lib.MSA_ERR_UNSUPPORTED),
+    (dict(d=96), _lib.MSA_ERR_UNSUPPORTED),
+    (dict(d_idx=16), _lib.MSA_ERR_UNSUPPORTED),
+    (dict(topk=33), _lib.MSA_ERR_UNSUPPORTED),
+    (dict(causal=0), _lib.MSA_ERR_UNSUPPORTED),
+    (dict(scale=0.0), _lib.MSA_ERR_ARG),
+    (dict(scale=float("nan")), _lib.MSA_ERR_ARG),
+])
+def test_bad_problems_are_rejected_on_the_host(kw, code):
+    p = _prob(**kw)
+    assert _lib.msa_workspace_size(p, _lib.MSA_WS_FWD) == 0
+    assert _lib.msa_index_topk(p, 16, 16, 16, None, None, 0, None) == code
+    assert _lib.msa_fwd(p, 16, 16, 16, 16, 16, 16, None, 0, None) == code
+
+
+def test_null_and_misaligned_pointers_are_rejected():
+    p = _prob()
+    assert _lib.msa_index_topk(p, None, 16, 16, None, None, 0, None) == _lib.MSA_ERR_ARG
+    assert _lib.msa_index_topk(p, 18, 16, 16, None, None, 0, None) == _lib.MSA_ERR_ARG
+    assert _lib.msa_fwd(p, 16, 16, 16, 16, 16, 16, None, 0, None) == _lib.MSA_ERR_WORKSPACE
+    assert _lib.msa_fwd(p, 16, 16, None, 16, 16, 16, 256, 1 << 40, None) == _lib.MSA_ERR_ARG
+    small = _lib.msa_workspace_size(p, _lib.MSA_WS_FWD) - 1
+    assert _lib.msa_fwd(p, 16, 16, 16, 16, 16, 16, 256, small, None) == _lib.MSA_ERR_WORKSPACE
+
+
+def test_empty_problem_is_a_no_op():
+    p = _prob(N=0)
+    assert _lib.msa_index_topk(p, None, None, None, None, None, 0, None) == _lib.MSA_OK
+    assert _lib.msa_fwd(p, None, None, None, None, None, None, None, 0, None) == _lib.MSA_OK
+
+
+def test_workspace_sizes_grow_with_the_problem():
+    a = [_lib.msa_workspace_size(_prob(N=n), w) for n in (1024, 4096) for w in range(3)]
+    assert all(x > 0 for x in a)
+    assert a[3] > a[0] and a[4] > a[1] and a[5] > a[2]
+
+
+def test_product_code_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "block_sparse_gqa_topk_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "liboracle" not in text and "msa_oracle" not in text, f
