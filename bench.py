@@ -1,0 +1,385 @@
+#!/usr/bin/env python
+"""Benchmark of the MSA training hot path on GB300.
+
+One step = the whole hot path over one batch of the 128K workload (B=1,
+N=131072, H_q=32, H_kv=8, d=128, d_idx=64, Bk=128, k=16, causal; seeded
+N(0,1) inputs with 16 needle blocks per group): index scoring + top-k (+ index
+LSE), block-sparse forward, fused backward with the KL gradient.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  `value` is device-timed tokens/s with inputs resident in
+HBM; `e2e` is the same metric through the public API with pinned host inputs
+copied in and the KL read back every step; `roofline` is the dominant kernel,
+timed live with CUDA events around its launches inside the timed steps;
+`cpu_baseline` is the float64 oracle on a bounded row sample on the host cores.
+`--impl reference` times that oracle alone (the reference arm).
+Under torchrun (N > 1) every rank runs an independent replica (no data-path
+collective): weak scaling, value = tokens of all ranks / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_sparse_gqa_topk_gb300 import synth  # noqa: E402
+
+METRIC = "MSA fwd+bwd tokens/s @128K (Bk=128,k=16); % of bf16 tensor-pipe peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def workload_name(cfg):
+    return (f"MSA fwd+bwd: B={cfg.B} N={cfg.N} H_q={cfg.H_q} H_kv={cfg.H_kv} d={cfg.d} "
+            f"d_idx={cfg.d_idx} Bk={cfg.Bk} k={cfg.topk} causal bf16, N(0,1) + "
+            f"{cfg.n_needle} needle blocks/group, seed {cfg.seed}")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "of measured"
+    return dict(FALLBACK_PEAKS), "of fallback"
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work (what the method must compute, not what a kernel happens to do)
+# ----------------------------------------------------------------------------
+def token_set_total(cfg, block_idx_np):
+    """Sum over (b, g, i) of |T(b,g,i)|: selected blocks wholly before the query
+    count Bk tokens, the own block counts i - Bk*c_i + 1."""
+    i = np.arange(cfg.N)
+    ci = i // cfg.Bk
+    bi = block_idx_np
+    full = ((bi >= 0) & (bi < ci[None, None, :, None])).sum(axis=-1)
+    tot = full.astype(np.int64).sum() * cfg.Bk + cfg.B * cfg.H_kv * int((i - ci * cfg.Bk + 1).sum())
+    return int(tot)
+
+
+def algorithmic_flops(cfg, sum_T):
+    nb = cfg.nb
+    full_blocks = cfg.N // cfg.Bk
+    idx = 2 * cfg.d_idx * cfg.Bk * cfg.Bk * (full_blocks * (full_blocks - 1) // 2) * cfg.H_kv * cfg.B
+    G = cfg.G
+    fwd_main = 4 * cfg.d * sum_T * G           # S = QK^T and O = PV, every head of the group
+    idx_lse = 2 * cfg.d_idx * sum_T            # index logits over T, once per group
+    bwd_main = 10 * cfg.d * sum_T * G          # S, dP recompute; dV, dK, dQ
+    bwd_kl = 6 * cfg.d_idx * sum_T             # z recompute; dk_idx, dq_idx
+    _ = nb
+    return {"index": idx, "index_lse": idx_lse, "fwd": fwd_main, "bwd": bwd_main + bwd_kl}
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if gpu_id:
+                cmd += ["-i", gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# the oracle on a bounded sample (cpu_baseline and the reference arm)
+# ----------------------------------------------------------------------------
+def oracle_sample(cfg, host, n_rows, seed):
+    import oracle
+    rows = synth.sample_rows(cfg, n_rows, seed)
+    t0 = time.perf_counter()
+    bi, _, _ = oracle.select(cfg, host, rows=rows)
+    oracle.forward(cfg, host, bi, rows=rows)
+    oracle.backward(cfg, host, bi, cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N), rows=rows)
+    dt = time.perf_counter() - t0
+    return len(rows), dt
+
+
+def run_reference(args, cfg, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    host = synth.make_inputs(cfg)
+    rows_per_step = args.ref_rows
+    for w in range(args.warmup):
+        oracle_sample(cfg, host, rows_per_step, seed=500 + w)
+    total_rows, total_t = 0, 0.0
+    for k in range(args.steps):
+        n, dt = oracle_sample(cfg, host, rows_per_step, seed=600 + k)
+        total_rows += n
+        total_t += dt
+    v = total_rows / total_t
+    cores = os.cpu_count()
+    sample = (f"{rows_per_step} seeded query rows (+ first/last) of the 128K workload per step, "
+              f"all {cfg.H_kv} groups: index top-k, forward, backward in float64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(cfg), "global_batch": cfg.B, "seq_len": cfg.N,
+                   "parallelism": "host threads"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, cfg, rank, world):
+    import torch
+    import torch.distributed as dist
+    from block_sparse_gqa_topk_gb300 import _lib, ops
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    _lib.load()
+    host = synth.make_inputs(cfg)
+    names = ("q", "k", "v", "q_idx", "k_idx", "dO")
+
+    def to_dev(x):
+        return torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    d = {n: to_dev(host[n]) for n in names}
+    w = cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(t, phase_ev=None):
+        if phase_ev:
+            phase_ev[0].record(stream)
+        bi, li = ops.msa_index_topk(t["q_idx"], t["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d)
+        if phase_ev:
+            phase_ev[1].record(stream)
+        o, lse = ops.msa_fwd(t["q"], t["k"], t["v"], bi, scale=cfg.scale, d_idx=cfg.d_idx)
+        if phase_ev:
+            phase_ev[2].record(stream)
+        g = ops.msa_bwd(t["q"], t["k"], t["v"], o, lse, t["dO"], t["q_idx"], t["k_idx"], bi, li, w,
+                        scale=cfg.scale)
+        if phase_ev:
+            phase_ev[3].record(stream)
+        return bi, g
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        bi, g = step(d)
+    torch.cuda.synchronize()
+    st = ops.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {_lib.status_string(st)}")
+    sum_T = token_set_total(cfg, bi.cpu().numpy())
+    flops = algorithmic_flops(cfg, sum_T)
+
+    # per-kernel events (hook) and per-phase events, one set per timed step
+    K = args.steps
+    kev = {kname: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(K)] for kname in ("index", "fwd", "bwd")}
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for lst in kev.values():  # materialise the events so their handles exist
+        for a, b in lst:
+            a.record(stream)
+            b.record(stream)
+    kid = {"index": _lib.MSA_KERNEL_INDEX, "fwd": _lib.MSA_KERNEL_FWD, "bwd": _lib.MSA_KERNEL_BWD}
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    launches0 = _lib.msa_kernel_launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for s in range(K):
+        for kname, lst in kev.items():
+            _lib.msa_set_kernel_events(kid[kname], lst[s][0].cuda_event, lst[s][1].cuda_event)
+        step(d, pev[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = _lib.msa_kernel_launch_count() - launches0
+    clk = clocks.stop()
+    for kname in kev:
+        _lib.msa_set_kernel_events(kid[kname], None, None)
+    st = ops.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {_lib.status_string(st)}")
+
+    ms = t_start.elapsed_time(t_end) / K
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    tokens = cfg.B * cfg.N * world
+    value = tokens / (ms / 1000.0)
+
+    kern_ms = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in kev.items()}
+    phase_ms = {
+        "index": statistics.mean(e[0].elapsed_time(e[1]) for e in pev),
+        "fwd": statistics.mean(e[1].elapsed_time(e[2]) for e in pev),
+        "bwd": statistics.mean(e[2].elapsed_time(e[3]) for e in pev),
+    }
+    peaks, peak_src = load_peaks()
+    peak_tf = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    kflops = {"index": flops["index"], "fwd": flops["fwd"], "bwd": flops["bwd"]}
+    dom = max(kern_ms, key=lambda k: kern_ms[k])
+    achieved = kflops[dom] / (kern_ms[dom] / 1000.0) / 1e12
+    traffic = None
+    tf_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tf_path):
+        try:
+            with open(tf_path) as f:
+                traffic = json.load(f).get(dom)
+        except (OSError, ValueError):
+            traffic = None
+    total_flops = sum(flops.values())
+
+    # ---- end to end through the public API with host buffers ----
+    pinned = {n: torch.from_numpy(host[n].view(np.int16)).pin_memory() for n in names}
+    dbuf = {n: torch.empty_like(d[n]) for n in names}
+    kl_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    h2d = sum(pinned[n].numel() * 2 for n in names)
+    e2e_steps = max(1, min(K, args.e2e_steps))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for n in names:
+            dbuf[n].view(torch.int16).copy_(pinned[n], non_blocking=True)
+        _, g = step(dbuf)
+        kl_host.copy_(g["kl"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_val = tokens / (e2e_ms / 1000.0)
+    del pinned, dbuf
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_rows, dt = oracle_sample(cfg, host, args.cpu_rows, seed=900)
+        cpu = {"value": n_rows / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": (f"{n_rows} seeded query rows of the 128K workload, all {cfg.H_kv} groups: "
+                          f"index top-k, forward, backward in float64 ({dt:.1f} s)")}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_name(cfg), "global_batch": cfg.B * world,
+                       "seq_len": cfg.N, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (q and dO are 1.07 GB each)"},
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf,
+                         "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
+                         "peak_source": f"bf16_tflops_sustained {peak_src}"},
+            "pct_bf16_peak_step": total_flops / (ms / 1000.0) / 1e12 / peak_tf,
+            "kernels_ms": kern_ms, "phases_ms": phase_ms,
+            "kernel_tflops": {k: kflops[k] / (kern_ms[k] / 1000.0) / 1e12 for k in kern_ms},
+            "algorithmic_tflop_per_step": total_flops / 1e12,
+            "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": 4, "steps": e2e_steps},
+            "cpu_baseline": cpu,
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default="128k", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-rows", type=int, default=96)
+    ap.add_argument("--ref-rows", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    cfg = synth.CONFIGS[args.config]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, cfg, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -26,7 +26,12 @@ MSA_WS_BWD = 2
 
 # every symbol include/msa.h declares
 EXPORTS = ("msa_workspace_size", "msa_index_topk", "msa_fwd", "msa_bwd",
-           "msa_get_device_status", "msa_status_string", "msa_debug_set", "msa_version")
+           "msa_get_device_status", "msa_status_string", "msa_debug_set",
+           "msa_set_kernel_events", "msa_kernel_launch_count", "msa_version")
+
+MSA_KERNEL_INDEX = 0
+MSA_KERNEL_FWD = 1
+MSA_KERNEL_BWD = 2
 
 
 class Problem(ctypes.Structure):
@@ -70,6 +75,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_status_string.restype = ctypes.c_char_p
     lib.msa_debug_set.argtypes = [ctypes.c_uint64, i32]
     lib.msa_debug_set.restype = i32
+    lib.msa_set_kernel_events.argtypes = [i32, vp, vp]
+    lib.msa_set_kernel_events.restype = i32
+    lib.msa_kernel_launch_count.argtypes = []
+    lib.msa_kernel_launch_count.restype = ctypes.c_uint64
     lib.msa_version.argtypes = []
     lib.msa_version.restype = i32
     _lib = lib
@@ -113,6 +122,15 @@ def msa_get_device_status(stream) -> int:
 
 def msa_debug_set(wait_limit_ns: int, flags: int) -> int:
     return load().msa_debug_set(int(wait_limit_ns), int(flags))
+
+
+def msa_set_kernel_events(kernel: int, start, stop) -> int:
+    """start/stop: cudaEvent_t handles (torch.cuda.Event().cuda_event) or None."""
+    return load().msa_set_kernel_events(int(kernel), start, stop)
+
+
+def msa_kernel_launch_count() -> int:
+    return int(load().msa_kernel_launch_count())
 
 
 def msa_version() -> int:

@@ -325,7 +325,10 @@ cudaError_t launch_gather(const GatherParams& p, const Ctx& cx, cudaStream_t st)
   auto kern = gather_fwd_kernel<D, G, MAIN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
+  if (MAIN) kernel_event(MSA_KERNEL_FWD, true, st);
   kern<<<cx.num_sms, kFwdThreads, L::kBytes, st>>>(p);
+  if (MAIN) kernel_event(MSA_KERNEL_FWD, false, st);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -371,6 +374,7 @@ cudaError_t launch_index_lse(const Shape& s, const void* q_idx, const void* k_id
   const int64_t rows = s.rows_kv();
   lse_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(lse_part, block_idx, lse_idx,
                                                                      rows, s.topk, s.nb);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -410,6 +414,7 @@ cudaError_t launch_attn_fwd(const Shape& s, const void* q, const void* k, const 
     fwd_combine_kernel<64><<<grid, 256, 0, st>>>(o_part, lse_part, block_idx,
                                                  static_cast<__nv_bfloat16*>(o), lse,
                                                  s.rows_kv(), s.N, s.H_kv, s.G, s.topk, s.nb);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -334,7 +334,10 @@ cudaError_t launch_tc(const Shape& s, const CUtensorMap& tq, const CUtensorMap& 
   auto kern = index_topk_tc_kernel<DI, KM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
+  kernel_event(MSA_KERNEL_INDEX, true, st);
   kern<<<grid, kThreads, L::kAlloc, st>>>(tq, tk, p);
+  kernel_event(MSA_KERNEL_INDEX, false, st);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -357,6 +360,7 @@ cudaError_t launch_index_topk(const Shape& s, const void* q_idx, const void* k_i
     const int64_t n = s.rows_kv() * s.topk;
     local_only_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(block_idx, s.rows_kv(), s.N,
                                                                    s.topk);
+    note_launch();
     return cudaGetLastError();
   }
   const int DI = s.d_idx;

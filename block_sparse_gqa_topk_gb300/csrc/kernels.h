@@ -84,4 +84,9 @@ bool encode_tiled(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* 
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Launch bookkeeping (msa_api.cu): counts launches and records the profiling
+// events of msa_set_kernel_events around the named kernels.
+void note_launch(int n = 1);
+void kernel_event(int kernel, bool before, cudaStream_t st);
+
 }  // namespace msa

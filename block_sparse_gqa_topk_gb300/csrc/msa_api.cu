@@ -4,6 +4,7 @@
 // caller's workspace, and sequences the kernels on the caller's stream.  The only
 // library state is the per-device status word and the failure-test knob.
 #include <math.h>
+#include <atomic>
 #include <mutex>
 #include <string.h>
 
@@ -101,7 +102,22 @@ size_t ws_fwd(const Shape& s) {
 
 int finish(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
 
+std::atomic<uint64_t> g_launches{0};
+cudaEvent_t g_ev[3][2] = {{nullptr, nullptr}, {nullptr, nullptr}, {nullptr, nullptr}};
+
 }  // namespace
+
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+void kernel_event(int kernel, bool before, cudaStream_t st) {
+  cudaEvent_t ev = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (kernel >= 0 && kernel < 3 && g_ev[kernel][0] && g_ev[kernel][1])
+      ev = g_ev[kernel][before ? 0 : 1];
+  }
+  if (ev) cudaEventRecord(ev, st);
+}
 
 size_t bwd_ws_bytes(const Shape& s);
 cudaError_t run_bwd(const Shape& s, const void* q, const void* k, const void* v, const void* o,
@@ -117,6 +133,16 @@ using namespace msa;
 extern "C" {
 
 int msa_version(void) { return 10000; }
+
+int msa_set_kernel_events(int kernel, cudaEvent_t start, cudaEvent_t stop) {
+  if (kernel < 0 || kernel > 2) return MSA_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_ev[kernel][0] = (start && stop) ? start : nullptr;
+  g_ev[kernel][1] = (start && stop) ? stop : nullptr;
+  return MSA_OK;
+}
+
+uint64_t msa_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* msa_status_string(int code) {
   switch (code) {

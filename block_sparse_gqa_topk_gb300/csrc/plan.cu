@@ -148,13 +148,16 @@ cudaError_t launch_plan(const Shape& s, const int32_t* block_idx, int qpt, const
   if (n > 0) {
     plan_count_kernel<<<grid, 256, 0, st>>>(block_idx, s.rows_kv(), s.topk, s.N, s.nb, pl.cnt,
                                             cx.status);
+    note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   plan_scan_kernel<<<1, 1024, 0, st>>>(pl.cnt, pl.off, pl.toff, keys, qpt);
+  note_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (n > 0) {
     plan_fill_kernel<<<grid, 256, 0, st>>>(block_idx, s.rows_kv(), s.topk, s.N, s.nb, pl.off,
                                            pl.cnt, pl.entries);
+    note_launch();
     e = cudaGetLastError();
   }
   return e;

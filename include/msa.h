@@ -144,6 +144,21 @@ const char* msa_status_string(int code);
  * out, the kernel records MSA_ERR_DEVICE_TIMEOUT and returns without hanging. */
 int msa_debug_set(uint64_t wait_limit_ns, int flags);
 
+/* Profiling hook.  Kernels: MSA_KERNEL_INDEX (the index scoring + top-k kernel of
+ * msa_index_topk), MSA_KERNEL_FWD (the gathered attention kernel of msa_fwd),
+ * MSA_KERNEL_BWD (the fused backward kernel of msa_bwd).  When start and stop are
+ * both non-NULL, every later launch of that kernel records `start` on its stream
+ * just before the launch and `stop` just after it; NULL clears the hook.  The
+ * events are the caller's (created on the current device) and are only recorded,
+ * never synchronised or destroyed by the library. */
+#define MSA_KERNEL_INDEX 0
+#define MSA_KERNEL_FWD 1
+#define MSA_KERNEL_BWD 2
+int msa_set_kernel_events(int kernel, cudaEvent_t start, cudaEvent_t stop);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t msa_kernel_launch_count(void);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int msa_version(void);
 
