@@ -27,7 +27,8 @@ MSA_WS_BWD = 2
 # every symbol include/msa.h declares
 EXPORTS = ("msa_workspace_size", "msa_index_topk", "msa_fwd", "msa_bwd",
            "msa_get_device_status", "msa_status_string", "msa_debug_set",
-           "msa_set_kernel_events", "msa_kernel_launch_count", "msa_version")
+           "msa_set_kernel_events", "msa_kernel_launch_count", "msa_index_topk_noalloc",
+           "msa_noalloc_scratch_bytes", "msa_version")
 
 MSA_KERNEL_INDEX = 0
 MSA_KERNEL_FWD = 1
@@ -79,6 +80,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_set_kernel_events.restype = i32
     lib.msa_kernel_launch_count.argtypes = []
     lib.msa_kernel_launch_count.restype = ctypes.c_uint64
+    lib.msa_index_topk_noalloc.argtypes = [P, vp, vp, vp, vp, vp]
+    lib.msa_index_topk_noalloc.restype = i32
+    lib.msa_noalloc_scratch_bytes.argtypes = []
+    lib.msa_noalloc_scratch_bytes.restype = sz
     lib.msa_version.argtypes = []
     lib.msa_version.restype = i32
     _lib = lib
@@ -112,6 +117,16 @@ def msa_bwd(prob, q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx, kl_weig
     return load().msa_bwd(ctypes.byref(prob), q, k, v, o, lse, dO, q_idx, k_idx, block_idx,
                           lse_idx, float(kl_weight), dq, dk, dv, dq_idx, dk_idx, kl_out, ws,
                           ws_bytes, stream)
+
+
+def msa_index_topk_noalloc(prob, q_idx, k_idx, block_idx, lse_idx, stream) -> int:
+    """msa_index_topk with the library's built-in scratch instead of a workspace."""
+    return load().msa_index_topk_noalloc(ctypes.byref(prob), q_idx, k_idx, block_idx, lse_idx,
+                                         stream)
+
+
+def msa_noalloc_scratch_bytes() -> int:
+    return int(load().msa_noalloc_scratch_bytes())
 
 
 def msa_get_device_status(stream) -> int:

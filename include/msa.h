@@ -159,6 +159,24 @@ int msa_set_kernel_events(int kernel, cudaEvent_t start, cudaEvent_t stop);
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t msa_kernel_launch_count(void);
 
+/*
+ * Index branch without a caller workspace.  Same computation and outputs as
+ * msa_index_topk, for callers that cannot allocate device memory (a plug-in inside
+ * a framework that owns every allocation, a service whose device footprint is fixed
+ * at start-up).  The pages have no counterpart: this is an interface convenience.
+ * Scratch comes from a 64 MiB array compiled into the library (every GPU that loads
+ * the library holds it until exit; msa_noalloc_scratch_bytes() returns the size).
+ * Problems whose index workspace (msa_workspace_size(p, MSA_WS_INDEX)) exceeds it
+ * return MSA_ERR_WORKSPACE before anything is enqueued; with lse_idx == NULL no
+ * scratch is used.  The first call on a device looks up the array's device address
+ * and must come before any stream capture.  All calls on a device share the array
+ * and it keeps the previous call's contents (the kernels clear what they need):
+ * calls that may overlap on the GPU race and must be ordered by the caller.
+ */
+int msa_index_topk_noalloc(const msa_problem_t* p, const void* q_idx, const void* k_idx,
+                           int32_t* block_idx, float* lse_idx, cudaStream_t stream);
+size_t msa_noalloc_scratch_bytes(void);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int msa_version(void);
 
