@@ -505,50 +505,55 @@ __global__ void bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
   }
 }
 
-// Sum of the per-slot partials of one row: dq (rows of G heads x D) or dq_idx (DI).
-// One warp per output row; lanes own E = W/32 consecutive columns.
-template <int W>
-__global__ void slot_reduce_kernel(const __nv_bfloat16* __restrict__ part,
-                                   const int32_t* __restrict__ block_idx,
-                                   __nv_bfloat16* __restrict__ out, int64_t rows_kv, int G, int N,
-                                   int H_kv, int topk, int nb) {
-  constexpr int E = W / 32;
-  const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+// Sum of the per-slot partials of one (b, g, i) row: dq (the G heads of the group, G*W
+// contiguous bf16 per slot) or dq_idx (G = 1, W = d_idx).  Lanes read 16-byte chunks;
+// when a row has fewer than 32 chunks a warp serves several rows.
+template <int W, int G>
+__global__ void __launch_bounds__(256) slot_reduce_kernel(
+    const __nv_bfloat16* __restrict__ part, const int32_t* __restrict__ block_idx,
+    __nv_bfloat16* __restrict__ out, int64_t rows_kv, int N, int H_kv, int topk, int nb) {
+  constexpr int TC = G * W / 8;               // 16-byte chunks per row and slot
+  constexpr int RPW = TC >= 32 ? 1 : 32 / TC; // rows per warp
+  constexpr int CPL = TC >= 32 ? TC / 32 : 1; // chunks per lane
   const int lane = threadIdx.x & 31;
-  if (w >= rows_kv * G) return;
-  const int64_t rkv = w / G;
-  const int h = (int)(w - rkv * G);
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t rkv = warp * RPW + (TC >= 32 ? 0 : lane / TC);
+  const int l = TC >= 32 ? lane : lane % TC;
+  if (rkv >= rows_kv) return;
   const int i = (int)(rkv % N);
   const int64_t bg = rkv / N;
   const int g = (int)(bg % H_kv);
   const int64_t b = bg / H_kv;
-  float acc[E];
+  float acc[CPL][8];
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int x = 0; x < CPL; ++x)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[x][e] = 0.f;
   const int32_t* sel = block_idx + rkv * topk;
   for (int s = 0; s < topk; ++s) {
     const int c = __ldg(&sel[s]);
     if (c < 0 || c >= nb) continue;
-    const __nv_bfloat16* src = part + ((rkv * topk + s) * G + h) * W + lane * E;
-    if constexpr (E >= 2) {
+    const uint4* src = reinterpret_cast<const uint4*>(part + (rkv * topk + s) * G * W);
 #pragma unroll
-      for (int e = 0; e < E; e += 2) {
-        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(src + e);
-        acc[e] += __low2float(x);
-        acc[e + 1] += __high2float(x);
+    for (int x = 0; x < CPL; ++x) {
+      const uint4 raw = __ldg(&src[l + 32 * x]);
+      const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[x][2 * e] += __low2float(pr[e]);
+        acc[x][2 * e + 1] += __high2float(pr[e]);
       }
-    } else {
-      acc[0] += __bfloat162float(src[0]);
     }
   }
-  // out row: dq [b][i][g*G + h][W]  or  dq_idx [b][i][g][W] (G == 1)
-  __nv_bfloat16* dst = out + (((b * N + i) * H_kv + g) * G + h) * W + lane * E;
-  if constexpr (E >= 2) {
+  // out row: dq [b][i][g*G .. g*G+G-1][W]  or  dq_idx [b][i][g][W]
+  uint4* dst = reinterpret_cast<uint4*>(out + ((b * N + i) * H_kv + g) * (int64_t)G * W);
 #pragma unroll
-    for (int e = 0; e < E; e += 2)
-      *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e], acc[e + 1]);
-  } else {
-    dst[0] = __float2bfloat16(acc[0]);
+  for (int x = 0; x < CPL; ++x) {
+    uint4 o;
+    uint32_t* pw = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pw[e] = pack_bf16(acc[x][2 * e], acc[x][2 * e + 1]);
+    dst[l + 32 * x] = o;
   }
 }
 
@@ -683,27 +688,34 @@ cudaError_t run_bwd(const Shape& s, const void* q, const void* k, const void* v,
   else e = dispatch_bwd_g<64, 32>(s.G, p, cx, st);
   if (e != cudaSuccess) return e;
   {
-    const int64_t warps = s.rows_kv() * s.G;
-    const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
-    if (s.d == 128)
-      slot_reduce_kernel<128><<<grid, 256, 0, st>>>(w.dq_part, block_idx,
-                                                    static_cast<__nv_bfloat16*>(dq), s.rows_kv(),
-                                                    s.G, s.N, s.H_kv, s.topk, s.nb);
+    __nv_bfloat16* dqb = static_cast<__nv_bfloat16*>(dq);
+    __nv_bfloat16* dqib = static_cast<__nv_bfloat16*>(dq_idx);
+    const int64_t R = s.rows_kv();
+    auto grid_for = [&](int tc) {
+      const int64_t rpw = tc >= 32 ? 1 : 32 / tc;
+      const int64_t warps = (R + rpw - 1) / rpw;
+      return (unsigned)((warps + 7) / 8);
+    };
+    if (s.d == 128 && s.G == 4)
+      slot_reduce_kernel<128, 4><<<grid_for(64), 256, 0, st>>>(w.dq_part, block_idx, dqb, R, s.N,
+                                                              s.H_kv, s.topk, s.nb);
+    else if (s.d == 128)
+      slot_reduce_kernel<128, 8><<<grid_for(128), 256, 0, st>>>(w.dq_part, block_idx, dqb, R, s.N,
+                                                               s.H_kv, s.topk, s.nb);
+    else if (s.G == 4)
+      slot_reduce_kernel<64, 4><<<grid_for(32), 256, 0, st>>>(w.dq_part, block_idx, dqb, R, s.N,
+                                                             s.H_kv, s.topk, s.nb);
     else
-      slot_reduce_kernel<64><<<grid, 256, 0, st>>>(w.dq_part, block_idx,
-                                                   static_cast<__nv_bfloat16*>(dq), s.rows_kv(),
-                                                   s.G, s.N, s.H_kv, s.topk, s.nb);
+      slot_reduce_kernel<64, 8><<<grid_for(64), 256, 0, st>>>(w.dq_part, block_idx, dqb, R, s.N,
+                                                             s.H_kv, s.topk, s.nb);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const unsigned grid2 = (unsigned)((s.rows_kv() * 32 + 255) / 256);
     if (s.d_idx == 64)
-      slot_reduce_kernel<64><<<grid2, 256, 0, st>>>(w.dqi_part, block_idx,
-                                                    static_cast<__nv_bfloat16*>(dq_idx),
-                                                    s.rows_kv(), 1, s.N, s.H_kv, s.topk, s.nb);
+      slot_reduce_kernel<64, 1><<<grid_for(8), 256, 0, st>>>(w.dqi_part, block_idx, dqib, R, s.N,
+                                                            s.H_kv, s.topk, s.nb);
     else
-      slot_reduce_kernel<32><<<grid2, 256, 0, st>>>(w.dqi_part, block_idx,
-                                                    static_cast<__nv_bfloat16*>(dq_idx),
-                                                    s.rows_kv(), 1, s.N, s.H_kv, s.topk, s.nb);
+      slot_reduce_kernel<32, 1><<<grid_for(4), 256, 0, st>>>(w.dqi_part, block_idx, dqib, R, s.N,
+                                                            s.H_kv, s.topk, s.nb);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t n = (int64_t)s.B * s.N * s.d_idx;

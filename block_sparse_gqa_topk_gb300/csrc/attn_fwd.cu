@@ -246,61 +246,83 @@ __global__ void __launch_bounds__(kFwdThreads, 1) gather_fwd_kernel(const Gather
   }
 }
 
-// o[b,i,h] and lse[b,h,i] from the k partials of each (b, g, i, h) row.  One warp
-// per row; lanes own D/32 consecutive columns.
-template <int D>
-__global__ void fwd_combine_kernel(const __nv_bfloat16* __restrict__ o_part,
-                                   const float* __restrict__ lse_part,
-                                   const int32_t* __restrict__ block_idx,
-                                   __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-                                   int64_t rows, int N, int H_kv, int G, int topk, int nb) {
-  constexpr int E = D / 32;
-  const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= rows * G) return;
-  const int64_t rkv = w / G;  // (b*H_kv + g)*N + i
-  const int h = (int)(w - rkv * G);
+// o[b,i,h] and lse[b,h,i] from the k partials of each (b, g, i) row.  One warp per
+// row: the partials of one slot are G*D contiguous bf16 (all heads of the group), read
+// as 16-byte chunks; the per-(slot, head) weights exp(lse_s - lse) come from shared
+// memory, computed by G lanes.
+template <int D, int G>
+__global__ void __launch_bounds__(256) fwd_combine_kernel(
+    const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
+    const int32_t* __restrict__ block_idx, __nv_bfloat16* __restrict__ o,
+    float* __restrict__ lse, int64_t rows, int N, int H_kv, int topk, int nb) {
+  constexpr int TC = G * D / 8;              // 16-byte chunks per slot
+  constexpr int CPL = (TC + 31) / 32;        // chunks per lane
+  __shared__ float wts[8][32 * G];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t rkv = (int64_t)blockIdx.x * 8 + wib;  // (b*H_kv + g)*N + i
+  if (rkv >= rows) return;
   const int i = (int)(rkv % N);
   const int64_t bg = rkv / N;
-  const int g = (int)(bg % H_kv), b = (int)(bg / H_kv);
+  const int g = (int)(bg % H_kv);
+  const int64_t b = bg / H_kv;
   const int32_t* sel = block_idx + rkv * topk;
-  float m = -INFINITY;
-  for (int s = 0; s < topk; ++s) {
-    const int c = __ldg(&sel[s]);
-    if (c >= 0 && c < nb) m = fmaxf(m, __ldg(&lse_part[(rkv * topk + s) * G + h]));
+  float* w = wts[wib];
+  if (lane < G) {
+    const int h = lane;
+    float m = -INFINITY;
+    for (int s = 0; s < topk; ++s) {
+      const int c = __ldg(&sel[s]);
+      if (c >= 0 && c < nb) m = fmaxf(m, __ldg(&lse_part[(rkv * topk + s) * G + h]));
+    }
+    float l = 0.f;
+    for (int s = 0; s < topk; ++s) {
+      const int c = __ldg(&sel[s]);
+      const float ls = (c >= 0 && c < nb) ? __ldg(&lse_part[(rkv * topk + s) * G + h]) : -INFINITY;
+      const float e = ls == -INFINITY ? 0.f : __expf(ls - m);
+      w[s * G + h] = e;
+      l += e;
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    for (int s = 0; s < topk; ++s) w[s * G + h] *= inv;
+    lse[(b * H_kv * G + g * G + h) * N + i] = m + logf(l);
   }
-  float acc[E];
+  __syncwarp();
+  float acc[CPL][8];
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float l = 0.f;
+  for (int x = 0; x < CPL; ++x)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[x][e] = 0.f;
   for (int s = 0; s < topk; ++s) {
     const int c = __ldg(&sel[s]);
-    if (c < 0 || c >= nb) continue;
-    const int64_t pr = (rkv * topk + s) * G + h;
-    const float ls = __ldg(&lse_part[pr]);
-    const float wgt = (ls == -INFINITY) ? 0.f : __expf(ls - m);
-    l += wgt;
-    const __nv_bfloat16* src = o_part + pr * D + lane * E;
-    if constexpr (E == 4) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(src);
-      const __nv_bfloat162 x0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-      const __nv_bfloat162 x1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-      acc[0] += wgt * __low2float(x0);
-      acc[1] += wgt * __high2float(x0);
-      acc[2] += wgt * __low2float(x1);
-      acc[3] += wgt * __high2float(x1);
-    } else {
+    if (c < 0 || c >= nb) continue;  // same for every lane
+    const uint4* src = reinterpret_cast<const uint4*>(o_part + (rkv * topk + s) * G * D);
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += wgt * __bfloat162float(src[e]);
+    for (int x = 0; x < CPL; ++x) {
+      const int ch = lane + 32 * x;
+      if (ch < TC) {
+        const float wt = w[s * G + (ch * 8) / D];
+        const uint4 raw = __ldg(&src[ch]);
+        const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[x][2 * e] += wt * __low2float(pr[e]);
+          acc[x][2 * e + 1] += wt * __high2float(pr[e]);
+        }
+      }
     }
   }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  const int hq = g * G + h;
-  __nv_bfloat16* dst = o + (((int64_t)b * N + i) * H_kv * G + hq) * D + lane * E;
+  uint4* dst = reinterpret_cast<uint4*>(o + ((b * N + i) * H_kv * G + (int64_t)g * G) * D);
 #pragma unroll
-  for (int e = 0; e < E; e += 2)
-    *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
-  if (lane == 0) lse[((int64_t)b * H_kv * G + hq) * N + i] = m + logf(l);
+  for (int x = 0; x < CPL; ++x) {
+    const int ch = lane + 32 * x;
+    if (ch < TC) {
+      uint4 out;
+      uint32_t* pw = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pw[e] = pack_bf16(acc[x][2 * e], acc[x][2 * e + 1]);
+      dst[ch] = out;
+    }
+  }
 }
 
 // lse_idx[b,g,i] = logsumexp over the row's valid slots of the partial lse.
@@ -325,23 +347,9 @@ cudaError_t launch_gather(const GatherParams& p, const Ctx& cx, cudaStream_t st)
   auto kern = gather_fwd_kernel<D, G, MAIN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
-  if (MAIN) kernel_event(MSA_KERNEL_FWD, true, st);
   kern<<<cx.num_sms, kFwdThreads, L::kBytes, st>>>(p);
-  if (MAIN) kernel_event(MSA_KERNEL_FWD, false, st);
   note_launch();
   return cudaGetLastError();
-}
-
-template <int D, bool MAIN>
-cudaError_t dispatch_g(int G, const GatherParams& p, const Ctx& cx, cudaStream_t st) {
-  switch (G) {
-    case 1: return launch_gather<D, 1, MAIN>(p, cx, st);
-    case 2: return launch_gather<D, 2, MAIN>(p, cx, st);
-    case 4: return launch_gather<D, 4, MAIN>(p, cx, st);
-    case 8: return launch_gather<D, 8, MAIN>(p, cx, st);
-    case 16: return launch_gather<D, 16, MAIN>(p, cx, st);
-  }
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -382,38 +390,31 @@ cudaError_t launch_attn_fwd(const Shape& s, const void* q, const void* k, const 
                             const int32_t* block_idx, const Plan& pl, __nv_bfloat16* o_part,
                             float* lse_part, void* o, float* lse, const Ctx& cx,
                             cudaStream_t st) {
-  GatherParams p{};
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k = static_cast<const __nv_bfloat16*>(k);
-  p.v = static_cast<const __nv_bfloat16*>(v);
-  p.off = pl.off;
-  p.toff = pl.toff;
-  p.entries = pl.entries;
-  p.o_part = o_part;
-  p.lse_part = lse_part;
-  p.keys = s.keys();
-  p.N = s.N;
-  p.H_kv = s.H_kv;
-  p.nb = s.nb;
-  p.topk = s.topk;
-  p.causal = s.causal;
-  p.q_tok_stride = s.H_q * s.d;
-  p.k_tok_stride = s.H_kv * s.d;
-  p.k_shared = 0;
-  p.scale_log2 = s.scale * 1.4426950408889634f;
-  cudaError_t e = s.d == 128 ? dispatch_g<128, true>(s.G, p, cx, st)
-                             : dispatch_g<64, true>(s.G, p, cx, st);
+  cudaError_t e = launch_attn_fwd_tc(s, q, k, v, pl, o_part, lse_part, cx, st);
   if (e != cudaSuccess) return e;
-  const int64_t warps = s.rows_kv() * s.G;
-  const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
-  if (s.d == 128)
-    fwd_combine_kernel<128><<<grid, 256, 0, st>>>(o_part, lse_part, block_idx,
-                                                  static_cast<__nv_bfloat16*>(o), lse,
-                                                  s.rows_kv(), s.N, s.H_kv, s.G, s.topk, s.nb);
-  else
-    fwd_combine_kernel<64><<<grid, 256, 0, st>>>(o_part, lse_part, block_idx,
-                                                 static_cast<__nv_bfloat16*>(o), lse,
-                                                 s.rows_kv(), s.N, s.H_kv, s.G, s.topk, s.nb);
+  const unsigned grid = (unsigned)((s.rows_kv() + 7) / 8);
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+#define MSA_COMBINE(DD, GG)                                                                 \
+  fwd_combine_kernel<DD, GG><<<grid, 256, 0, st>>>(o_part, lse_part, block_idx, ob, lse,     \
+                                                   s.rows_kv(), s.N, s.H_kv, s.topk, s.nb)
+  if (s.d == 128) {
+    switch (s.G) {
+      case 1: MSA_COMBINE(128, 1); break;
+      case 2: MSA_COMBINE(128, 2); break;
+      case 4: MSA_COMBINE(128, 4); break;
+      case 8: MSA_COMBINE(128, 8); break;
+      default: MSA_COMBINE(128, 16); break;
+    }
+  } else {
+    switch (s.G) {
+      case 1: MSA_COMBINE(64, 1); break;
+      case 2: MSA_COMBINE(64, 2); break;
+      case 4: MSA_COMBINE(64, 4); break;
+      case 8: MSA_COMBINE(64, 8); break;
+      default: MSA_COMBINE(64, 16); break;
+    }
+  }
+#undef MSA_COMBINE
   note_launch();
   return cudaGetLastError();
 }

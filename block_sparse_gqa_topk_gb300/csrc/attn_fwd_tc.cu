@@ -1,0 +1,473 @@
+// attn_fwd_tc.cu -- main-branch block-sparse forward on the 5th-generation tensor
+// cores (tcgen05 + TMEM), over the gathered tiles of plan.cu.
+//
+// Method: MSA summary (7minutos.es), "Cómo funcionan las dos ramas" ¶3 (exact
+// softmax attention of every head of a group over the causally visible tokens of
+// the group's blocks) and "El codiseño del kernel" (KV-outer query gather packing
+// queries x heads into one 128x128 score MMA, split + combine across CTAs);
+// Flash-MSA article (tech.kuratif.com) ¶6 (the LSE is kept for the backward).
+//
+// A tile is one key block c of one (batch, group) and 128 rows = 128/G gathered
+// queries x G heads.  Per CTA (persistent, a contiguous range of tiles):
+//   warps 4-7  loaders: gather the tile's q rows with cp.async into a 3-stage ring
+//              in the 128-byte-swizzled K-major layout tcgen05 reads; one thread
+//              TMA-loads K and V of the block when the key changes;
+//   warp 8     TMEM owner + one MMA thread: S = Q K^T (M=N=128, K=d) into a 2-deep
+//              TMEM ring, then O = P V with V as an MN-major operand;
+//   warps 0-3  softmax (thread = row = TMEM lane): tcgen05.ld S, causal mask, max,
+//              exp2, sum, P (bf16) into smem for the PV MMA; then tcgen05.ld O,
+//              normalise and store the bf16 partial and its lse.
+// Every wait is bounded; on expiry the CTA unwinds and records
+// MSA_ERR_DEVICE_TIMEOUT.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace msa {
+namespace {
+
+constexpr int kTcThreads = 288;  // 9 warps
+constexpr int kQStages = 3;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct FwdTcParams {
+  const __nv_bfloat16* q;
+  const int* off;
+  const int* toff;
+  const int* entries;
+  __nv_bfloat16* o_part;  // [(rkv*topk + slot)*G + h][D]
+  float* lse_part;        // [(rkv*topk + slot)*G + h]
+  int64_t keys;
+  int N, H_kv, nb, topk;
+  float scale_log2;
+  uint64_t wait_ns;
+  int* status;
+};
+
+template <int D>
+struct TcLayout {
+  static constexpr int kHalves = D / 64;        // 64-element (128-byte) column blocks
+  static constexpr int kHalf = 128 * 128;       // one [128 rows][64] bf16 block
+  static constexpr int kTile = kHalves * kHalf; // 128 x D bf16
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTile;
+  static constexpr int kQ = kV + kTile;                  // kQStages tiles
+  static constexpr int kP = kQ + kQStages * kTile;       // [128 rows][128 keys] bf16
+  static constexpr int kBar = kP + 2 * kHalf;
+  // barriers: kvfull, kvempty, qfull[3], qempty[3], sfull[2], ofull[2], tfree[2],
+  //           pfull, pempty, mmadone
+  static constexpr int kNumBars = 2 + 2 * kQStages + 6 + 3;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+// K-major tile split in 64-column blocks: element (r, k) of a [128][D] tile.
+template <int D>
+__device__ __forceinline__ uint32_t kmaj_off(int r, int chunk) {  // chunk = k / 8
+  return (uint32_t)((chunk >> 3) * (128 * 128) + r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
+}
+
+// Descriptor of an MN-major operand (contiguous along N) stored as [K rows][64-wide
+// column blocks] with the 128-byte swizzle: SBO = 1024 (8 K-rows), LBO = the stride
+// between 64-wide column blocks.
+__device__ __forceinline__ uint64_t umma_desc_mnmajor_sw128(uint32_t smem_addr, uint32_t lbo) {
+  return (uint64_t)((smem_addr & 0x3FFFF) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ int tc_find_key(const int* __restrict__ toff, int64_t keys, int t) {
+  int64_t lo = 0, hi = keys - 1;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) >> 1;
+    if (__ldg(&toff[mid]) <= t) lo = mid; else hi = mid - 1;
+  }
+  return (int)lo;
+}
+
+// Key of tile t given the key of an earlier tile of the same CTA (tiles are visited
+// in increasing order, so keys only move forward; empty keys are skipped).
+struct KeyCursor {
+  int key = -1;
+  __device__ __forceinline__ int at(const int* __restrict__ toff, int64_t keys, int t) {
+    if (key < 0) {
+      key = tc_find_key(toff, keys, t);
+    } else {
+      while (key + 1 < keys && __ldg(&toff[key + 1]) <= t) ++key;
+    }
+    return key;
+  }
+};
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const FwdTcParams p) {
+  using L = TcLayout<D>;
+  constexpr int QPT = 128 / G;
+  constexpr int CH = D / 8;  // 16-byte chunks per q row
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sK = smem + L::kK;
+  uint8_t* sV = smem + L::kV;
+  uint8_t* sQ = smem + L::kQ;
+  uint8_t* sP = smem + L::kP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* kvfull = bars;
+  uint64_t* kvempty = bars + 1;
+  uint64_t* qfull = bars + 2;
+  uint64_t* qempty = qfull + kQStages;
+  uint64_t* sfull = qempty + kQStages;
+  uint64_t* ofull = sfull + 2;
+  uint64_t* tfree = ofull + 2;
+  uint64_t* pfull = tfree + 2;
+  uint64_t* pempty = pfull + 1;
+  uint64_t* mmadone = pempty + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = __ldg(&p.toff[p.keys]);
+  const int per = (total + gridDim.x - 1) / gridDim.x;
+  const int t_begin = blockIdx.x * per;
+  const int t_end = min(total, t_begin + per);
+  const int n_tiles = max(0, t_end - t_begin);
+
+  if (threadIdx.x == 0) {
+    mbar_init(kvfull, 1);
+    mbar_init(kvempty, 1);
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(&qfull[s], 128);  // every loader thread
+      mbar_init(&qempty[s], 1);   // tcgen05.commit after the S MMA
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sfull[b], 1);
+      mbar_init(&ofull[b], 1);
+      mbar_init(&tfree[b], 4);  // one arrive per softmax warp
+    }
+    mbar_init(pfull, 4);
+    mbar_init(pempty, 1);
+    mbar_init(mmadone, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  // TMEM columns: S[b] at 128*b, O[b] at 256 + 128*b
+
+  if (n_tiles > 0) {
+    if (warp >= 4 && warp < 8) {
+      // ================================ loaders =================================
+      // Order per tile: gather q(u) -> publish q(u-1) -> (new block) swap K/V.  The
+      // swap waits for the previous block's last PV MMA, which needs q(u-1)
+      // published first.
+      const int lt = threadIdx.x - 128;  // 0..127
+      KeyCursor kc;
+      int prev_key = -1, kv_loads = 0, kv_issued = 0;
+      for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
+        const int t = t_begin + u;
+        const int st = u % kQStages;
+        const int key = kc.at(p.toff, p.keys, t);
+        const int bg = key / p.nb, c = key - bg * p.nb;
+        const int b = bg / p.H_kv, g = bg - b * p.H_kv;
+        const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * QPT;
+        const int ne = min(QPT, __ldg(&p.off[key + 1]) - e0);
+        if (!mbar_wait(&qempty[st], ((u / kQStages) & 1) ^ 1, p.wait_ns, abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* dq = sQ + st * L::kTile;
+        for (int x = lt; x < 128 * CH; x += 128) {
+          const int r = x / CH, ch = x % CH;
+          const int qi = r / G, h = r % G;
+          const bool ok = qi < ne;
+          const int i = ok ? (__ldg(&p.entries[e0 + qi]) >> 5) : 0;
+          const int64_t src = (((int64_t)b * p.N + i) * p.H_kv * G + g * G + h) * D + ch * 8;
+          cp_async_16(dq + kmaj_off<D>(r, ch), p.q + src, ok);
+        }
+        cp_async_commit();
+        if (u >= 1) {  // the previous tile's copies have landed: publish them
+          cp_async_wait<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(&qfull[(u - 1) % kQStages]);
+        }
+        if (key != prev_key) {
+          if (lt == 0) {
+            // the previous block's MMAs must be done with K/V before they are replaced
+            if (kv_loads > 0 && !mbar_wait(kvempty, (kv_loads - 1) & 1, p.wait_ns, abort_flag))
+              *abort_flag = 1;
+            if (!*abort_flag) {
+              mbar_arrive_expect_tx(kvfull, 2 * L::kTile);
+#pragma unroll
+              for (int h = 0; h < L::kHalves; ++h) {
+                tma_load_4d(sK + h * L::kHalf, &tm_k, kvfull, h * 64, g, c * 128, b);
+                tma_load_4d(sV + h * L::kHalf, &tm_v, kvfull, h * 64, g, c * 128, b);
+              }
+              kv_issued = kv_loads + 1;
+            }
+          }
+          ++kv_loads;
+          prev_key = key;
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      if (!*abort_flag) mbar_arrive(&qfull[(n_tiles - 1) % kQStages]);
+      // teardown: the last K/V TMA issued must have landed
+      if (lt == 0 && kv_issued > 0) mbar_wait(kvfull, (kv_issued - 1) & 1, 1000000000ull);
+    } else if (warp == 8) {
+      // ============================== MMA issuer ================================
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = umma_idesc_bf16_f32(128, 128);
+        constexpr uint32_t idesc_o = umma_idesc_bf16_f32(128, D) | (1u << 16);  // B MN-major
+        const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
+        int kv_uses = 0;
+        int cur_key = -1;
+        bool issued = false;
+        KeyCursor kc;
+        auto issue_s = [&](int u) -> bool {
+          const int st = u % kQStages, b = u & 1;
+          if (!mbar_wait(&qfull[st], (u / kQStages) & 1, p.wait_ns, abort_flag)) return false;
+          if (!mbar_wait(&tfree[b], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t aQ = smem_u32(sQ + st * L::kTile);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * L::kHalf + (kk & 3) * 32;
+            tc_mma_bf16(tmem + 128 * b, umma_desc_kmajor<128>(aQ + off),
+                        umma_desc_kmajor<128>(aK + off), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&qempty[st]);
+          tc_commit(&sfull[b]);
+          issued = true;
+          return true;
+        };
+        auto wait_kv = [&](int u) -> bool {
+          const int key = kc.at(p.toff, p.keys, t_begin + u);
+          if (key != cur_key) {
+            if (!mbar_wait(kvfull, kv_uses & 1, p.wait_ns, abort_flag)) return false;
+            ++kv_uses;
+            cur_key = key;
+          }
+          return true;
+        };
+        bool ok = wait_kv(0) && issue_s(0);
+        for (int u = 0; u < n_tiles && ok; ++u) {
+          const int b = u & 1;
+          const bool has_next = u + 1 < n_tiles;
+          KeyCursor peek = kc;
+          const bool next_same = has_next && peek.at(p.toff, p.keys, t_begin + u + 1) == cur_key;
+          if (next_same) ok = issue_s(u + 1);
+          if (!ok) break;
+          if (!mbar_wait(pfull, u & 1, p.wait_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step
+            const uint32_t pa = aP + (kk >> 2) * L::kHalf + (kk & 3) * 32;
+            const uint32_t vb = aV + kk * 2048;  // 16 K-rows = 2 swizzle atoms
+            tc_mma_bf16(tmem + 256 + 128 * b, umma_desc_kmajor<128>(pa),
+                        umma_desc_mnmajor_sw128(vb, L::kHalf), idesc_o, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(pempty);
+          tc_commit(&ofull[b]);
+          if (has_next && !next_same) {
+            tc_commit(kvempty);  // this block's K/V may be replaced
+            ok = wait_kv(u + 1) && issue_s(u + 1);
+          }
+        }
+        if (!ok) *abort_flag = 1;
+        if (issued) {
+          tc_commit(mmadone);
+          mbar_wait(mmadone, 0, 1000000000ull);
+        }
+      }
+    } else if (warp < 4) {
+      // ============================ softmax + epilogue =============================
+      const int row = threadIdx.x;  // TMEM lane
+      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+      KeyCursor kc;
+      for (int u = 0; u < n_tiles; ++u) {
+        const int t = t_begin + u;
+        const int b = u & 1;
+        const int key = kc.at(p.toff, p.keys, t);
+        const int bg = key / p.nb, c = key - bg * p.nb;
+        const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * QPT;
+        const int ne = min(QPT, __ldg(&p.off[key + 1]) - e0);
+        const int qi = row / G;
+        const int ent = qi < ne ? __ldg(&p.entries[e0 + qi]) : -1;
+        const int i = ent >> 5;
+        bool ok = __all_sync(0xffffffffu, mbar_wait(&sfull[b], (u >> 1) & 1, p.wait_ns, abort_flag));
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        float sv[128];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + 128 * b + 32 * h, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) sv[32 * h + x] = __uint_as_float(r[x]);
+        }
+        // causal mask j <= i (and j < N), scaled to log2 units
+        const int jlim = ent >= 0 ? min(i, p.N - 1) - c * 128 : -1;  // last valid column
+        float m = -INFINITY;
+#pragma unroll
+        for (int x = 0; x < 128; ++x) {
+          sv[x] = x <= jlim ? sv[x] * p.scale_log2 : -INFINITY;
+          m = fmaxf(m, sv[x]);
+        }
+        const float ms = m == -INFINITY ? 0.f : m;
+        float l = 0.f;
+#pragma unroll
+        for (int x = 0; x < 128; ++x) {
+          sv[x] = exp2f(sv[x] - ms);
+          l += sv[x];
+        }
+        // P (bf16) into the K-major smem operand, once the previous PV is done
+        ok = __all_sync(0xffffffffu, mbar_wait(pempty, (u & 1) ^ 1, p.wait_ns, abort_flag));
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) {
+          uint4 w;
+          w.x = pack_bf16(sv[8 * ch + 0], sv[8 * ch + 1]);
+          w.y = pack_bf16(sv[8 * ch + 2], sv[8 * ch + 3]);
+          w.z = pack_bf16(sv[8 * ch + 4], sv[8 * ch + 5]);
+          w.w = pack_bf16(sv[8 * ch + 6], sv[8 * ch + 7]);
+          *reinterpret_cast<uint4*>(sP + kmaj_off<128>(row, ch)) = w;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pfull);
+        // ---- epilogue: O row / l -> bf16 partial, lse partial ----
+        ok = __all_sync(0xffffffffu, mbar_wait(&ofull[b], (u >> 1) & 1, p.wait_ns, abort_flag));
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* dst = nullptr;
+        if (ent >= 0) {
+          const int64_t prow = ((((int64_t)bg * p.N + i) * p.topk + (ent & 31)) * G + row % G);
+          dst = p.o_part + prow * D;
+          p.lse_part[prow] = l > 0.f ? (ms + log2f(l)) * kLn2 : -INFINITY;
+        }
+#pragma unroll
+        for (int h = 0; h < D / 32; ++h) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + 256 + 128 * b + 32 * h, r);
+          tmem_wait_ld();
+          if (dst) {
+#pragma unroll
+            for (int x = 0; x < 32; x += 8) {
+              uint4 w;
+              w.x = pack_bf16(__uint_as_float(r[x + 0]) * inv, __uint_as_float(r[x + 1]) * inv);
+              w.y = pack_bf16(__uint_as_float(r[x + 2]) * inv, __uint_as_float(r[x + 3]) * inv);
+              w.z = pack_bf16(__uint_as_float(r[x + 4]) * inv, __uint_as_float(r[x + 5]) * inv);
+              w.w = pack_bf16(__uint_as_float(r[x + 6]) * inv, __uint_as_float(r[x + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + 32 * h + x) = w;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tfree[b]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) set_status(p.status, MSA_ERR_DEVICE_TIMEOUT);
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_fwd_tc_dg(const FwdTcParams& prm, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const Ctx& cx, cudaStream_t st) {
+  using L = TcLayout<D>;
+  auto kern = fwd_tc_kernel<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  kernel_event(MSA_KERNEL_FWD, true, st);
+  kern<<<cx.num_sms, kTcThreads, L::kAlloc, st>>>(tk, tv, prm);
+  kernel_event(MSA_KERNEL_FWD, false, st);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_tc_d(int G, const FwdTcParams& prm, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const Ctx& cx, cudaStream_t st) {
+  switch (G) {
+    case 1: return launch_fwd_tc_dg<D, 1>(prm, tk, tv, cx, st);
+    case 2: return launch_fwd_tc_dg<D, 2>(prm, tk, tv, cx, st);
+    case 4: return launch_fwd_tc_dg<D, 4>(prm, tk, tv, cx, st);
+    case 8: return launch_fwd_tc_dg<D, 8>(prm, tk, tv, cx, st);
+    case 16: return launch_fwd_tc_dg<D, 16>(prm, tk, tv, cx, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd_tc(const Shape& s, const void* q, const void* k, const void* v,
+                               const Plan& pl, __nv_bfloat16* o_part, float* lse_part,
+                               const Ctx& cx, cudaStream_t st) {
+  CUtensorMap tk, tv;
+  const uint64_t dims[4] = {(uint64_t)s.d, (uint64_t)s.H_kv, (uint64_t)s.N, (uint64_t)s.B};
+  const uint64_t strides[3] = {(uint64_t)s.d * 2, (uint64_t)s.H_kv * s.d * 2,
+                               (uint64_t)s.N * s.H_kv * s.d * 2};
+  const uint32_t box[4] = {64, 1, 128, 1};
+  if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  FwdTcParams prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.off = pl.off;
+  prm.toff = pl.toff;
+  prm.entries = pl.entries;
+  prm.o_part = o_part;
+  prm.lse_part = lse_part;
+  prm.keys = s.keys();
+  prm.N = s.N;
+  prm.H_kv = s.H_kv;
+  prm.nb = s.nb;
+  prm.topk = s.topk;
+  prm.scale_log2 = s.scale * kLog2e;
+  prm.wait_ns = cx.wait_ns;
+  prm.status = cx.status;
+  if (s.d == 128) return launch_fwd_tc_d<128>(s.G, prm, tk, tv, cx, st);
+  return launch_fwd_tc_d<64>(s.G, prm, tk, tv, cx, st);
+}
+
+}  // namespace msa

@@ -60,6 +60,11 @@ cudaError_t launch_attn_fwd(const Shape& s, const void* q, const void* k, const 
                             float* lse_part, void* o, float* lse, const Ctx& cx,
                             cudaStream_t st);
 
+// tcgen05 gathered forward kernel (partials only; launch_attn_fwd adds the combine).
+cudaError_t launch_attn_fwd_tc(const Shape& s, const void* q, const void* k, const void* v,
+                               const Plan& pl, __nv_bfloat16* o_part, float* lse_part,
+                               const Ctx& cx, cudaStream_t st);
+
 // Backward pieces.
 struct BwdBufs {
   float* D;          // [B][H_q][N]

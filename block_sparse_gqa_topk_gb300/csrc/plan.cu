@@ -7,7 +7,7 @@
 // the MoBA-style varlen view of Flash-MSA (tech.kuratif.com ¶7, deephorus.pages.dev
 // ¶4) and fmha_sm100's KV-outer query gather (7minutos.es, "El codiseño del
 // kernel", second idea).  This file builds the lists from block_idx:
-//   count  -> per-list sizes (one atomic per selected block),
+//   count  -> per-list sizes (shared-memory histograms per row chunk),
 //   scan   -> CSR offsets and tile offsets (one CTA, decoupled chunks),
 //   fill   -> (query << 5 | slot) entries.
 // HBM-bound integer work: block_idx is read twice, entries written once.
@@ -116,6 +116,70 @@ __global__ void plan_fill_kernel(const int32_t* __restrict__ block_idx, int64_t 
   entries[pos] = (i << 5) | slot;
 }
 
+// Shared-memory variants: one CTA takes kRowsPerCta consecutive rows of one
+// (b, g), histograms their block ids in shared memory and touches global memory
+// once per non-empty bin (count) or reserves one range per bin (fill), instead of
+// one global atomic per entry.  Used when the nb-bin histogram fits in smem.
+constexpr int kRowsPerCta = 1024;
+constexpr int kSmemBins = 16384;
+
+__global__ void plan_count_smem_kernel(const int32_t* __restrict__ block_idx, int N, int topk,
+                                       int nb, int* __restrict__ cnt, int* status) {
+  extern __shared__ int hist[];
+  const int chunks = (N + kRowsPerCta - 1) / kRowsPerCta;
+  const int64_t bg = blockIdx.x / chunks;
+  const int i0 = (blockIdx.x % chunks) * kRowsPerCta;
+  const int i1 = min(N, i0 + kRowsPerCta);
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) hist[c] = 0;
+  __syncthreads();
+  const int32_t* src = block_idx + (bg * N + i0) * topk;
+  const int n = (i1 - i0) * topk;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int c = __ldg(&src[e]);
+    if (c < 0) continue;
+    if (c >= nb) {
+      set_status(status, MSA_ERR_ARG);
+      continue;
+    }
+    atomicAdd(&hist[c], 1);
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < nb; c += blockDim.x)
+    if (hist[c]) atomicAdd(&cnt[bg * nb + c], hist[c]);
+}
+
+__global__ void plan_fill_smem_kernel(const int32_t* __restrict__ block_idx, int N, int topk,
+                                      int nb, const int* __restrict__ off,
+                                      int* __restrict__ cursor, int* __restrict__ entries) {
+  extern __shared__ int hist[];
+  const int chunks = (N + kRowsPerCta - 1) / kRowsPerCta;
+  const int64_t bg = blockIdx.x / chunks;
+  const int i0 = (blockIdx.x % chunks) * kRowsPerCta;
+  const int i1 = min(N, i0 + kRowsPerCta);
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) hist[c] = 0;
+  __syncthreads();
+  const int32_t* src = block_idx + (bg * N + i0) * topk;
+  const int n = (i1 - i0) * topk;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int c = __ldg(&src[e]);
+    if (c >= 0 && c < nb) atomicAdd(&hist[c], 1);
+  }
+  __syncthreads();
+  // reserve one range per non-empty bin; the bin becomes this CTA's write cursor
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+    const int h = hist[c];
+    if (h) hist[c] = off[bg * nb + c] + atomicAdd(&cursor[bg * nb + c], h);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int c = __ldg(&src[e]);
+    if (c < 0 || c >= nb) continue;
+    const int q = e / topk;
+    const int pos = atomicAdd(&hist[c], 1);
+    entries[pos] = ((i0 + q) << 5) | (e - q * topk);
+  }
+}
+
 }  // namespace
 
 size_t plan_bytes(const Shape& s) {
@@ -145,7 +209,22 @@ cudaError_t launch_plan(const Shape& s, const int32_t* block_idx, int qpt, const
   cudaError_t e = cudaMemsetAsync(pl.cnt, 0, (size_t)keys * 4, st);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((n + 255) / 256);
-  if (n > 0) {
+  const bool smem_bins = s.nb <= kSmemBins;
+  const int64_t chunks = (s.N + kRowsPerCta - 1) / kRowsPerCta;
+  const unsigned grid_s = (unsigned)((int64_t)s.B * s.H_kv * chunks);
+  const size_t hist_bytes = (size_t)s.nb * sizeof(int);
+  if (n > 0 && smem_bins) {
+    if (hist_bytes > 48 * 1024) {
+      cudaFuncSetAttribute(plan_count_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)hist_bytes);
+      cudaFuncSetAttribute(plan_fill_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)hist_bytes);
+    }
+    plan_count_smem_kernel<<<grid_s, 512, hist_bytes, st>>>(block_idx, s.N, s.topk, s.nb,
+                                                            pl.cnt, cx.status);
+    note_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else if (n > 0) {
     plan_count_kernel<<<grid, 256, 0, st>>>(block_idx, s.rows_kv(), s.topk, s.N, s.nb, pl.cnt,
                                             cx.status);
     note_launch();
@@ -154,7 +233,12 @@ cudaError_t launch_plan(const Shape& s, const int32_t* block_idx, int qpt, const
   plan_scan_kernel<<<1, 1024, 0, st>>>(pl.cnt, pl.off, pl.toff, keys, qpt);
   note_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (n > 0) {
+  if (n > 0 && smem_bins) {
+    plan_fill_smem_kernel<<<grid_s, 512, hist_bytes, st>>>(block_idx, s.N, s.topk, s.nb, pl.off,
+                                                           pl.cnt, pl.entries);
+    note_launch();
+    e = cudaGetLastError();
+  } else if (n > 0) {
     plan_fill_kernel<<<grid, 256, 0, st>>>(block_idx, s.rows_kv(), s.topk, s.N, s.nb, pl.off,
                                            pl.cnt, pl.entries);
     note_launch();
