@@ -191,11 +191,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         uint8_t* dq = sQ + st * L::kTile;
+        // the tile's entries, loaded once per warp: lane l holds query slots l + 32 m
+        constexpr int NE = (QPT + 31) / 32;
+        int my_ent[NE];
+#pragma unroll
+        for (int m = 0; m < NE; ++m) {
+          const int qs = lane + 32 * m;
+          my_ent[m] = qs < ne ? __ldg(&p.entries[e0 + qs]) : -1;
+        }
         for (int x = lt; x < 128 * CH; x += 128) {
           const int r = x / CH, ch = x % CH;
           const int qi = r / G, h = r % G;
-          const bool ok = qi < ne;
-          const int i = ok ? (__ldg(&p.entries[e0 + qi]) >> 5) : 0;
+          int ent = -1;
+#pragma unroll
+          for (int m = 0; m < NE; ++m) {
+            const int v = __shfl_sync(0xffffffffu, my_ent[m], qi & 31);
+            if ((qi >> 5) == m) ent = v;
+          }
+          const bool ok = ent >= 0;
+          const int i = ok ? (ent >> 5) : 0;
           const int64_t src = (((int64_t)b * p.N + i) * p.H_kv * G + g * G + h) * D + ch * 8;
           cp_async_16(dq + kmaj_off<D>(r, ch), p.q + src, ok);
         }

@@ -73,10 +73,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // try_wait suspends the thread for a while before failing; poll the abort flag
+    // and the clock only every few attempts so waiting warps stay off the issue slots
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (abort && *abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// Named barrier among `count` threads (multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -65,6 +65,14 @@ cudaError_t launch_attn_fwd_tc(const Shape& s, const void* q, const void* k, con
                                const Plan& pl, __nv_bfloat16* o_part, float* lse_part,
                                const Ctx& cx, cudaStream_t st);
 
+// tcgen05 fused backward tile kernel (dk, dv written; dq, dq_idx, dk_idx as partials).
+cudaError_t launch_attn_bwd_tc(const Shape& s, const void* q, const void* k, const void* v,
+                               const void* dO, const float* lse, const float* Dv,
+                               const void* q_idx, const void* k_idx, const float* lse_idx,
+                               float kl_weight, const Plan& pl, __nv_bfloat16* dq_part,
+                               __nv_bfloat16* dqi_part, float* dki_part, double* kl_acc, void* dk,
+                               void* dv, const Ctx& cx, cudaStream_t st);
+
 // Backward pieces.
 struct BwdBufs {
   float* D;          // [B][H_q][N]
