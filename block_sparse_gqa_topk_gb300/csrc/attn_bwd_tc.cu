@@ -68,21 +68,23 @@ struct BL {
   static constexpr int kSQ = 0;
   static constexpr int kSdO = kSQ + (D / 64) * kQH;
   static constexpr int kSQi = kSdO + (D / 64) * kQH;  // [16][64]
-  static constexpr int kSLse = kSQi + 16 * 128;       // float[64] lse*log2e
+  static constexpr int kSLse = kSQi + 16 * 128;       // float[64] lse (natural log)
   static constexpr int kSD = kSLse + 64 * 4;          // float[64] D
   static constexpr int kSRi = kSD + 64 * 4;           // int[64] query index of the row, -1 pad
   static constexpr int kSRp = kSRi + 64 * 4;          // int[64] dq partial row, -1 pad
   static constexpr int kSQiq = kSRp + 64 * 4;         // int[16] query index of the slot, -1 pad
   static constexpr int kSQp = kSQiq + 16 * 4;         // int[16] dq_idx partial row, -1 pad
-  static constexpr int kSLi = kSQp + 16 * 4;          // float[16] lse_idx*log2e
+  static constexpr int kSLi = kSQp + 16 * 4;          // float[16] lse_idx (natural log)
   static constexpr int kStage = ((kSLi + 16 * 4) + 1023) & ~1023;
   static constexpr int kStages0 = kKi + kKH;
   static constexpr int kPT = kStages0 + 2 * kStage;   // P^T [128][64] bf16 (SW128)
   static constexpr int kdST = kPT + 128 * 128;        // dS^T [128][64]
   static constexpr int kTeach = kdST + 128 * 128;     // p_T float [128][17] (padded rows)
   static constexpr int kDZ = kTeach + 128 * 17 * 4;   // dz bf16 [128][16] (32-byte rows)
-  static constexpr int kBar = kDZ + 128 * 32;
-  static constexpr int kNumBars = 16;
+  static constexpr int kStg = kDZ + 128 * 32;        // dQ staging [2][32 rows][272 B]
+  static constexpr int kStgRow = 2 * D + 16;
+  static constexpr int kBar = kStg + 2 * 32 * kStgRow;
+  static constexpr int kNumBars = 18;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* mmadone = bar + 12;
   uint64_t* e_sync1 = bar + 13;  // every epilogue warp has written its teacher rows
   uint64_t* e_sync2 = bar + 14;  // every epilogue warp has written its dz rows
+  uint64_t* e_stg = bar + 15;    // [2] a warpgroup's dQ rows are staged (bars 15, 16)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
 
@@ -155,6 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(mmadone, 1);
     mbar_init(e_sync1, kEpiWarps);
     mbar_init(e_sync2, kEpiWarps);
+    mbar_init(&e_stg[0], 4);
+    mbar_init(&e_stg[1], 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -171,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================= loaders ==================================
     const int lt = threadIdx.x - 256;  // 0..63
     int u = 0, nkeys = 0, kv_issued = 0;  // nkeys: blocks with at least one chunk
+    int next_ent = -1;
     for (int64_t kk = blockIdx.x; kk < p.keys && !*abort_flag; kk += gridDim.x) {
       const int c = (int)(kk / BG), bg = (int)(kk % BG);
       const int b = bg / p.H_kv, g = bg - b * p.H_kv;
@@ -216,8 +222,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = sm + L::kStages0 + s * L::kStage;
         const int q0 = e_begin + ch * QC;
         const int nq = min(QC, e_end - q0);
-        // the chunk's entries, once per warp (lane q holds query slot q)
-        const int my_ent = lane < nq ? __ldg(&p.entries[q0 + lane]) : -1;
+        // this chunk's entries (prefetched one chunk ahead), lane q = query slot q
+        const int my_ent = ch == 0 ? (lane < nq ? __ldg(&p.entries[q0 + lane]) : -1) : next_ent;
+        {
+          const int q1 = q0 + QC;
+          const int nq1 = min(QC, e_end - q1);
+          next_ent = (ch + 1 < nch && lane < nq1) ? __ldg(&p.entries[q1 + lane]) : -1;
+        }
         for (int x = lt; x < kRows * (D / 8); x += kLoadThreads) {
           const int r = x / (D / 8), cc = x % (D / 8);
           const int qi = r / G, h = r % G;
@@ -240,26 +251,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           const int r = lt, qi = r / G, h = r % G;  // one row per loader thread
           const int ent = __shfl_sync(0xffffffffu, my_ent, qi);
-          float l2 = 0.f, dd = 0.f;
-          int ri = -1, rp = -1;
-          if (ent >= 0) {
-            const int64_t x = ((int64_t)b * p.H_kv * G + g * G + h) * p.N + (ent >> 5);
-            l2 = __ldg(&p.lse[x]) * kLog2e;
-            dd = __ldg(&p.Dv[x]);
-            ri = ent >> 5;
-            rp = (int)((((int64_t)bg * p.N + ri) * p.topk + (ent & 31)) * G + h);
-          }
-          reinterpret_cast<float*>(st + L::kSLse)[r] = l2;
-          reinterpret_cast<float*>(st + L::kSD)[r] = dd;
+          const bool ok = ent >= 0;
+          const int ri = ok ? (ent >> 5) : -1;
+          const int64_t x = ((int64_t)b * p.H_kv * G + g * G + h) * p.N + (ok ? ri : 0);
+          cp_async_4(st + L::kSLse + 4 * r, p.lse + x, ok);
+          cp_async_4(st + L::kSD + 4 * r, p.Dv + x, ok);
           reinterpret_cast<int*>(st + L::kSRi)[r] = ri;
-          reinterpret_cast<int*>(st + L::kSRp)[r] = rp;
+          reinterpret_cast<int*>(st + L::kSRp)[r] =
+              ok ? (int)((((int64_t)bg * p.N + ri) * p.topk + (ent & 31)) * G + h) : -1;
           if (lt < kQS) {
-            const bool ok = my_ent >= 0;
-            reinterpret_cast<int*>(st + L::kSQiq)[lt] = ok ? (my_ent >> 5) : -1;
+            const bool okq = my_ent >= 0;
+            const int iq = okq ? (my_ent >> 5) : 0;
+            reinterpret_cast<int*>(st + L::kSQiq)[lt] = okq ? iq : -1;
             reinterpret_cast<int*>(st + L::kSQp)[lt] =
-                ok ? (int)(((int64_t)bg * p.N + (my_ent >> 5)) * p.topk + (my_ent & 31)) : -1;
-            reinterpret_cast<float*>(st + L::kSLi)[lt] =
-                ok ? __ldg(&p.lse_idx[(int64_t)bg * p.N + (my_ent >> 5)]) * kLog2e : 0.f;
+                okq ? (int)(((int64_t)bg * p.N + iq) * p.topk + (my_ent & 31)) : -1;
+            cp_async_4(st + L::kSLi + 4 * lt, p.lse_idx + (int64_t)bg * p.N + iq, okq);
           }
         }
         cp_async_commit();
@@ -389,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 2; ++e) {
               const int r = 32 * wg + x + e;
               const bool valid = j <= s_ri[r];  // s_ri = -1 for padding rows
-              const float v = valid ? exp2f(__uint_as_float(a[x + e]) * p.scale_log2 - s_lse[r]) : 0.f;
+              const float v =
+                  valid ? ex2_fast(__uint_as_float(a[x + e]) * p.scale_log2 - s_lse[r] * kLog2e) : 0.f;
               pv[e] = v;
               dv2[e] = v * (__uint_as_float(d2[x + e]) - s_D[r]);
               pt[(x + e) / G] += v;
@@ -443,10 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int qs = n * 8 + (lane & 3) * 2 + (e & 1);
               const int kloc = kl0 + ((e >> 1) << 3);
               const bool valid = c * 128 + kloc <= s_qi[qs];  // s_qi = -1 for padding
-              const float zl2 = zt[n][e] * p.sidx_log2 - s_li[qs];  // log2 p_I
-              const float pI = valid ? exp2f(zl2) : 0.f;
+              const float zl2 = zt[n][e] * p.sidx_log2 - s_li[qs] * kLog2e;  // log2 p_I
+              const float pI = valid ? ex2_fast(zl2) : 0.f;
               const float pT = sTeach[kloc * kTS + qs];
-              if (valid && pT > 0.f) klc += pT * (log2f(pT) - zl2);
+              if (valid && pT > 0.f) klc += pT * (__log2f(pT) - zl2);
               zt[n][e] = valid ? p.w * (pI - pT) : 0.f;  // dz
             }
             *reinterpret_cast<uint32_t*>(sDZ + swz32(kl0, n) + (lane & 3) * 4) =
@@ -509,10 +516,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t a[32];
           tmem_ld_32x32b_x32(tmem + lb + cDQT + 32 * wg, a);
           tmem_wait_ld();
+          // stage the warpgroup's 32 rows (row-major, padded) so the global stores
+          // below write whole 256-byte partial rows; lanes (2m, 2m+1) swap one value
+          // so each stores a bf16 pair
+          uint8_t* stg = sm + L::kStg + wg * 32 * L::kStgRow;
+          const bool odd = lane & 1;
+          const int dcol = tl & ~1;
 #pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const int rp = s_rp[32 * wg + x];
-            if (rp >= 0) p.dq_part[(int64_t)rp * D + tl] = __float2bfloat16(__uint_as_float(a[x]) * p.scale);
+          for (int x = 0; x < 32; x += 2) {
+            const float v0 = __uint_as_float(a[x]) * p.scale;
+            const float v1 = __uint_as_float(a[x + 1]) * p.scale;
+            const float mine = odd ? v1 : v0;
+            const float give = odd ? v0 : v1;
+            const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+            *reinterpret_cast<uint32_t*>(stg + (x + (odd ? 1 : 0)) * L::kStgRow + dcol * 2) =
+                odd ? pack_bf16(got, mine) : pack_bf16(mine, got);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&e_stg[wg]);
+        ok = __all_sync(0xffffffffu, mbar_wait(&e_stg[wg], u & 1, p.wait_ns, abort_flag));
+        if (!ok) break;
+        {
+          const uint8_t* stg = sm + L::kStg + wg * 32 * L::kStgRow;
+          const int wt = (warp & 3) * 32 + lane;  // 0..127 within the warpgroup
+          constexpr int CPR = D / 8;              // 16-byte chunks per row
+#pragma unroll
+          for (int x = wt; x < 32 * CPR; x += 128) {
+            const int r = x / CPR, cc = x % CPR;
+            const int rp = s_rp[32 * wg + r];
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + r * L::kStgRow + cc * 16);
+            if (rp >= 0) *reinterpret_cast<uint4*>(p.dq_part + (int64_t)rp * D + cc * 8) = v;
           }
         }
         tc_fence_before();

@@ -28,7 +28,8 @@
 namespace msa {
 namespace {
 
-constexpr int kTcThreads = 288;  // 9 warps
+constexpr int kTcThreads = 416;  // 13 warps: 8 softmax, 4 loaders, 1 MMA
+constexpr int kLoadThreads = 128;
 constexpr int kQStages = 3;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -55,11 +56,11 @@ struct TcLayout {
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;                  // kQStages tiles
-  static constexpr int kP = kQ + kQStages * kTile;       // [128 rows][128 keys] bf16
-  static constexpr int kBar = kP + 2 * kHalf;
+  static constexpr int kP = kQ + kQStages * kTile;       // [2][128 rows][128 keys] bf16
+  static constexpr int kBar = kP + 2 * 2 * kHalf;
   // barriers: kvfull, kvempty, qfull[3], qempty[3], sfull[2], ofull[2], tfree[2],
-  //           pfull, pempty, mmadone
-  static constexpr int kNumBars = 2 + 2 * kQStages + 6 + 3;
+  //           pfull[2], pempty[2], mmadone
+  static constexpr int kNumBars = 2 + 2 * kQStages + 6 + 5;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -102,6 +103,11 @@ struct KeyCursor {
   }
 };
 
+// Byte offset of 16-byte chunk `chunk` of row r in rows of 128 bytes, swizzled.
+__device__ __forceinline__ uint32_t sw128_row(int r, int chunk) {
+  return (uint32_t)(r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -128,9 +134,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* sfull = qempty + kQStages;
   uint64_t* ofull = sfull + 2;
   uint64_t* tfree = ofull + 2;
-  uint64_t* pfull = tfree + 2;
-  uint64_t* pempty = pfull + 1;
-  uint64_t* mmadone = pempty + 1;
+  uint64_t* pfull = tfree + 2;   // [2]
+  uint64_t* pempty = pfull + 2;  // [2]
+  uint64_t* mmadone = pempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -145,7 +151,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(kvfull, 1);
     mbar_init(kvempty, 1);
     for (int s = 0; s < kQStages; ++s) {
-      mbar_init(&qfull[s], 128);  // every loader thread
+      mbar_init(&qfull[s], kLoadThreads);  // every loader thread
       mbar_init(&qempty[s], 1);   // tcgen05.commit after the S MMA
     }
     for (int b = 0; b < 2; ++b) {
@@ -153,13 +159,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&ofull[b], 1);
       mbar_init(&tfree[b], 4);  // one arrive per softmax warp
     }
-    mbar_init(pfull, 4);
-    mbar_init(pempty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&pfull[b], 4);
+      mbar_init(&pempty[b], 1);
+    }
     mbar_init(mmadone, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == 12) {
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
   }
@@ -170,12 +178,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // TMEM columns: S[b] at 128*b, O[b] at 256 + 128*b
 
   if (n_tiles > 0) {
-    if (warp >= 4 && warp < 8) {
+    if (warp >= 8 && warp < 12) {
       // ================================ loaders =================================
       // Order per tile: gather q(u) -> publish q(u-1) -> (new block) swap K/V.  The
       // swap waits for the previous block's last PV MMA, which needs q(u-1)
       // published first.
-      const int lt = threadIdx.x - 128;  // 0..127
+      const int lt = threadIdx.x - 256;  // 0..63
       KeyCursor kc;
       int prev_key = -1, kv_loads = 0, kv_issued = 0;
       for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
@@ -199,7 +207,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int qs = lane + 32 * m;
           my_ent[m] = qs < ne ? __ldg(&p.entries[e0 + qs]) : -1;
         }
-        for (int x = lt; x < 128 * CH; x += 128) {
+        for (int x = lt; x < 128 * CH; x += kLoadThreads) {
           const int r = x / CH, ch = x % CH;
           const int qi = r / G, h = r % G;
           int ent = -1;
@@ -243,7 +251,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!*abort_flag) mbar_arrive(&qfull[(n_tiles - 1) % kQStages]);
       // teardown: the last K/V TMA issued must have landed
       if (lt == 0 && kv_issued > 0) mbar_wait(kvfull, (kv_issued - 1) & 1, 1000000000ull);
-    } else if (warp == 8) {
+    } else if (warp == 12) {
       // ============================== MMA issuer ================================
       if (lane == 0) {
         constexpr uint32_t idesc_s = umma_idesc_bf16_f32(128, 128);
@@ -287,19 +295,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const bool next_same = has_next && peek.at(p.toff, p.keys, t_begin + u + 1) == cur_key;
           if (next_same) ok = issue_s(u + 1);
           if (!ok) break;
-          if (!mbar_wait(pfull, u & 1, p.wait_ns, abort_flag)) {
+          if (!mbar_wait(&pfull[b], (u >> 1) & 1, p.wait_ns, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step
-            const uint32_t pa = aP + (kk >> 2) * L::kHalf + (kk & 3) * 32;
+            const uint32_t pa = aP + b * 2 * L::kHalf + (kk >> 2) * L::kHalf + (kk & 3) * 32;
             const uint32_t vb = aV + kk * 2048;  // 16 K-rows = 2 swizzle atoms
             tc_mma_bf16(tmem + 256 + 128 * b, umma_desc_kmajor<128>(pa),
                         umma_desc_mnmajor_sw128(vb, L::kHalf), idesc_o, kk > 0 ? 1u : 0u);
           }
-          tc_commit(pempty);
+          tc_commit(&pempty[b]);
           tc_commit(&ofull[b]);
           if (has_next && !next_same) {
             tc_commit(kvempty);  // this block's K/V may be replaced
@@ -312,14 +320,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_wait(mmadone, 0, 1000000000ull);
         }
       }
-    } else if (warp < 4) {
-      // ============================ softmax + epilogue =============================
-      const int row = threadIdx.x;  // TMEM lane
-      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    } else {
+      // ====================== softmax + epilogue: warps 0-7 =======================
+      // Warpgroup wg handles the tiles u with u % 2 == wg, i.e. TMEM buffer wg and
+      // P tile wg, so the two groups' softmax and epilogues overlap.
+      const int wg = warp >> 2;
+      const int row = (warp & 3) * 32 + lane;  // TMEM lane
+      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+      uint8_t* sPw = sP + wg * 2 * L::kHalf;
       KeyCursor kc;
-      for (int u = 0; u < n_tiles; ++u) {
+      for (int u = wg; u < n_tiles; u += 2) {
         const int t = t_begin + u;
-        const int b = u & 1;
+        const int b = wg;
         const int key = kc.at(p.toff, p.keys, t);
         const int bg = key / p.nb, c = key - bg * p.nb;
         const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * QPT;
@@ -333,49 +345,66 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        float sv[128];
+        // causal mask j <= i (and j < N), scaled to log2 units; two passes over the
+        // TMEM row (max, then exp/sum/pack), 32 columns at a time
+        const int jlim = ent >= 0 ? min(i, p.N - 1) - c * 128 : -1;  // last valid column
+        // blocks wholly before every query of the warp need no mask (the usual case)
+        const bool full = __all_sync(0xffffffffu, jlim >= 127);
+        float m = -INFINITY;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tmem + lane_base + 128 * b + 32 * h, r);
           tmem_wait_ld();
+          if (full) {
 #pragma unroll
-          for (int x = 0; x < 32; ++x) sv[32 * h + x] = __uint_as_float(r[x]);
-        }
-        // causal mask j <= i (and j < N), scaled to log2 units
-        const int jlim = ent >= 0 ? min(i, p.N - 1) - c * 128 : -1;  // last valid column
-        float m = -INFINITY;
+            for (int x = 0; x < 32; x += 2)
+              m = fmax3(m, __uint_as_float(r[x]), __uint_as_float(r[x + 1]));
+          } else {
 #pragma unroll
-        for (int x = 0; x < 128; ++x) {
-          sv[x] = x <= jlim ? sv[x] * p.scale_log2 : -INFINITY;
-          m = fmaxf(m, sv[x]);
+            for (int x = 0; x < 32; x += 2)
+              m = fmax3(m, 32 * h + x <= jlim ? __uint_as_float(r[x]) : -INFINITY,
+                        32 * h + x + 1 <= jlim ? __uint_as_float(r[x + 1]) : -INFINITY);
+          }
         }
-        const float ms = m == -INFINITY ? 0.f : m;
-        float l = 0.f;
-#pragma unroll
-        for (int x = 0; x < 128; ++x) {
-          sv[x] = exp2f(sv[x] - ms);
-          l += sv[x];
-        }
-        // P (bf16) into the K-major smem operand, once the previous PV is done
-        ok = __all_sync(0xffffffffu, mbar_wait(pempty, (u & 1) ^ 1, p.wait_ns, abort_flag));
+        const float ms = m == -INFINITY ? 0.f : m * p.scale_log2;
+        // P (bf16) into this group's K-major smem operand, once its previous PV is done
+        ok = __all_sync(0xffffffffu, mbar_wait(&pempty[b], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag));
         if (!ok) {
           *abort_flag = 1;
           break;
         }
+        float l = 0.f;
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          uint4 w;
-          w.x = pack_bf16(sv[8 * ch + 0], sv[8 * ch + 1]);
-          w.y = pack_bf16(sv[8 * ch + 2], sv[8 * ch + 3]);
-          w.z = pack_bf16(sv[8 * ch + 4], sv[8 * ch + 5]);
-          w.w = pack_bf16(sv[8 * ch + 6], sv[8 * ch + 7]);
-          *reinterpret_cast<uint4*>(sP + kmaj_off<128>(row, ch)) = w;
+        for (int h = 0; h < 4; ++h) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + 128 * b + 32 * h, r);
+          tmem_wait_ld();
+          float e[32];
+          if (full) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) e[x] = ex2_fast(__uint_as_float(r[x]) * p.scale_log2 - ms);
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+              e[x] = 32 * h + x <= jlim ? ex2_fast(__uint_as_float(r[x]) * p.scale_log2 - ms) : 0.f;
+          }
+#pragma unroll
+          for (int x = 0; x < 32; ++x) l += e[x];
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint4 w;
+            w.x = pack_bf16(e[8 * ch + 0], e[8 * ch + 1]);
+            w.y = pack_bf16(e[8 * ch + 2], e[8 * ch + 3]);
+            w.z = pack_bf16(e[8 * ch + 4], e[8 * ch + 5]);
+            w.w = pack_bf16(e[8 * ch + 6], e[8 * ch + 7]);
+            *reinterpret_cast<uint4*>(sPw + kmaj_off<128>(row, 4 * h + ch)) = w;
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(pfull);
+        if (lane == 0) mbar_arrive(&pfull[b]);
         // ---- epilogue: O row / l -> bf16 partial, lse partial ----
         ok = __all_sync(0xffffffffu, mbar_wait(&ofull[b], (u >> 1) & 1, p.wait_ns, abort_flag));
         if (!ok) {
@@ -384,18 +413,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* dst = nullptr;
+        int prow = -1;
         if (ent >= 0) {
-          const int64_t prow = ((((int64_t)bg * p.N + i) * p.topk + (ent & 31)) * G + row % G);
-          dst = p.o_part + prow * D;
+          prow = (int)((((int64_t)bg * p.N + i) * p.topk + (ent & 31)) * G + row % G);
           p.lse_part[prow] = l > 0.f ? (ms + log2f(l)) * kLn2 : -INFINITY;
         }
+        // Stage 64 columns at a time in this warp's own (now free) P rows, swizzled,
+        // then store whole 128-byte partial-row segments (4 rows per instruction).
 #pragma unroll
-        for (int h = 0; h < D / 32; ++h) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + 256 + 128 * b + 32 * h, r);
-          tmem_wait_ld();
-          if (dst) {
+        for (int h = 0; h < D / 64; ++h) {
+          uint8_t* stg = sPw + h * L::kHalf + (warp & 3) * 32 * 128;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem + lane_base + 256 + 128 * b + 64 * h + 32 * hh, r);
+            tmem_wait_ld();
 #pragma unroll
             for (int x = 0; x < 32; x += 8) {
               uint4 w;
@@ -403,9 +435,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               w.y = pack_bf16(__uint_as_float(r[x + 2]) * inv, __uint_as_float(r[x + 3]) * inv);
               w.z = pack_bf16(__uint_as_float(r[x + 4]) * inv, __uint_as_float(r[x + 5]) * inv);
               w.w = pack_bf16(__uint_as_float(r[x + 6]) * inv, __uint_as_float(r[x + 7]) * inv);
-              *reinterpret_cast<uint4*>(dst + 32 * h + x) = w;
+              *reinterpret_cast<uint4*>(stg + sw128_row(lane, 4 * hh + x / 8)) = w;
             }
           }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int x = lane + 32 * k;
+            const int rr = x >> 3, cc = x & 7;
+            const int pr = __shfl_sync(0xffffffffu, prow, rr);
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + sw128_row(rr, cc));
+            if (pr >= 0) *reinterpret_cast<uint4*>(p.o_part + (int64_t)pr * D + 64 * h + 8 * cc) = v;
+          }
+          __syncwarp();
         }
         tc_fence_before();
         __syncwarp();
@@ -417,7 +459,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) set_status(p.status, MSA_ERR_DEVICE_TIMEOUT);
-  if (warp == 8) {
+  if (warp == 12) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -149,6 +149,14 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32: relative error about
+// 2^-22, results below 2^-126 flushed to zero).  Softmax weights that small carry no
+// weight in any sum they enter.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -199,6 +207,13 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(int M, int N) {
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, bool pred = true) {
   const int n = pred ? 16 : 0;  // zero-fill when predicated off
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(n)
+               : "memory");
+}
+// 4-byte asynchronous copy (zero-fill when predicated off).
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src, bool pred = true) {
+  const int n = pred ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
                "r"(n)
                : "memory");
 }
