@@ -227,13 +227,14 @@ def run_ours(args, cfg, rank, world):
     # per-kernel events (hook) and per-phase events, one set per timed step
     K = args.steps
     kev = {kname: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(K)] for kname in ("index", "fwd", "bwd")}
+                   for _ in range(K)] for kname in ("index", "index_lse", "fwd", "bwd")}
     pev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     for lst in kev.values():  # materialise the events so their handles exist
         for a, b in lst:
             a.record(stream)
             b.record(stream)
-    kid = {"index": _lib.MSA_KERNEL_INDEX, "fwd": _lib.MSA_KERNEL_FWD, "bwd": _lib.MSA_KERNEL_BWD}
+    kid = {"index": _lib.MSA_KERNEL_INDEX, "index_lse": _lib.MSA_KERNEL_INDEX_LSE,
+           "fwd": _lib.MSA_KERNEL_FWD, "bwd": _lib.MSA_KERNEL_BWD}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -279,7 +280,7 @@ def run_ours(args, cfg, rank, world):
     }
     peaks, peak_src = load_peaks()
     peak_tf = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    kflops = {"index": flops["index"], "fwd": flops["fwd"], "bwd": flops["bwd"]}
+    kflops = {k: flops[k] for k in kern_ms}
     dom = max(kern_ms, key=lambda k: kern_ms[k])
     achieved = kflops[dom] / (kern_ms[dom] / 1000.0) / 1e12
     traffic = None

@@ -33,6 +33,7 @@ EXPORTS = ("msa_workspace_size", "msa_index_topk", "msa_fwd", "msa_bwd",
 MSA_KERNEL_INDEX = 0
 MSA_KERNEL_FWD = 1
 MSA_KERNEL_BWD = 2
+MSA_KERNEL_INDEX_LSE = 3
 
 
 class Problem(ctypes.Structure):

@@ -1,0 +1,416 @@
+// index_lse.cu -- log-sum-exp of the index branch over each query's selected tokens,
+// on the 5th-generation tensor cores.
+//
+// Method: the index distribution of a query row is the softmax of its scaled
+// index scores over the tokens of its k selected blocks, the student side of the
+// KL alignment loss (MSA summary, 7minutos.es, "Cómo se entrena MSA" ¶1-2).  The
+// top-k never computes it (the selection is exp-free, "El codiseño del kernel");
+// its normaliser is recomputed afterwards over the selected blocks only
+// ("Accelerating Million-Token Training", deephorus.pages.dev, ¶4): this file.
+//
+// Work unit: a tile is one key block c of one (batch, group) and up to 128 of the
+// queries whose block set holds c (the inverted lists of plan.cu with 128 queries
+// per tile).  Per CTA (persistent, a contiguous range of tiles):
+//   warps 8-11  loaders: gather the tile's 128 q_idx rows with cp.async into a
+//               4-stage ring in the swizzled K-major layout tcgen05 reads; one
+//               thread TMA-loads the block's k_idx tile into a 2-deep buffer;
+//   warp 12     TMEM owner + one MMA thread: S = Q_idx K_idx^T (128 x 128, K = d_idx)
+//               into a 4-slot TMEM ring;
+//   warps 0-7   two warpgroups taking alternate tiles (thread = row = TMEM lane):
+//               tcgen05.ld the row's 128 scores, causal mask, max, exp2 sum, and the
+//               partial lse of (row, slot).
+// A second kernel merges the k partials of every row.  The exp2 throughput of the
+// SM bounds the first kernel: 128 x 128 exponentials per tile.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace msa {
+namespace {
+
+constexpr int kThreads = 416;  // warps 0-7 softmax, 8-11 loaders, 12 MMA + TMEM owner
+constexpr int kLoadThreads = 128;
+constexpr int kQStages = 4;
+constexpr int kSlots = 4;      // TMEM score slots of 128 fp32 columns
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int DI>
+struct LseLayout {
+  static constexpr int kRowB = DI * 2;                // 64 or 128 bytes per row
+  static constexpr int kTile = 128 * kRowB;           // one 128-row operand
+  static constexpr int kK = 0;                        // 2 k_idx buffers
+  static constexpr int kQ = 2 * kTile;                // kQStages q_idx tiles
+  static constexpr int kBar = kQ + kQStages * kTile;
+  // kfull[2], kempty[2], qfull[kQStages], qempty[kQStages], sfull[kSlots],
+  // tfree[kSlots], mmadone
+  static constexpr int kNumBars = 4 + 2 * kQStages + 2 * kSlots + 1;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16;
+  // >= 116 KB so that one CTA (and its 512-column TMEM allocation) owns an SM
+  static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
+};
+
+struct LseParams {
+  const __nv_bfloat16* q_idx;  // [B][N][H_kv][DI]
+  const int* off;
+  const int* toff;
+  const int* entries;
+  float* lse_part;             // [((b*H_kv + g)*N + i)*topk + slot]
+  int64_t keys;
+  int N, H_kv, nb, topk;
+  float scale_log2;            // scale_idx * log2(e)
+  uint64_t wait_ns;
+  int* status;
+};
+
+__device__ __forceinline__ int lse_find_key(const int* __restrict__ toff, int64_t keys, int t) {
+  int64_t lo = 0, hi = keys - 1;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) >> 1;
+    if (__ldg(&toff[mid]) <= t) lo = mid; else hi = mid - 1;
+  }
+  return (int)lo;
+}
+
+// Key of tile t, given that the tiles of a CTA are visited in increasing order.
+struct Cursor {
+  int key = -1;
+  __device__ __forceinline__ int at(const int* __restrict__ toff, int64_t keys, int t) {
+    if (key < 0) {
+      key = lse_find_key(toff, keys, t);
+    } else {
+      while (key + 1 < keys && __ldg(&toff[key + 1]) <= t) ++key;
+    }
+    return key;
+  }
+};
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int DI>
+__global__ void __launch_bounds__(kThreads, 1)
+    index_lse_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const LseParams p) {
+  using L = LseLayout<DI>;
+  constexpr int RB = L::kRowB;
+  constexpr int CH = DI / 8;  // 16-byte chunks per row
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sK = smem + L::kK;
+  uint8_t* sQ = smem + L::kQ;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* kfull = bars;                 // [2] k_idx tile landed
+  uint64_t* kempty = bars + 2;            // [2] last MMA of the block retired
+  uint64_t* qfull = bars + 4;             // [kQStages] q rows gathered
+  uint64_t* qempty = qfull + kQStages;    // [kQStages] MMA done reading
+  uint64_t* sfull = qempty + kQStages;    // [kSlots] scores in TMEM
+  uint64_t* tfree = sfull + kSlots;       // [kSlots] scores read out
+  uint64_t* mmadone = tfree + kSlots;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = __ldg(&p.toff[p.keys]);
+  const int per = (total + gridDim.x - 1) / gridDim.x;
+  const int t_begin = blockIdx.x * per;
+  const int t_end = min(total, t_begin + per);
+  const int n_tiles = max(0, t_end - t_begin);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+    }
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(&qfull[s], kLoadThreads);
+      mbar_init(&qempty[s], 1);
+    }
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&sfull[s], 1);
+      mbar_init(&tfree[s], 4);  // one arrive per warp of the reading warpgroup
+    }
+    mbar_init(mmadone, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 12) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (n_tiles > 0) {
+    if (warp >= 8 && warp < 12) {
+      // ================================ loaders =================================
+      // Per tile: (new block) TMA its k_idx tile -> gather q(u) -> publish q(u-1).
+      // The k_idx wait is on the block two keys back: its last tile is at most u-2,
+      // published in an earlier iteration, and the MMA thread releases the buffer
+      // right after that tile's MMA.
+      const int lt = threadIdx.x - 256;
+      Cursor kc;
+      int prev_key = -1, k_loads = 0, k_issued = 0;
+      for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
+        const int t = t_begin + u;
+        const int st = u % kQStages;
+        const int key = kc.at(p.toff, p.keys, t);
+        const int bg = key / p.nb, c = key - bg * p.nb;
+        const int b = bg / p.H_kv, g = bg - b * p.H_kv;
+        const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * 128;
+        const int ne = min(128, __ldg(&p.off[key + 1]) - e0);
+        if (key != prev_key) {
+          if (lt == 0) {
+            const int kb = k_loads & 1;
+            if (k_loads >= 2 &&
+                !mbar_wait(&kempty[kb], ((k_loads >> 1) - 1) & 1, p.wait_ns, abort_flag))
+              *abort_flag = 1;
+            if (!*abort_flag) {
+              mbar_arrive_expect_tx(&kfull[kb], L::kTile);
+              tma_load_3d(sK + kb * L::kTile, &tm_k, &kfull[kb], 0, c * 128, b);
+              k_issued = k_loads + 1;
+            }
+          }
+          ++k_loads;
+          prev_key = key;
+        }
+        if (!mbar_wait(&qempty[st], ((u / kQStages) & 1) ^ 1, p.wait_ns, abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* dq = sQ + st * L::kTile;
+#pragma unroll 4
+        for (int x = lt; x < 128 * CH; x += kLoadThreads) {
+          const int r = x / CH, ch = x % CH;
+          const int ent = r < ne ? __ldg(&p.entries[e0 + r]) : -1;
+          const bool ok = ent >= 0;
+          const int i = ok ? (ent >> 5) : 0;
+          const int64_t src = (((int64_t)b * p.N + i) * p.H_kv + g) * DI + ch * 8;
+          cp_async_16(dq + swz<RB>(r, ch), p.q_idx + src, ok);
+        }
+        cp_async_commit();
+        if (u >= 1) {
+          cp_async_wait<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(&qfull[(u - 1) % kQStages]);
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      if (!*abort_flag) mbar_arrive(&qfull[(n_tiles - 1) % kQStages]);
+      // teardown: every k_idx TMA issued must have landed before the CTA exits
+      if (lt == 0)
+        for (int n = max(0, k_issued - 2); n < k_issued; ++n)
+          mbar_wait(&kfull[n & 1], (n >> 1) & 1, 1000000000ull);
+    } else if (warp == 12) {
+      // ============================== MMA issuer ================================
+      if (lane == 0) {
+        constexpr uint32_t idesc = umma_idesc_bf16_f32(128, 128);
+        Cursor kc;
+        int cur_key = -1, k_uses = 0;
+        bool issued = false, ok = true;
+        for (int u = 0; u < n_tiles; ++u) {
+          const int key = kc.at(p.toff, p.keys, t_begin + u);
+          if (key != cur_key) {
+            if (!mbar_wait(&kfull[k_uses & 1], (k_uses >> 1) & 1, p.wait_ns, abort_flag)) {
+              ok = false;
+              break;
+            }
+            ++k_uses;
+            cur_key = key;
+          }
+          const int st = u % kQStages, sl = u % kSlots;
+          if (!mbar_wait(&qfull[st], (u / kQStages) & 1, p.wait_ns, abort_flag) ||
+              !mbar_wait(&tfree[sl], ((u / kSlots) & 1) ^ 1, p.wait_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t qd = umma_desc_kmajor<RB>(smem_u32(sQ + st * L::kTile));
+          const uint64_t kd = umma_desc_kmajor<RB>(smem_u32(sK + ((k_uses - 1) & 1) * L::kTile));
+#pragma unroll
+          for (int kk = 0; kk < DI / 16; ++kk)  // +32 bytes per K=16 step
+            tc_mma_bf16(tmem + 128 * sl, qd + 2 * kk, kd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+          tc_commit(&qempty[st]);
+          tc_commit(&sfull[sl]);
+          issued = true;
+          // after the block's last tile its k_idx buffer may be refilled
+          Cursor peek = kc;
+          if (u + 1 < n_tiles && peek.at(p.toff, p.keys, t_begin + u + 1) != key)
+            tc_commit(&kempty[(k_uses - 1) & 1]);
+        }
+        if (!ok) *abort_flag = 1;
+        if (issued) {
+          tc_commit(mmadone);
+          mbar_wait(mmadone, 0, 1000000000ull);
+        }
+      }
+    } else {
+      // ====================== row log-sum-exp: warps 0-7 ========================
+      const int wg = warp >> 2;
+      const int row = (warp & 3) * 32 + lane;  // TMEM lane
+      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+      const float sl2 = p.scale_log2;
+      Cursor kc;
+      for (int u = wg; u < n_tiles; u += 2) {
+        const int t = t_begin + u;
+        const int sl = u % kSlots;
+        const int key = kc.at(p.toff, p.keys, t);
+        const int bg = key / p.nb, c = key - bg * p.nb;
+        const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * 128;
+        const int ne = min(128, __ldg(&p.off[key + 1]) - e0);
+        const int ent = row < ne ? __ldg(&p.entries[e0 + row]) : -1;
+        const int i = ent >> 5;
+        const bool ok =
+            __all_sync(0xffffffffu, mbar_wait(&sfull[sl], (u / kSlots) & 1, p.wait_ns, abort_flag));
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const int jlim = ent >= 0 ? min(i, p.N - 1) - c * 128 : -1;  // last valid column
+        const bool full = __all_sync(0xffffffffu, jlim >= 127);
+        float m = -INFINITY;  // running max of the raw scores
+        float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t ra[32], rb[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + 128 * sl + 64 * hh, ra);
+          tmem_ld_32x32b_x32(tmem + lane_base + 128 * sl + 64 * hh + 32, rb);
+          tmem_wait_ld();
+          uint32_t r[64];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            r[x] = ra[x];
+            r[32 + x] = rb[x];
+          }
+          if (hh == 1) {  // the slot is in registers: hand it back to the MMA
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tfree[sl]);
+          }
+          float cm = -INFINITY;
+          if (full) {
+#pragma unroll
+            for (int x = 0; x < 64; x += 2)
+              cm = fmax3(cm, __uint_as_float(r[x]), __uint_as_float(r[x + 1]));
+          } else {
+#pragma unroll
+            for (int x = 0; x < 64; x += 2)
+              cm = fmax3(cm, 64 * hh + x <= jlim ? __uint_as_float(r[x]) : -INFINITY,
+                         64 * hh + x + 1 <= jlim ? __uint_as_float(r[x + 1]) : -INFINITY);
+          }
+          const float nm = fmaxf(m, cm);
+          if (nm != -INFINITY) {
+            const float ms = nm * sl2;
+            const float rescale = ex2_fast(m * sl2 - ms);  // 0 while m = -inf
+            l0 *= rescale;
+            l1 *= rescale;
+            if (full) {
+#pragma unroll
+              for (int x = 0; x < 64; x += 2) {
+                l0 += ex2_fast(__uint_as_float(r[x]) * sl2 - ms);
+                l1 += ex2_fast(__uint_as_float(r[x + 1]) * sl2 - ms);
+              }
+            } else {
+#pragma unroll
+              for (int x = 0; x < 64; x += 2) {
+                l0 += 64 * hh + x <= jlim ? ex2_fast(__uint_as_float(r[x]) * sl2 - ms) : 0.f;
+                l1 += 64 * hh + x + 1 <= jlim ? ex2_fast(__uint_as_float(r[x + 1]) * sl2 - ms)
+                                              : 0.f;
+              }
+            }
+            m = nm;
+          }
+        }
+        if (ent >= 0) {
+          const float l = l0 + l1;
+          p.lse_part[((int64_t)bg * p.N + i) * p.topk + (ent & 31)] =
+              l > 0.f ? (m * sl2 + log2f(l)) * kLn2 : -INFINITY;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) set_status(p.status, MSA_ERR_DEVICE_TIMEOUT);
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// lse_idx[b,g,i] = log-sum-exp over the row's valid slots of the partial lse.
+__global__ void lse_combine_kernel(const float* __restrict__ lse_part,
+                                   const int32_t* __restrict__ block_idx,
+                                   float* __restrict__ lse_idx, int64_t rows, int topk, int nb) {
+  const int64_t r = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (r >= rows) return;
+  const int32_t* sel = block_idx + r * topk;
+  float m = -INFINITY;
+  for (int s = 0; s < topk; ++s)
+    if (sel[s] >= 0 && sel[s] < nb) m = fmaxf(m, lse_part[r * topk + s]);
+  float l = 0.f;
+  for (int s = 0; s < topk; ++s)
+    if (sel[s] >= 0 && sel[s] < nb) l += __expf(lse_part[r * topk + s] - m);
+  lse_idx[r] = m + logf(l);
+}
+
+template <int DI>
+cudaError_t launch_lse_tc(const CUtensorMap& tk, const LseParams& prm, const Ctx& cx,
+                          cudaStream_t st) {
+  using L = LseLayout<DI>;
+  auto kern = index_lse_tc_kernel<DI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  kernel_event(MSA_KERNEL_INDEX_LSE, true, st);
+  kern<<<cx.num_sms, kThreads, L::kAlloc, st>>>(tk, prm);
+  kernel_event(MSA_KERNEL_INDEX_LSE, false, st);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_index_lse(const Shape& s, const void* q_idx, const void* k_idx,
+                             const int32_t* block_idx, const Plan& pl, float* lse_part,
+                             float* lse_idx, const Ctx& cx, cudaStream_t st) {
+  const int DI = s.d_idx;
+  CUtensorMap tk;
+  const uint64_t dims[3] = {(uint64_t)DI, (uint64_t)s.N, (uint64_t)s.B};
+  const uint64_t strides[2] = {(uint64_t)DI * 2, (uint64_t)s.N * DI * 2};
+  const uint32_t box[3] = {(uint32_t)DI, 128, 1};
+  if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_idx, dims, strides, box,
+                    DI == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  LseParams prm;
+  prm.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
+  prm.off = pl.off;
+  prm.toff = pl.toff;
+  prm.entries = pl.entries;
+  prm.lse_part = lse_part;
+  prm.keys = s.keys();
+  prm.N = s.N;
+  prm.H_kv = s.H_kv;
+  prm.nb = s.nb;
+  prm.topk = s.topk;
+  prm.scale_log2 = s.scale_idx * kLog2e;
+  prm.wait_ns = cx.wait_ns;
+  prm.status = cx.status;
+  cudaError_t e = DI == 64 ? launch_lse_tc<64>(tk, prm, cx, st) : launch_lse_tc<32>(tk, prm, cx, st);
+  if (e != cudaSuccess) return e;
+  const int64_t rows = s.rows_kv();
+  lse_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(lse_part, block_idx, lse_idx,
+                                                                     rows, s.topk, s.nb);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace msa

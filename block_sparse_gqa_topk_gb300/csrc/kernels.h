@@ -49,7 +49,6 @@ cudaError_t launch_index_topk(const Shape& s, const void* q_idx, const void* k_i
                               int32_t* block_idx, const Ctx& cx, cudaStream_t st);
 
 // Index LSE over the selected tokens (gathered, KV-outer) -> lse_idx.
-size_t index_lse_ws_bytes(const Shape& s);
 cudaError_t launch_index_lse(const Shape& s, const void* q_idx, const void* k_idx,
                              const int32_t* block_idx, const Plan& pl, float* lse_part,
                              float* lse_idx, const Ctx& cx, cudaStream_t st);

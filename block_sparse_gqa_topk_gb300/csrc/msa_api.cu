@@ -103,7 +103,7 @@ size_t ws_fwd(const Shape& s) {
 int finish(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
 
 std::atomic<uint64_t> g_launches{0};
-cudaEvent_t g_ev[3][2] = {{nullptr, nullptr}, {nullptr, nullptr}, {nullptr, nullptr}};
+cudaEvent_t g_ev[4][2] = {};
 
 }  // namespace
 
@@ -113,7 +113,7 @@ void kernel_event(int kernel, bool before, cudaStream_t st) {
   cudaEvent_t ev = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (kernel >= 0 && kernel < 3 && g_ev[kernel][0] && g_ev[kernel][1])
+    if (kernel >= 0 && kernel < 4 && g_ev[kernel][0] && g_ev[kernel][1])
       ev = g_ev[kernel][before ? 0 : 1];
   }
   if (ev) cudaEventRecord(ev, st);
@@ -135,7 +135,7 @@ extern "C" {
 int msa_version(void) { return 10000; }
 
 int msa_set_kernel_events(int kernel, cudaEvent_t start, cudaEvent_t stop) {
-  if (kernel < 0 || kernel > 2) return MSA_ERR_ARG;
+  if (kernel < 0 || kernel > 3) return MSA_ERR_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   g_ev[kernel][0] = (start && stop) ? start : nullptr;
   g_ev[kernel][1] = (start && stop) ? stop : nullptr;

@@ -146,7 +146,8 @@ int msa_debug_set(uint64_t wait_limit_ns, int flags);
 
 /* Profiling hook.  Kernels: MSA_KERNEL_INDEX (the index scoring + top-k kernel of
  * msa_index_topk), MSA_KERNEL_FWD (the gathered attention kernel of msa_fwd),
- * MSA_KERNEL_BWD (the fused backward kernel of msa_bwd).  When start and stop are
+ * MSA_KERNEL_BWD (the fused backward kernel of msa_bwd), MSA_KERNEL_INDEX_LSE (the
+ * gathered index log-sum-exp kernel of msa_index_topk when lse_idx is requested).  When start and stop are
  * both non-NULL, every later launch of that kernel records `start` on its stream
  * just before the launch and `stop` just after it; NULL clears the hook.  The
  * events are the caller's (created on the current device) and are only recorded,
@@ -154,6 +155,7 @@ int msa_debug_set(uint64_t wait_limit_ns, int flags);
 #define MSA_KERNEL_INDEX 0
 #define MSA_KERNEL_FWD 1
 #define MSA_KERNEL_BWD 2
+#define MSA_KERNEL_INDEX_LSE 3
 int msa_set_kernel_events(int kernel, cudaEvent_t start, cudaEvent_t stop);
 
 /* Number of kernels this library has launched in this process (all devices). */
