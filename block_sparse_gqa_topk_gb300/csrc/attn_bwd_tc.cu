@@ -65,9 +65,13 @@ struct BL {
   static constexpr int kV = kK + (D / 64) * kKH;
   static constexpr int kKi = kV + (D / 64) * kKH;   // k_idx [128][64], zero-padded
   static constexpr int kQH = 64 * 128;              // [64][64] bf16 block
+  // big stage (2 slots): q and dO rows of a chunk, released by the MMAs (3)-(5)
   static constexpr int kSQ = 0;
   static constexpr int kSdO = kSQ + (D / 64) * kQH;
-  static constexpr int kSQi = kSdO + (D / 64) * kQH;  // [16][64]
+  static constexpr int kBig = kSdO + (D / 64) * kQH;
+  // small stage (3 slots): q_idx rows and per-row scalars, released by the epilogue
+  // and the dk_idx MMA
+  static constexpr int kSQi = 0;                      // [16][64] bf16 (SW128)
   static constexpr int kSLse = kSQi + 16 * 128;       // float[64] lse (natural log)
   static constexpr int kSD = kSLse + 64 * 4;          // float[64] D
   static constexpr int kSRi = kSD + 64 * 4;           // int[64] query index of the row, -1 pad
@@ -75,16 +79,19 @@ struct BL {
   static constexpr int kSQiq = kSRp + 64 * 4;         // int[16] query index of the slot, -1 pad
   static constexpr int kSQp = kSQiq + 16 * 4;         // int[16] dq_idx partial row, -1 pad
   static constexpr int kSLi = kSQp + 16 * 4;          // float[16] lse_idx (natural log)
-  static constexpr int kStage = ((kSLi + 16 * 4) + 1023) & ~1023;
-  static constexpr int kStages0 = kKi + kKH;
-  static constexpr int kPT = kStages0 + 2 * kStage;   // P^T [128][64] bf16 (SW128)
+  static constexpr int kSmall = ((kSLi + 16 * 4) + 1023) & ~1023;
+  static constexpr int kBig0 = kKi + kKH;
+  static constexpr int kSmall0 = kBig0 + 2 * kBig;
+  static constexpr int kPT = kSmall0 + 3 * kSmall;    // P^T [128][64] bf16 (SW128)
   static constexpr int kdST = kPT + 128 * 128;        // dS^T [128][64]
   static constexpr int kTeach = kdST + 128 * 128;     // p_T float [128][17] (padded rows)
-  static constexpr int kDZ = kTeach + 128 * 17 * 4;   // dz bf16 [128][16] (32-byte rows)
-  static constexpr int kStg = kDZ + 128 * 32;        // dQ staging [2][32 rows][272 B]
-  static constexpr int kStgRow = 2 * D + 16;
-  static constexpr int kBar = kStg + 2 * 32 * kStgRow;
-  static constexpr int kNumBars = 18;
+  // dz^T bf16 [128 keys][16 slots]: 32-byte rows in the 32-byte swizzle, the K-major A
+  // operand of the dk_idx MMA
+  static constexpr int kDZ = (kTeach + 128 * 17 * 4 + 1023) & ~1023;
+  // dQ staging, one [32 rows][32 d] bf16 block (64-byte rows) per epilogue warp
+  static constexpr int kStg = kDZ + 128 * 32;
+  static constexpr int kBar = kStg + 8 * 32 * 64;
+  static constexpr int kNumBars = 20;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -101,6 +108,10 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t a, uint32_t lbo) {
   return (uint64_t)((a & 0x3FFFF) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
          ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
+// K-major operand with 32-byte rows in the 32-byte swizzle: SBO = 8 rows x 32 B.
+__device__ __forceinline__ uint64_t desc_sw32(uint32_t a) {
+  return (uint64_t)((a & 0x3FFFF) >> 4) | ((uint64_t)(256 >> 4) << 32) | (1ull << 46) | (6ull << 61);
+}
 __host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn, int b_mn) {
   return umma_idesc_bf16_f32(M, N) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
 }
@@ -109,7 +120,7 @@ __device__ __forceinline__ void fence_async_smem() {
 }
 
 // TMEM columns
-constexpr uint32_t cDK = 0, cDV = 128, cST = 256, cDPT = 320, cDQT = 384;
+constexpr uint32_t cDK = 0, cDV = 128, cST = 256, cDPT = 320, cDQT = 384, cDKI = 448;
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -124,18 +135,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
   uint64_t* kvfull = bar + 0;
   uint64_t* kvempty = bar + 1;  // MMA commit + 8 epilogue warps (k_idx reads)
-  uint64_t* qfull = bar + 2;    // [2]
-  uint64_t* qempty = bar + 4;   // [2] MMA commit + 8 epilogue warps
-  uint64_t* b_s = bar + 6;      // (1)(2) done
-  uint64_t* b_p = bar + 7;      // E1 done (P^T, dS^T in smem)
-  uint64_t* b_q = bar + 8;      // (3)(4)(5) done
-  uint64_t* b_e = bar + 9;      // E2 done (dQ^T columns read)
-  uint64_t* b_key = bar + 10;   // block's MMAs done
-  uint64_t* b_kfree = bar + 11; // block's accumulators read out
-  uint64_t* mmadone = bar + 12;
-  uint64_t* e_sync1 = bar + 13;  // every epilogue warp has written its teacher rows
-  uint64_t* e_sync2 = bar + 14;  // every epilogue warp has written its dz rows
-  uint64_t* e_stg = bar + 15;    // [2] a warpgroup's dQ rows are staged (bars 15, 16)
+  uint64_t* qfull = bar + 2;    // [2] chunk gathered (both stage parts)
+  uint64_t* bempty = bar + 4;   // [2] big stage free: MMA commit after (3)-(5)
+  uint64_t* sempty = bar + 6;   // [3] small stage free: dk_idx MMA commit + 8 epilogue warps
+  uint64_t* b_s = bar + 9;      // (1)(2) done
+  uint64_t* b_p = bar + 10;     // E1 done (P^T, dS^T in smem)
+  uint64_t* b_q = bar + 11;     // (3)(4)(5) done
+  uint64_t* b_e = bar + 12;     // E2 done (dQ^T columns and the staging read)
+  uint64_t* b_key = bar + 13;   // block's MMAs done
+  uint64_t* b_kfree = bar + 14; // block's accumulators read out
+  uint64_t* mmadone = bar + 15;
+  uint64_t* e_sync2 = bar + 16;  // every epilogue warp has written its dz (the dk_idx MMA waits)
+  uint64_t* zfree = bar + 17;    // the dk_idx MMA has read dz
+  uint64_t* e_wg = bar + 18;     // [2] a warpgroup's four warps have written their dz
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
 
@@ -147,8 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(kvempty, 1 + kEpiWarps);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&qfull[s], kLoadThreads);
-      mbar_init(&qempty[s], 1 + kEpiWarps);
+      mbar_init(&bempty[s], 1);
     }
+    for (int s = 0; s < 3; ++s) mbar_init(&sempty[s], 1 + kEpiWarps);
     mbar_init(b_s, 1);
     mbar_init(b_p, kEpiWarps);
     mbar_init(b_q, 1);
@@ -156,13 +169,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_key, 1);
     mbar_init(b_kfree, kEpiWarps);
     mbar_init(mmadone, 1);
-    mbar_init(e_sync1, kEpiWarps);
     mbar_init(e_sync2, kEpiWarps);
-    mbar_init(&e_stg[0], 4);
-    mbar_init(&e_stg[1], 4);
+    mbar_init(zfree, 1);
+    mbar_init(&e_wg[0], 4);
+    mbar_init(&e_wg[1], 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
+  for (int x = threadIdx.x; x < 128 * 32 / 16; x += blockDim.x)
+    reinterpret_cast<uint4*>(sm + L::kDZ)[x] = make_uint4(0u, 0u, 0u, 0u);
   if (warp == 10) {
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
@@ -215,11 +230,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             cp_async_16(sm + L::kKi + sw128(r, cc), p.k_idx + src, ok);
           }
         }
-        if (!mbar_wait(&qempty[s], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag)) {
+        const int s3 = u % 3;
+        if (!mbar_wait(&bempty[s], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag) ||
+            !mbar_wait(&sempty[s3], ((u / 3) & 1) ^ 1, p.wait_ns, abort_flag)) {
           *abort_flag = 1;
           break;
         }
-        uint8_t* st = sm + L::kStages0 + s * L::kStage;
+        uint8_t* st = sm + L::kBig0 + s * L::kBig;       // q, dO
+        uint8_t* ss = sm + L::kSmall0 + s3 * L::kSmall;  // q_idx, scalars
         const int q0 = e_begin + ch * QC;
         const int nq = min(QC, e_end - q0);
         // this chunk's entries (prefetched one chunk ahead), lane q = query slot q
@@ -246,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool ok = ent >= 0 && cc * 8 < p.DI;
           const int i = ok ? (ent >> 5) : 0;
           const int64_t src = (((int64_t)b * p.N + i) * p.H_kv + g) * p.DI + (ok ? cc * 8 : 0);
-          cp_async_16(st + L::kSQi + sw128(qi, cc), p.q_idx + src, ok);
+          cp_async_16(ss + L::kSQi + sw128(qi, cc), p.q_idx + src, ok);
         }
         {
           const int r = lt, qi = r / G, h = r % G;  // one row per loader thread
@@ -254,18 +272,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool ok = ent >= 0;
           const int ri = ok ? (ent >> 5) : -1;
           const int64_t x = ((int64_t)b * p.H_kv * G + g * G + h) * p.N + (ok ? ri : 0);
-          cp_async_4(st + L::kSLse + 4 * r, p.lse + x, ok);
-          cp_async_4(st + L::kSD + 4 * r, p.Dv + x, ok);
-          reinterpret_cast<int*>(st + L::kSRi)[r] = ri;
-          reinterpret_cast<int*>(st + L::kSRp)[r] =
+          cp_async_4(ss + L::kSLse + 4 * r, p.lse + x, ok);
+          cp_async_4(ss + L::kSD + 4 * r, p.Dv + x, ok);
+          reinterpret_cast<int*>(ss + L::kSRi)[r] = ri;
+          reinterpret_cast<int*>(ss + L::kSRp)[r] =
               ok ? (int)((((int64_t)bg * p.N + ri) * p.topk + (ent & 31)) * G + h) : -1;
           if (lt < kQS) {
             const bool okq = my_ent >= 0;
             const int iq = okq ? (my_ent >> 5) : 0;
-            reinterpret_cast<int*>(st + L::kSQiq)[lt] = okq ? iq : -1;
-            reinterpret_cast<int*>(st + L::kSQp)[lt] =
+            reinterpret_cast<int*>(ss + L::kSQiq)[lt] = okq ? iq : -1;
+            reinterpret_cast<int*>(ss + L::kSQp)[lt] =
                 okq ? (int)(((int64_t)bg * p.N + iq) * p.topk + (my_ent & 31)) : -1;
-            cp_async_4(st + L::kSLi + 4 * lt, p.lse_idx + (int64_t)bg * p.N + iq, okq);
+            cp_async_4(ss + L::kSLi + 4 * lt, p.lse_idx + (int64_t)bg * p.N + iq, okq);
           }
         }
         cp_async_commit();
@@ -283,8 +301,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t aPT = smem_u32(sm + L::kPT), adST = smem_u32(sm + L::kdST);
       constexpr uint32_t i12 = idesc(128, 64, 0, 0), i34 = idesc(128, D, 0, 1);
       constexpr uint32_t i5 = idesc(128, 64, 1, 1);
+      constexpr uint32_t iki = idesc(128, 64, 0, 1);  // dk_idx += dz^T q_idx (K = 16 slots)
+      const uint32_t aDZ = smem_u32(sm + L::kDZ);
       int u = 0, nkeys = 0;
       bool ok = true, issued = false;
+      int pend = -1, pend_ch = 0;  // chunk whose dk_idx MMA is not issued yet (same block)
+      // dk_idx(v): once every epilogue warp has written chunk v's dz
+      auto issue_dki = [&](int v, int vch) -> bool {
+        if (!mbar_wait(e_sync2, v & 1, p.wait_ns, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t aQi = smem_u32(sm + L::kSmall0 + (v % 3) * L::kSmall + L::kSQi);
+        tc_mma_bf16(tmem + cDKI, desc_sw32(aDZ), desc_mn(aQi, L::kQH), iki, vch > 0 ? 1u : 0u);
+        tc_commit(zfree);
+        tc_commit(&sempty[v % 3]);
+        return true;
+      };
       for (int64_t kk = blockIdx.x; kk < p.keys && ok; kk += gridDim.x) {
         const int c = (int)(kk / BG), bg = (int)(kk % BG);
         const int key = bg * p.nb + c;
@@ -293,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nch == 0) continue;
         for (int ch = 0; ch < nch && ok; ++ch, ++u) {
           const int s = u & 1;
-          const uint32_t st = smem_u32(sm + L::kStages0 + s * L::kStage);
+          const uint32_t st = smem_u32(sm + L::kBig0 + s * L::kBig);
           const uint32_t aQ = st + L::kSQ, adO = st + L::kSdO;
           ok = mbar_wait(&qfull[s], (u >> 1) & 1, p.wait_ns, abort_flag);
           if (ok && ch == 0) ok = mbar_wait(kvfull, nkeys & 1, p.wait_ns, abort_flag);
@@ -311,6 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(b_s);
           issued = true;
+          if (pend >= 0) {
+            if (!(ok = issue_dki(pend, pend_ch))) break;
+            pend = -1;
+          }
           if (!(ok = mbar_wait(b_p, u & 1, p.wait_ns, abort_flag))) break;
           if (u > 0 && !(ok = mbar_wait(b_e, (u - 1) & 1, p.wait_ns, abort_flag))) break;
           tc_fence_after();
@@ -327,10 +362,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_mma_bf16(tmem + cDQT, desc_mn(aK + k * 2048, L::kKH), desc_mn(adST + k * 2048, L::kKH),
                         i5, k > 0);
           tc_commit(b_q);
-          tc_commit(&qempty[s]);
+          tc_commit(&bempty[s]);
           if (ch == nch - 1) {
+            if (!(ok = issue_dki(u, ch))) break;
             tc_commit(kvempty);
             tc_commit(b_key);
+          } else {
+            pend = u;
+            pend_ch = ch;
           }
         }
         if (ok) ++nkeys;
@@ -346,13 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = warp >> 2;              // which 32 of the 64 row columns
     const int tl = (warp & 3) * 32 + lane; // TMEM lane: key (E1, block end), d (E2)
     const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
-    const int kw = warp * 16;              // mma.sync: this warp's 16 keys
+    const int q4 = warp & 3;               // this warp's 32 keys (E1, KL) / 32 d (E2)
     const uint8_t* sKi = sm + L::kKi;
     float* sTeach = reinterpret_cast<float*>(sm + L::kTeach);
     uint8_t* sDZ = sm + L::kDZ;
-    float dki[8][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) dki[n][0] = dki[n][1] = dki[n][2] = dki[n][3] = 0.f;
     double kl = 0.0;
     int u = 0, nkeys = 0;
     bool ok = true;
@@ -365,150 +401,160 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = c * 128 + tl;  // key of this thread's TMEM lane
       for (int ch = 0; ch < nch; ++ch, ++u) {
         const int s = u & 1;
-        const uint8_t* st = sm + L::kStages0 + s * L::kStage;
-        const float* s_lse = reinterpret_cast<const float*>(st + L::kSLse);
-        const float* s_D = reinterpret_cast<const float*>(st + L::kSD);
-        const int* s_ri = reinterpret_cast<const int*>(st + L::kSRi);
-        const int* s_rp = reinterpret_cast<const int*>(st + L::kSRp);
-        const int* s_qi = reinterpret_cast<const int*>(st + L::kSQiq);
-        const int* s_qp = reinterpret_cast<const int*>(st + L::kSQp);
-        const float* s_li = reinterpret_cast<const float*>(st + L::kSLi);
-        const uint8_t* sQi = st + L::kSQi;
+        const uint8_t* ss = sm + L::kSmall0 + (u % 3) * L::kSmall;
+        const float* s_lse = reinterpret_cast<const float*>(ss + L::kSLse);
+        const float* s_D = reinterpret_cast<const float*>(ss + L::kSD);
+        const int* s_ri = reinterpret_cast<const int*>(ss + L::kSRi);
+        const int* s_rp = reinterpret_cast<const int*>(ss + L::kSRp);
+        const int* s_qi = reinterpret_cast<const int*>(ss + L::kSQiq);
+        const int* s_qp = reinterpret_cast<const int*>(ss + L::kSQp);
+        const float* s_li = reinterpret_cast<const float*>(ss + L::kSLi);
+        const uint8_t* sQi = ss + L::kSQi;
         ok = __all_sync(0xffffffffu, mbar_wait(&qfull[s], (u >> 1) & 1, p.wait_ns, abort_flag) &&
                                          mbar_wait(b_s, u & 1, p.wait_ns, abort_flag));
         if (!ok) break;
         tc_fence_after();
         // ---- E1: this warpgroup's 32 rows of key tl: P^T, dS^T, teacher ----
         {
-          uint32_t a[32], d2[32];
-          tmem_ld_32x32b_x32(tmem + lb + cST + 32 * wg, a);
-          tmem_ld_32x32b_x32(tmem + lb + cDPT + 32 * wg, d2);
-          tmem_wait_ld();
-          uint32_t pk[16], dk2[16];  // bf16 pairs
           float pt[QH];
 #pragma unroll
           for (int q = 0; q < QH; ++q) pt[q] = 0.f;
 #pragma unroll
-          for (int x = 0; x < 32; x += 2) {
-            float pv[2], dv2[2];
+          for (int hh = 0; hh < 2; ++hh) {  // 16 rows at a time
+            uint32_t a[16], d2[16];
+            tmem_ld_32x32b_x16(tmem + lb + cST + 32 * wg + 16 * hh, a);
+            tmem_ld_32x32b_x16(tmem + lb + cDPT + 32 * wg + 16 * hh, d2);
+            tmem_wait_ld();
+            uint32_t pk[8], dk2[8];  // bf16 pairs
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int r = 32 * wg + x + e;
-              const bool valid = j <= s_ri[r];  // s_ri = -1 for padding rows
-              const float v =
-                  valid ? ex2_fast(__uint_as_float(a[x + e]) * p.scale_log2 - s_lse[r] * kLog2e) : 0.f;
-              pv[e] = v;
-              dv2[e] = v * (__uint_as_float(d2[x + e]) - s_D[r]);
-              pt[(x + e) / G] += v;
+            for (int x4 = 0; x4 < 16; x4 += 4) {
+              const int r0 = 32 * wg + 16 * hh + x4;
+              const int4 ri4 = *reinterpret_cast<const int4*>(s_ri + r0);
+              const float4 ls4 = *reinterpret_cast<const float4*>(s_lse + r0);
+              const float4 dd4 = *reinterpret_cast<const float4*>(s_D + r0);
+              const int ri[4] = {ri4.x, ri4.y, ri4.z, ri4.w};  // -1 for padding rows
+              const float ls[4] = {ls4.x * kLog2e, ls4.y * kLog2e, ls4.z * kLog2e, ls4.w * kLog2e};
+              const float dd[4] = {dd4.x, dd4.y, dd4.z, dd4.w};
+              float pv[4], dv2[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int x = x4 + e;
+                const float v =
+                    j <= ri[e] ? ex2_fast(__uint_as_float(a[x]) * p.scale_log2 - ls[e]) : 0.f;
+                pv[e] = v;
+                dv2[e] = v * (__uint_as_float(d2[x]) - dd[e]);
+                pt[(16 * hh + x) / G] += v;
+              }
+              pk[x4 / 2] = pack_bf16(pv[0], pv[1]);
+              pk[x4 / 2 + 1] = pack_bf16(pv[2], pv[3]);
+              dk2[x4 / 2] = pack_bf16(dv2[0], dv2[1]);
+              dk2[x4 / 2 + 1] = pack_bf16(dv2[2], dv2[3]);
             }
-            pk[x / 2] = pack_bf16(pv[0], pv[1]);
-            dk2[x / 2] = pack_bf16(dv2[0], dv2[1]);
-          }
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            *reinterpret_cast<uint4*>(sm + L::kPT + sw128(tl, 4 * wg + cc)) =
-                make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-            *reinterpret_cast<uint4*>(sm + L::kdST + sw128(tl, 4 * wg + cc)) =
-                make_uint4(dk2[4 * cc], dk2[4 * cc + 1], dk2[4 * cc + 2], dk2[4 * cc + 3]);
+            for (int cc = 0; cc < 2; ++cc) {
+              const uint32_t o = sw128(tl, 4 * wg + 2 * hh + cc);
+              *reinterpret_cast<uint4*>(sm + L::kPT + o) =
+                  make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+              *reinterpret_cast<uint4*>(sm + L::kdST + o) =
+                  make_uint4(dk2[4 * cc], dk2[4 * cc + 1], dk2[4 * cc + 2], dk2[4 * cc + 3]);
+            }
           }
 #pragma unroll
           for (int q = 0; q < QH; ++q) sTeach[tl * kTS + wg * QH + q] = pt[q] * (1.f / G);
-          if (QC < kQS && wg == 1) {  // padded query slots of the teacher
-#pragma unroll
-            for (int q = QC; q < kQS; ++q) sTeach[tl * kTS + q] = 0.f;
-          }
         }
         fence_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_p);
-        // teacher complete for every key (bounded mbarrier, not bar.sync: a warp
-        // that gives up must not leave the others waiting forever)
-        __syncwarp();
-        if (lane == 0) mbar_arrive(e_sync1);
-        ok = __all_sync(0xffffffffu, mbar_wait(e_sync1, u & 1, p.wait_ns, abort_flag));
-        if (!ok) break;
         // ---- KL on mma.sync (overlaps the MMAs (3)-(5)) ----
+        // This warp: keys 32 q4 .. 32 q4 + 31 (its own E1 lanes, so the teacher it reads
+        // was written by this warp) x the query slots of its warpgroup (n8 tile nt).
+        constexpr int NT = (G == 4) ? 1 : 0;  // slots per n8 tile belong to one warpgroup (G=4)
+        const int nt = NT ? wg : 0;
+        if (u > 0) {  // the previous chunk's dk_idx MMA must be done reading dz
+          ok = __all_sync(0xffffffffu, mbar_wait(zfree, (u - 1) & 1, p.wait_ns, abort_flag));
+          if (!ok) break;
+        }
+        __syncwarp();  // teacher rows of this warp's lanes
         {
           float zt[2][4];
 #pragma unroll
-          for (int n = 0; n < 2; ++n) zt[n][0] = zt[n][1] = zt[n][2] = zt[n][3] = 0.f;
+          for (int m = 0; m < 2; ++m) zt[m][0] = zt[m][1] = zt[m][2] = zt[m][3] = 0.f;
 #pragma unroll
-          for (int kc = 0; kc < 4; ++kc) {  // d_idx (zero-padded to 64)
-            uint32_t a[4], bq[4];
-            ldmatrix_x4(a, sKi + sw128(kw + (lane & 15), kc * 2 + (lane >> 4)));
-            ldmatrix_x4(bq, sQi + sw128((lane & 7) + ((lane >> 4) << 3), kc * 2 + ((lane >> 3) & 1)));
-            mma_bf16_16816(zt[0], a, bq[0], bq[1]);
-            mma_bf16_16816(zt[1], a, bq[2], bq[3]);
+          for (int kp = 0; kp < 2; ++kp) {  // two d_idx steps of 16 per x4 load (zero-padded to 64)
+            uint32_t bq[4];
+            ldmatrix_x4(bq, sQi + sw128(8 * nt + (lane & 7), 4 * kp + (lane >> 3)));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int kc = 2 * kp + h;
+#pragma unroll
+              for (int m = 0; m < 2; ++m) {
+                uint32_t a[4];
+                ldmatrix_x4(a, sKi + sw128(32 * q4 + 16 * m + (lane & 15), kc * 2 + (lane >> 4)));
+                mma_bf16_16816(zt[m], a, bq[2 * h], bq[2 * h + 1]);
+              }
+            }
           }
-          const int kl0 = kw + (lane >> 2);
+          const int qs0 = 8 * nt + (lane & 3) * 2;  // this lane's slot pair
+          const bool mine = NT ? true : ((lane & 3) >> 1) == wg;  // G=8: 4 slots per warpgroup
           float klc = 0.f;
 #pragma unroll
-          for (int n = 0; n < 2; ++n) {
+          for (int m = 0; m < 2; ++m) {
+            const int kl0 = 32 * q4 + 16 * m + (lane >> 2);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int qs = n * 8 + (lane & 3) * 2 + (e & 1);
+              const int qs = qs0 + (e & 1);
               const int kloc = kl0 + ((e >> 1) << 3);
-              const bool valid = c * 128 + kloc <= s_qi[qs];  // s_qi = -1 for padding
-              const float zl2 = zt[n][e] * p.sidx_log2 - s_li[qs] * kLog2e;  // log2 p_I
+              const bool valid = mine && c * 128 + kloc <= s_qi[qs];  // s_qi = -1 for padding
+              const float zl2 = zt[m][e] * p.sidx_log2 - s_li[qs] * kLog2e;  // log2 p_I
               const float pI = valid ? ex2_fast(zl2) : 0.f;
-              const float pT = sTeach[kloc * kTS + qs];
-              if (valid && pT > 0.f) klc += pT * (__log2f(pT) - zl2);
-              zt[n][e] = valid ? p.w * (pI - pT) : 0.f;  // dz
+              const float pT = valid ? sTeach[kloc * kTS + qs] : 0.f;
+              if (pT > 0.f) klc += pT * (__log2f(pT) - zl2);
+              zt[m][e] = valid ? p.w * (pI - pT) : 0.f;  // dz
             }
-            *reinterpret_cast<uint32_t*>(sDZ + swz32(kl0, n) + (lane & 3) * 4) =
-                pack_bf16(zt[n][0], zt[n][1]);
-            *reinterpret_cast<uint32_t*>(sDZ + swz32(kl0 + 8, n) + (lane & 3) * 4) =
-                pack_bf16(zt[n][2], zt[n][3]);
+            if (mine) {
+              *reinterpret_cast<uint32_t*>(sDZ + swz32(kl0, nt) + (lane & 3) * 4) =
+                  pack_bf16(zt[m][0], zt[m][1]);
+              *reinterpret_cast<uint32_t*>(sDZ + swz32(kl0 + 8, nt) + (lane & 3) * 4) =
+                  pack_bf16(zt[m][2], zt[m][3]);
+            }
           }
           kl += (double)(klc * kLn2);
-          // dk_idx(16 keys x 64) += dz^T q_idx   (k = 16 query slots)
-          uint32_t az[4];
-          az[0] = pack_bf16(zt[0][0], zt[0][1]);
-          az[1] = pack_bf16(zt[0][2], zt[0][3]);
-          az[2] = pack_bf16(zt[1][0], zt[1][1]);
-          az[3] = pack_bf16(zt[1][2], zt[1][3]);
-          const int qrow = (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-          for (int n2 = 0; n2 < 4; ++n2) {
-            uint32_t bq[4];
-            ldmatrix_x4_trans(bq, sQi + sw128(qrow, n2 * 2 + (lane >> 4)));
-            mma_bf16_16816(dki[2 * n2], az, bq[0], bq[1]);
-            mma_bf16_16816(dki[2 * n2 + 1], az, bq[2], bq[3]);
-          }
         }
-        __syncwarp();  // dz complete for every key
-        if (lane == 0) mbar_arrive(e_sync2);
-        ok = __all_sync(0xffffffffu, mbar_wait(e_sync2, u & 1, p.wait_ns, abort_flag));
+        fence_async_smem();  // dz is read by the dk_idx MMA (async proxy)
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(e_sync2);
+          mbar_arrive(&e_wg[wg]);
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&e_wg[wg], u & 1, p.wait_ns, abort_flag));
         if (!ok) break;
-        if (warp * 16 < p.DI) {
-          // dq_idx(16 slots x 16 d_idx) = dz k_idx   (k = 128 keys)
-          float acc[2][4];
+        if (16 * q4 < p.DI) {
+          // dq_idx^T (16 d x 8 slots of this warpgroup) = k_idx^T dz^T   (k = 128 keys)
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int n = 0; n < 2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+          for (int ks2 = 0; ks2 < 4; ++ks2) {  // two 16-key steps per x4 dz load
+            uint32_t bz[4];
+            ldmatrix_x4_trans(bz, sDZ + swz32(32 * ks2 + (lane & 7) + (((lane >> 3) & 1) << 3) +
+                                                  ((lane >> 4) << 4), nt));
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            uint32_t a[4], bk[4];
-            ldmatrix_x4_trans(a, sDZ + swz32(ks * 16 + (lane & 7) + ((lane >> 4) << 3), (lane >> 3) & 1));
-            ldmatrix_x4_trans(bk, sKi + sw128(ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3),
-                                              warp * 2 + (lane >> 4)));
-            mma_bf16_16816(acc[0], a, bk[0], bk[1]);
-            mma_bf16_16816(acc[1], a, bk[2], bk[3]);
-          }
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int qs = (lane >> 2) + hh * 8;
-            const int qp = s_qp[qs];
-            if (qp >= 0) {
-              __nv_bfloat16* dst = p.dqi_part + (int64_t)qp * p.DI + warp * 16;
-#pragma unroll
-              for (int n = 0; n < 2; ++n)
-                *reinterpret_cast<uint32_t*>(dst + n * 8 + (lane & 3) * 2) =
-                    pack_bf16(acc[n][2 * hh] * p.sidx, acc[n][2 * hh + 1] * p.sidx);
+            for (int h = 0; h < 2; ++h) {
+              uint32_t a[4];
+              ldmatrix_x4_trans(a, sKi + sw128(32 * ks2 + 16 * h + (lane & 7) + ((lane >> 4) << 3),
+                                               2 * q4 + ((lane >> 3) & 1)));
+              mma_bf16_16816(acc, a, bz[2 * h], bz[2 * h + 1]);
             }
           }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int qs = 8 * nt + (lane & 3) * 2 + (e & 1);
+            const int dd = 16 * q4 + (lane >> 2) + ((e >> 1) << 3);
+            const int qp = s_qp[qs];
+            if ((NT || ((lane & 3) >> 1) == wg) && qp >= 0)
+              p.dqi_part[(int64_t)qp * p.DI + dd] = __float2bfloat16(acc[e] * p.sidx);
+          }
         }
-        // ---- E2: dQ^T columns of this warpgroup (thread = d) ----
+        // ---- E2: dQ^T columns of this warpgroup's rows (thread = d) ----
         ok = __all_sync(0xffffffffu, mbar_wait(b_q, u & 1, p.wait_ns, abort_flag));
         if (!ok) break;
         tc_fence_after();
@@ -516,12 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t a[32];
           tmem_ld_32x32b_x32(tmem + lb + cDQT + 32 * wg, a);
           tmem_wait_ld();
-          // stage the warpgroup's 32 rows (row-major, padded) so the global stores
-          // below write whole 256-byte partial rows; lanes (2m, 2m+1) swap one value
-          // so each stores a bf16 pair
-          uint8_t* stg = sm + L::kStg + wg * 32 * L::kStgRow;
+          // stage this warp's [32 rows][32 d] block so the global stores below write
+          // 64-byte row segments; lanes (2m, 2m+1) swap one value so each stores a pair
+          uint8_t* stg = sm + L::kStg + warp * (32 * 64);
           const bool odd = lane & 1;
-          const int dcol = tl & ~1;
 #pragma unroll
           for (int x = 0; x < 32; x += 2) {
             const float v0 = __uint_as_float(a[x]) * p.scale;
@@ -529,37 +573,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mine = odd ? v1 : v0;
             const float give = odd ? v0 : v1;
             const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-            *reinterpret_cast<uint32_t*>(stg + (x + (odd ? 1 : 0)) * L::kStgRow + dcol * 2) =
+            *reinterpret_cast<uint32_t*>(stg + (x + (odd ? 1 : 0)) * 64 + (lane & ~1) * 2) =
                 odd ? pack_bf16(got, mine) : pack_bf16(mine, got);
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&e_stg[wg]);
-        ok = __all_sync(0xffffffffu, mbar_wait(&e_stg[wg], u & 1, p.wait_ns, abort_flag));
-        if (!ok) break;
-        {
-          const uint8_t* stg = sm + L::kStg + wg * 32 * L::kStgRow;
-          const int wt = (warp & 3) * 32 + lane;  // 0..127 within the warpgroup
-          constexpr int CPR = D / 8;              // 16-byte chunks per row
+          __syncwarp();
 #pragma unroll
-          for (int x = wt; x < 32 * CPR; x += 128) {
-            const int r = x / CPR, cc = x % CPR;
+          for (int i = 0; i < 4; ++i) {
+            const int k = lane + 32 * i;
+            const int r = k >> 2, cc = k & 3;
             const int rp = s_rp[32 * wg + r];
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + r * L::kStgRow + cc * 16);
-            if (rp >= 0) *reinterpret_cast<uint4*>(p.dq_part + (int64_t)rp * D + cc * 8) = v;
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 64 + cc * 16);
+            if (rp >= 0) *reinterpret_cast<uint4*>(p.dq_part + (int64_t)rp * D + 32 * q4 + cc * 8) = v;
           }
+          __syncwarp();
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(b_e);
-          mbar_arrive(&qempty[s]);
+          mbar_arrive(&sempty[u % 3]);
           if (ch == nch - 1) mbar_arrive(kvempty);
         }
       }
       if (!ok) break;
-      // ---- block end: dK (x scale), dV from TMEM; dk_idx share from registers ----
+      // ---- block end: dK (x scale), dV and the dk_idx share from TMEM ----
       const bool in = j < p.N;
       __nv_bfloat16* dk_row = p.dk + (((int64_t)b * p.N + j) * p.H_kv + g) * D;
       __nv_bfloat16* dv_row = p.dv + (((int64_t)b * p.N + j) * p.H_kv + g) * D;
@@ -568,6 +605,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int x = wg * (D / 2); x < (wg + 1) * (D / 2); ++x) {
             dk_row[x] = __float2bfloat16(0.f);
             dv_row[x] = __float2bfloat16(0.f);
+          }
+          if (32 * wg < p.DI) {
+            float4* dst = reinterpret_cast<float4*>(
+                p.dki_part + (((int64_t)b * p.H_kv + g) * p.N + j) * p.DI + 32 * wg);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) dst[x] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
       } else {
@@ -598,29 +641,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        // dk_idx share of group g: warpgroup wg holds d_idx columns 32 wg .. 32 wg + 31
+        if (32 * wg < p.DI) {
+          uint32_t a[32];
+          tmem_ld_32x32b_x32(tmem + lb + cDKI + 32 * wg, a);
+          tmem_wait_ld();
+          if (in) {
+            float4* dst = reinterpret_cast<float4*>(
+                p.dki_part + (((int64_t)b * p.H_kv + g) * p.N + j) * p.DI + 32 * wg);
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              dst[x] = make_float4(__uint_as_float(a[4 * x]) * p.sidx, __uint_as_float(a[4 * x + 1]) * p.sidx,
+                                   __uint_as_float(a[4 * x + 2]) * p.sidx, __uint_as_float(a[4 * x + 3]) * p.sidx);
+          }
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_kfree);
         ++nkeys;
       }
-      // dk_idx share of group g for this warp's 16 keys (C-fragment layout)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int jj = c * 128 + kw + (lane >> 2) + hh * 8;
-        if (jj < p.N) {
-          float* dst = p.dki_part + (((int64_t)b * p.H_kv + g) * p.N + jj) * p.DI;
-#pragma unroll
-          for (int n = 0; n < 8; ++n) {
-            const int col = n * 8 + (lane & 3) * 2;
-            if (col < p.DI) {
-              dst[col] = dki[n][2 * hh] * p.sidx;
-              dst[col + 1] = dki[n][2 * hh + 1] * p.sidx;
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int n = 0; n < 8; ++n) dki[n][0] = dki[n][1] = dki[n][2] = dki[n][3] = 0.f;
     }
     if (!ok) *abort_flag = 1;
 #pragma unroll
