@@ -53,6 +53,21 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "of fallback"
 
 
+def job_rate(local_ms, units_per_rank, world, device=None):
+    """Whole-job throughput of `world` ranks that each processed `units_per_rank`
+    units in `local_ms`: the job takes as long as its slowest rank (max over ranks,
+    an all-reduce on the default process group when world > 1).  Returns
+    (max_ms, units of all ranks per second)."""
+    ms = float(local_ms)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, units_per_rank * world / (ms / 1000.0)
+
+
 # ----------------------------------------------------------------------------
 # algorithmic work (what the method must compute, not what a kernel happens to do)
 # ----------------------------------------------------------------------------
@@ -264,13 +279,7 @@ def run_ours(args, cfg, rank, world):
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {_lib.status_string(st)}")
 
-    ms = t_start.elapsed_time(t_end) / K
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    tokens = cfg.B * cfg.N * world
-    value = tokens / (ms / 1000.0)
+    ms, value = job_rate(t_start.elapsed_time(t_end) / K, cfg.B * cfg.N, world, dev)
 
     kern_ms = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in kev.items()}
     phase_ms = {
@@ -311,12 +320,7 @@ def run_ours(args, cfg, rank, world):
         kl_host.copy_(g["kl"], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_val = tokens / (e2e_ms / 1000.0)
+    e2e_ms, e2e_val = job_rate(e0.elapsed_time(e1) / e2e_steps, cfg.B * cfg.N, world, dev)
     del pinned, dbuf
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
