@@ -9,15 +9,18 @@
 //
 // A tile is one key block c of one (batch, group) and 128 rows = 128/G gathered
 // queries x G heads.  Per CTA (persistent, a contiguous range of tiles):
-//   warps 4-7  loaders: gather the tile's q rows with cp.async into a 3-stage ring
+//   warps 8-10 loaders: gather the tile's q rows with cp.async into a 3-stage ring
 //              in the 128-byte-swizzled K-major layout tcgen05 reads; one thread
 //              TMA-loads K and V of the block when the key changes;
-//   warp 8     TMEM owner + one MMA thread: S = Q K^T (M=N=128, K=d) into a 2-deep
+//   warp 11    TMEM owner + one MMA thread: S = Q K^T (M=N=128, K=d) into a 2-deep
 //              TMEM ring, then O = P V with V as an MN-major operand;
-//   warps 0-3  softmax (thread = row = TMEM lane): tcgen05.ld S, causal mask, max,
-//              exp2, sum, P (bf16) into smem for the PV MMA; then tcgen05.ld O,
-//              normalise and store the bf16 partial and its lse.
-// Every wait is bounded; on expiry the CTA unwinds and records
+//   warps 0-7  two softmax warpgroups taking alternate tiles (thread = row = TMEM
+//              lane): one pass over S with the max of the first 32 columns as the
+//              exp2 offset (exact two-pass fallback when a row sum would overflow),
+//              P (bf16) into smem for the PV MMA, S released at once; then O from
+//              TMEM, normalised, stored as bf16 partials with their lse.
+// S and O have separate release barriers, so the next S MMA of a warpgroup overlaps
+// its O epilogue.  Every wait is bounded; on expiry the CTA unwinds and records
 // MSA_ERR_DEVICE_TIMEOUT.
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -28,8 +31,8 @@
 namespace msa {
 namespace {
 
-constexpr int kTcThreads = 416;  // 13 warps: 8 softmax, 4 loaders, 1 MMA
-constexpr int kLoadThreads = 128;
+constexpr int kTcThreads = 384;  // 12 warps: 8 softmax, 3 loaders, 1 MMA
+constexpr int kLoadThreads = 96;
 constexpr int kQStages = 3;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -58,9 +61,9 @@ struct TcLayout {
   static constexpr int kQ = kV + kTile;                  // kQStages tiles
   static constexpr int kP = kQ + kQStages * kTile;       // [2][128 rows][128 keys] bf16
   static constexpr int kBar = kP + 2 * 2 * kHalf;
-  // barriers: kvfull, kvempty, qfull[3], qempty[3], sfull[2], ofull[2], tfree[2],
-  //           pfull[2], pempty[2], mmadone
-  static constexpr int kNumBars = 2 + 2 * kQStages + 6 + 5;
+  // barriers: kvfull, kvempty, qfull[3], qempty[3], sfull[2], ofull[2], sfree[2],
+  //           ofree[2], pfull[2], pempty[2], mmadone
+  static constexpr int kNumBars = 2 + 2 * kQStages + 8 + 5;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -108,6 +111,13 @@ __device__ __forceinline__ uint32_t sw128_row(int r, int chunk) {
   return (uint32_t)(r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
 }
 
+// The value of x, opaque to the optimiser: addresses derived from it are recomputed
+// inside a loop instead of being hoisted and held in registers across it.
+__device__ __forceinline__ int opaque(int x) {
+  asm volatile("" : "+r"(x));
+  return x;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -133,8 +143,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* qempty = qfull + kQStages;
   uint64_t* sfull = qempty + kQStages;
   uint64_t* ofull = sfull + 2;
-  uint64_t* tfree = ofull + 2;
-  uint64_t* pfull = tfree + 2;   // [2]
+  uint64_t* sfree = ofull + 2;   // [2] softmax done reading S[b]
+  uint64_t* ofree = sfree + 2;   // [2] epilogue done reading O[b]
+  uint64_t* pfull = ofree + 2;   // [2]
   uint64_t* pempty = pfull + 2;  // [2]
   uint64_t* mmadone = pempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
@@ -157,7 +168,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sfull[b], 1);
       mbar_init(&ofull[b], 1);
-      mbar_init(&tfree[b], 4);  // one arrive per softmax warp
+      mbar_init(&sfree[b], 4);  // one arrive per softmax warp
+      mbar_init(&ofree[b], 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&pfull[b], 4);
@@ -167,7 +179,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 12) {
+  if (warp == 11) {
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
   }
@@ -178,12 +190,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // TMEM columns: S[b] at 128*b, O[b] at 256 + 128*b
 
   if (n_tiles > 0) {
-    if (warp >= 8 && warp < 12) {
+    if (warp >= 8 && warp < 11) {
       // ================================ loaders =================================
       // Order per tile: gather q(u) -> publish q(u-1) -> (new block) swap K/V.  The
       // swap waits for the previous block's last PV MMA, which needs q(u-1)
       // published first.
-      const int lt = threadIdx.x - 256;  // 0..63
+      const int lt = threadIdx.x - 256;  // 0 .. kLoadThreads-1
       KeyCursor kc;
       int prev_key = -1, kv_loads = 0, kv_issued = 0;
       for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
@@ -251,7 +263,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!*abort_flag) mbar_arrive(&qfull[(n_tiles - 1) % kQStages]);
       // teardown: the last K/V TMA issued must have landed
       if (lt == 0 && kv_issued > 0) mbar_wait(kvfull, (kv_issued - 1) & 1, 1000000000ull);
-    } else if (warp == 12) {
+    } else if (warp == 11) {
       // ============================== MMA issuer ================================
       if (lane == 0) {
         constexpr uint32_t idesc_s = umma_idesc_bf16_f32(128, 128);
@@ -264,7 +276,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         auto issue_s = [&](int u) -> bool {
           const int st = u % kQStages, b = u & 1;
           if (!mbar_wait(&qfull[st], (u / kQStages) & 1, p.wait_ns, abort_flag)) return false;
-          if (!mbar_wait(&tfree[b], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag)) return false;
+          if (!mbar_wait(&sfree[b], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag)) return false;
           tc_fence_after();
           const uint32_t aQ = smem_u32(sQ + st * L::kTile);
 #pragma unroll
@@ -295,7 +307,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const bool next_same = has_next && peek.at(p.toff, p.keys, t_begin + u + 1) == cur_key;
           if (next_same) ok = issue_s(u + 1);
           if (!ok) break;
-          if (!mbar_wait(&pfull[b], (u >> 1) & 1, p.wait_ns, abort_flag)) {
+          if (!mbar_wait(&pfull[b], (u >> 1) & 1, p.wait_ns, abort_flag) ||
+              !mbar_wait(&ofree[b], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag)) {
             ok = false;
             break;
           }
@@ -326,7 +339,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // P tile wg, so the two groups' softmax and epilogues overlap.
       const int wg = warp >> 2;
       const int row = (warp & 3) * 32 + lane;  // TMEM lane
-      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
       uint8_t* sPw = sP + wg * 2 * L::kHalf;
       KeyCursor kc;
       for (int u = wg; u < n_tiles; u += 2) {
@@ -339,68 +351,95 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int qi = row / G;
         const int ent = qi < ne ? __ldg(&p.entries[e0 + qi]) : -1;
         const int i = ent >> 5;
+        const int rowv = opaque(row), lanev = opaque(lane);
         bool ok = __all_sync(0xffffffffu, mbar_wait(&sfull[b], (u >> 1) & 1, p.wait_ns, abort_flag));
         if (!ok) {
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
-        // causal mask j <= i (and j < N), scaled to log2 units; two passes over the
-        // TMEM row (max, then exp/sum/pack), 32 columns at a time
+        // causal mask j <= i (and j < N), scaled to log2 units
         const int jlim = ent >= 0 ? min(i, p.N - 1) - c * 128 : -1;  // last valid column
         // blocks wholly before every query of the warp need no mask (the usual case)
         const bool full = __all_sync(0xffffffffu, jlim >= 127);
-        float m = -INFINITY;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + 128 * b + 32 * h, r);
-          tmem_wait_ld();
-          if (full) {
-#pragma unroll
-            for (int x = 0; x < 32; x += 2)
-              m = fmax3(m, __uint_as_float(r[x]), __uint_as_float(r[x + 1]));
-          } else {
-#pragma unroll
-            for (int x = 0; x < 32; x += 2)
-              m = fmax3(m, 32 * h + x <= jlim ? __uint_as_float(r[x]) : -INFINITY,
-                        32 * h + x + 1 <= jlim ? __uint_as_float(r[x + 1]) : -INFINITY);
-          }
-        }
-        const float ms = m == -INFINITY ? 0.f : m * p.scale_log2;
         // P (bf16) into this group's K-major smem operand, once its previous PV is done
         ok = __all_sync(0xffffffffu, mbar_wait(&pempty[b], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag));
         if (!ok) {
           *abort_flag = 1;
           break;
         }
-        float l = 0.f;
+        const uint32_t srow = tmem + ((uint32_t)(rowv & ~31) << 16) + 128 * b;
+        // exp2 of 64 scores (columns 64 hp ..) minus the offset ms -> P, row sum
+        auto exp_pack = [&](const uint32_t (&r)[64], int hp, float ms, float& l) {
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + 128 * b + 32 * h, r);
+          for (int ch = 0; ch < 8; ++ch) {  // 8 columns -> one 16-byte P chunk
+            float e[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              const float v = __uint_as_float(r[8 * ch + x]) * p.scale_log2 - ms;
+              e[x] = (full || 64 * hp + 8 * ch + x <= jlim) ? ex2_fast(v) : 0.f;
+              l += e[x];
+            }
+            uint4 w;
+            w.x = pack_bf16(e[0], e[1]);
+            w.y = pack_bf16(e[2], e[3]);
+            w.z = pack_bf16(e[4], e[5]);
+            w.w = pack_bf16(e[6], e[7]);
+            *reinterpret_cast<uint4*>(sPw + kmaj_off<128>(rowv, 8 * hp + ch)) = w;
+          }
+        };
+        auto load64 = [&](uint32_t (&r)[64], int hp) {
+          tmem_ld_32x32b_x32(srow + 64 * hp, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld_32x32b_x32(srow + 64 * hp + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
           tmem_wait_ld();
-          float e[32];
+        };
+        // One pass: the offset is the max of the first 32 columns (column 0, the block's
+        // first key, is visible to every real row).  The partial lse ms + log2(l) is exact
+        // for any offset; only overflow matters, so a row sum above 2^64 falls back to
+        // the exact row max and a second pass.
+        float ms, l = 0.f;
+        {
+          uint32_t r[64];
+          load64(r, 0);
+          float m0 = -INFINITY;
           if (full) {
 #pragma unroll
-            for (int x = 0; x < 32; ++x) e[x] = ex2_fast(__uint_as_float(r[x]) * p.scale_log2 - ms);
+            for (int x = 0; x < 32; x += 2) m0 = fmax3(m0, __uint_as_float(r[x]), __uint_as_float(r[x + 1]));
           } else {
 #pragma unroll
-            for (int x = 0; x < 32; ++x)
-              e[x] = 32 * h + x <= jlim ? ex2_fast(__uint_as_float(r[x]) * p.scale_log2 - ms) : 0.f;
+            for (int x = 0; x < 32; x += 2)
+              m0 = fmax3(m0, x <= jlim ? __uint_as_float(r[x]) : -INFINITY,
+                         x + 1 <= jlim ? __uint_as_float(r[x + 1]) : -INFINITY);
           }
+          ms = m0 == -INFINITY ? 0.f : m0 * p.scale_log2;
+          exp_pack(r, 0, ms, l);
+          load64(r, 1);
+          exp_pack(r, 1, ms, l);
+        }
+        if (__any_sync(0xffffffffu, l > 0x1p64f)) {  // rare: exact max, second pass
+          float m = -INFINITY;
+#pragma unroll 1
+          for (int h = 0; h < 4; ++h) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(srow + 32 * h, r);
+            tmem_wait_ld();
 #pragma unroll
-          for (int x = 0; x < 32; ++x) l += e[x];
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint4 w;
-            w.x = pack_bf16(e[8 * ch + 0], e[8 * ch + 1]);
-            w.y = pack_bf16(e[8 * ch + 2], e[8 * ch + 3]);
-            w.z = pack_bf16(e[8 * ch + 4], e[8 * ch + 5]);
-            w.w = pack_bf16(e[8 * ch + 6], e[8 * ch + 7]);
-            *reinterpret_cast<uint4*>(sPw + kmaj_off<128>(row, 4 * h + ch)) = w;
+            for (int x = 0; x < 32; ++x)
+              m = fmaxf(m, 32 * h + x <= jlim ? __uint_as_float(r[x]) : -INFINITY);
+          }
+          ms = m == -INFINITY ? 0.f : m * p.scale_log2;
+          l = 0.f;
+#pragma unroll 1
+          for (int hp = 0; hp < 2; ++hp) {
+            uint32_t r[64];
+            load64(r, hp);
+            exp_pack(r, hp, ms, l);
           }
         }
+        // S[b] has been read: the next S MMA into it may start
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfree[b]);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -423,11 +462,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
           uint8_t* stg = sPw + h * L::kHalf + (warp & 3) * 32 * 128;
+          uint32_t r2[2][32];
+          const uint32_t orow = tmem + ((uint32_t)(rowv & ~31) << 16) + 256 + 128 * b + 64 * h;
+          tmem_ld_32x32b_x32(orow, r2[0]);
+          tmem_ld_32x32b_x32(orow + 32, r2[1]);
+          tmem_wait_ld();
+          if (h == D / 64 - 1) {  // O[b] has been read: the next PV into it may start
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ofree[b]);
+          }
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tmem + lane_base + 256 + 128 * b + 64 * h + 32 * hh, r);
-            tmem_wait_ld();
+            const uint32_t (&r)[32] = r2[hh];
 #pragma unroll
             for (int x = 0; x < 32; x += 8) {
               uint4 w;
@@ -435,13 +482,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               w.y = pack_bf16(__uint_as_float(r[x + 2]) * inv, __uint_as_float(r[x + 3]) * inv);
               w.z = pack_bf16(__uint_as_float(r[x + 4]) * inv, __uint_as_float(r[x + 5]) * inv);
               w.w = pack_bf16(__uint_as_float(r[x + 6]) * inv, __uint_as_float(r[x + 7]) * inv);
-              *reinterpret_cast<uint4*>(stg + sw128_row(lane, 4 * hh + x / 8)) = w;
+              *reinterpret_cast<uint4*>(stg + sw128_row(lanev, 4 * hh + x / 8)) = w;
             }
           }
           __syncwarp();
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const int x = lane + 32 * k;
+            const int x = lanev + 32 * k;
             const int rr = x >> 3, cc = x & 7;
             const int pr = __shfl_sync(0xffffffffu, prow, rr);
             const uint4 v = *reinterpret_cast<const uint4*>(stg + sw128_row(rr, cc));
@@ -449,9 +496,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           __syncwarp();
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tfree[b]);
       }
     }
   }
@@ -459,7 +503,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) set_status(p.status, MSA_ERR_DEVICE_TIMEOUT);
-  if (warp == 12) {
+  if (warp == 11) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -88,6 +88,33 @@ def test_fwd_matches_oracle(name, n_rows):
     assert eo <= O_TOL and el <= LSE_TOL
 
 
+def test_fwd_peaked_scores_matches_oracle():
+    """Keys in the last quarter of every block scaled by 40: their scores sit far above
+    the max of a block's first 32 columns, the forward's provisional softmax offset, so
+    its row sums exceed 2^64 and the exact two-pass path runs for most rows."""
+    cfg = T.with_(name="peaked", seed=42)
+    h = dict(host_inputs(cfg))
+    k = synth.bf16_bits_to_f32(h["k"]).copy()
+    peak = (np.arange(cfg.N) % cfg.Bk) >= 96
+    k[:, peak] *= 40.0
+    h["k"] = synth.f32_to_bf16_bits(k)
+    d = {n: to_dev(h[n]) for n in ("q", "k", "v")}
+    bi_ref, _, _ = oracle.select(cfg, h)
+    bi_full = bi_ref.reshape(cfg.B, cfg.N, cfg.H_kv, cfg.topk).transpose(0, 2, 1, 3)
+    block_idx = torch.from_numpy(np.ascontiguousarray(bi_full, dtype=np.int32)).cuda()
+    o, lse = ops.msa_fwd(d["q"], d["k"], d["v"], block_idx, scale=cfg.scale, d_idx=cfg.d_idx)
+    assert ops.device_status() == 0
+    o_ref, lse_ref, _ = oracle.forward(cfg, h, bi_ref, index=False)
+    o_g = f64(o).reshape(cfg.B * cfg.N, cfg.H_q, cfg.d)
+    lse_g = lse.cpu().numpy().transpose(0, 2, 1).reshape(cfg.B * cfg.N, cfg.H_q)
+    assert np.isfinite(o_g).all() and np.isfinite(lse_g).all()
+    eo = np.abs(o_g - o_ref).max()
+    el = np.abs(lse_g - lse_ref).max()
+    spread = (lse_ref.max() - lse_ref.min())
+    print(f"peaked: o max-abs {eo:.3e}  lse max-abs {el:.3e}  lse spread {spread:.1f}")
+    assert eo <= O_TOL and el <= LSE_TOL
+
+
 def test_device_wait_timeout_is_reported_not_hung():
     """A kernel whose producer withholds its loads: the consumer's bounded wait runs
     out, the kernel records MSA_ERR_DEVICE_TIMEOUT and returns; the context stays
