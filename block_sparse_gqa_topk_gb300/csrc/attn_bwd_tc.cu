@@ -11,18 +11,22 @@
 // in block-major order, heaviest blocks first) and walks the block's inverted list in
 // chunks of 64 rows (64/G gathered queries x G heads; 16 query slots).
 //   tcgen05 (one MMA thread, accumulators in TMEM, every M = 128):
-//     (1) S^T  = K Q^T     M=128 keys, N=64 rows, K=d
-//     (2) dP^T = V dO^T    M=128 keys, N=64 rows, K=d
-//     (3) dV  += P^T dO    M=128 keys, N=d,  K=64 rows   (dO as MN-major B)
-//     (4) dK  += dS^T Q    M=128 keys, N=d,  K=64 rows   (Q as MN-major B)
-//     (5) dQ^T = K^T dS^T  M=d, N=64 rows, K=128 keys    (both MN-major)
-//   epilogue warps 0-7 (two warpgroups, each owning 32 of the 64 row columns):
-//     E1  P^T = exp(scale S^T - lse), dS^T = P^T (dP^T - D) -> smem; p_T (teacher)
-//     KL  (mma.sync, while (3)-(5) run) z = k_idx q_idx^T, p_I, dz = w (p_I - p_T),
-//         dk_idx += dz^T q_idx (registers), dq_idx = dz k_idx -> per-slot partials
-//     E2  dQ^T columns -> bf16 per-slot partials
-// Chunk u+1's (1)(2) overlap chunk u's E2.  After the block's last chunk dK, dV
-// (TMEM) and dk_idx (registers) are written once: no atomics on dk/dv/dk_idx.
+//     (1) S^T  = K Q^T          M=128 keys, N=64 rows, K=d
+//     (2) dP^T = V dO^T         M=128 keys, N=64 rows, K=d
+//     (z) z^T  = k_idx q_idx^T  M=128 keys, N=16 slots, K=d_idx   (into the dQ^T columns)
+//     (3) dV  += P^T dO         M=128 keys, N=d,  K=64 rows   (dO as MN-major B)
+//     (4) dK  += dS^T Q         M=128 keys, N=d,  K=64 rows   (Q as MN-major B)
+//     (5) dQ^T = K^T dS^T       M=d, N=64 rows, K=128 keys    (both MN-major)
+//     (6) dk_idx += dz^T q_idx  M=128 keys, N=d_idx, K=16 slots
+//   epilogue warps 0-7 (two warpgroups, each owning 32 of the 64 row columns; thread =
+//   key):
+//     E1  P^T = exp(scale S^T - lse), dS^T = P^T (dP^T - D) -> smem; the teacher p_T
+//         (group mean of P) stays in registers; with z^T from TMEM: p_I, the KL and
+//         dz = w (p_I - p_T) for the warpgroup's slots -> dz^T in smem
+//     dq_idx (mma.sync, per warpgroup, while (3)-(6) run): dq_idx^T = k_idx^T dz^T
+//     E2  dQ^T from TMEM (thread = d) -> bf16 per-slot partials
+// Chunk u+1's (1)(2) overlap chunk u's E2.  After the block's last chunk dK, dV and
+// dk_idx (TMEM) are written once: no atomics on dk/dv/dk_idx.
 // Warps 8-9: loaders (cp.async gathers of q, dO, q_idx rows and k_idx; TMA for K, V).
 // Warp 10: TMEM owner and MMA issuer.
 #include <cudaTypedefs.h>
@@ -39,7 +43,6 @@ constexpr int kEpiWarps = 8;
 constexpr int kLoadThreads = 64;
 constexpr int kRows = 64;  // rows per chunk
 constexpr int kQS = 16;    // query slots per chunk
-constexpr int kTS = 17;    // teacher row stride (floats): conflict-free column access
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -84,14 +87,13 @@ struct BL {
   static constexpr int kSmall0 = kBig0 + 2 * kBig;
   static constexpr int kPT = kSmall0 + 3 * kSmall;    // P^T [128][64] bf16 (SW128)
   static constexpr int kdST = kPT + 128 * 128;        // dS^T [128][64]
-  static constexpr int kTeach = kdST + 128 * 128;     // p_T float [128][17] (padded rows)
   // dz^T bf16 [128 keys][16 slots]: 32-byte rows in the 32-byte swizzle, the K-major A
   // operand of the dk_idx MMA
-  static constexpr int kDZ = (kTeach + 128 * 17 * 4 + 1023) & ~1023;
+  static constexpr int kDZ = kdST + 128 * 128;
   // dQ staging, one [32 rows][32 d] bf16 block (64-byte rows) per epilogue warp
   static constexpr int kStg = kDZ + 128 * 32;
   static constexpr int kBar = kStg + 8 * 32 * 64;
-  static constexpr int kNumBars = 20;
+  static constexpr int kNumBars = 18;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -120,7 +122,8 @@ __device__ __forceinline__ void fence_async_smem() {
 }
 
 // TMEM columns
-constexpr uint32_t cDK = 0, cDV = 128, cST = 256, cDPT = 320, cDQT = 384, cDKI = 448;
+// z^T (16 columns) lives in the dQ^T columns between E2 of one chunk and (5) of the next.
+constexpr uint32_t cDK = 0, cDV = 128, cST = 256, cDPT = 320, cDQT = 384, cDKI = 448, cZ = cDQT;
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -145,9 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* b_key = bar + 13;   // block's MMAs done
   uint64_t* b_kfree = bar + 14; // block's accumulators read out
   uint64_t* mmadone = bar + 15;
-  uint64_t* e_sync2 = bar + 16;  // every epilogue warp has written its dz (the dk_idx MMA waits)
-  uint64_t* zfree = bar + 17;    // the dk_idx MMA has read dz
-  uint64_t* e_wg = bar + 18;     // [2] a warpgroup's four warps have written their dz
+  uint64_t* b_z = bar + 16;      // z^T = k_idx q_idx^T in the dQ^T columns
+  uint64_t* e_wg = bar + 17;     // [2] a warpgroup's four warps have written their dz
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
 
@@ -169,8 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_key, 1);
     mbar_init(b_kfree, kEpiWarps);
     mbar_init(mmadone, 1);
-    mbar_init(e_sync2, kEpiWarps);
-    mbar_init(zfree, 1);
+    mbar_init(b_z, 1);
     mbar_init(&e_wg[0], 4);
     mbar_init(&e_wg[1], 4);
     *abort_flag = 0;
@@ -302,20 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t i12 = idesc(128, 64, 0, 0), i34 = idesc(128, D, 0, 1);
       constexpr uint32_t i5 = idesc(128, 64, 1, 1);
       constexpr uint32_t iki = idesc(128, 64, 0, 1);  // dk_idx += dz^T q_idx (K = 16 slots)
-      const uint32_t aDZ = smem_u32(sm + L::kDZ);
+      constexpr uint32_t iz = idesc(128, 16, 0, 0);   // z^T = k_idx q_idx^T (K = d_idx)
+      const uint32_t aDZ = smem_u32(sm + L::kDZ), aKi = smem_u32(sm + L::kKi);
       int u = 0, nkeys = 0;
       bool ok = true, issued = false;
-      int pend = -1, pend_ch = 0;  // chunk whose dk_idx MMA is not issued yet (same block)
-      // dk_idx(v): once every epilogue warp has written chunk v's dz
-      auto issue_dki = [&](int v, int vch) -> bool {
-        if (!mbar_wait(e_sync2, v & 1, p.wait_ns, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t aQi = smem_u32(sm + L::kSmall0 + (v % 3) * L::kSmall + L::kSQi);
-        tc_mma_bf16(tmem + cDKI, desc_sw32(aDZ), desc_mn(aQi, L::kQH), iki, vch > 0 ? 1u : 0u);
-        tc_commit(zfree);
-        tc_commit(&sempty[v % 3]);
-        return true;
-      };
       for (int64_t kk = blockIdx.x; kk < p.keys && ok; kk += gridDim.x) {
         const int c = (int)(kk / BG), bg = (int)(kk % BG);
         const int key = bg * p.nb + c;
@@ -326,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = u & 1;
           const uint32_t st = smem_u32(sm + L::kBig0 + s * L::kBig);
           const uint32_t aQ = st + L::kSQ, adO = st + L::kSdO;
+          const uint32_t aQi = smem_u32(sm + L::kSmall0 + (u % 3) * L::kSmall + L::kSQi);
           ok = mbar_wait(&qfull[s], (u >> 1) & 1, p.wait_ns, abort_flag);
           if (ok && ch == 0) ok = mbar_wait(kvfull, nkeys & 1, p.wait_ns, abort_flag);
           if (ok && ch == 0 && nkeys > 0)
@@ -342,12 +334,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(b_s);
           issued = true;
-          if (pend >= 0) {
-            if (!(ok = issue_dki(pend, pend_ch))) break;
-            pend = -1;
-          }
-          if (!(ok = mbar_wait(b_p, u & 1, p.wait_ns, abort_flag))) break;
+          // z^T = k_idx q_idx^T (K = d_idx, zero-padded to 64) into the dQ^T columns once
+          // E2 of the previous chunk has read them; this commit also covers the previous
+          // chunk's dk_idx MMA, so E1 may then overwrite dz
           if (u > 0 && !(ok = mbar_wait(b_e, (u - 1) & 1, p.wait_ns, abort_flag))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc_mma_bf16(tmem + cZ, desc_k(aKi + k * 32), desc_k(aQi + k * 32), iz, k > 0);
+          tc_commit(b_z);
+          if (!(ok = mbar_wait(b_p, u & 1, p.wait_ns, abort_flag))) break;
           tc_fence_after();
           // (3) dV += P^T dO, (4) dK += dS^T Q     (K = 64 rows)
 #pragma unroll
@@ -361,15 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 8; ++k)
             tc_mma_bf16(tmem + cDQT, desc_mn(aK + k * 2048, L::kKH), desc_mn(adST + k * 2048, L::kKH),
                         i5, k > 0);
+          // (6) dk_idx += dz^T q_idx                 (K = 16 query slots)
+          tc_mma_bf16(tmem + cDKI, desc_sw32(aDZ), desc_mn(aQi, L::kQH), iki, ch > 0 ? 1u : 0u);
           tc_commit(b_q);
           tc_commit(&bempty[s]);
+          tc_commit(&sempty[u % 3]);
           if (ch == nch - 1) {
-            if (!(ok = issue_dki(u, ch))) break;
             tc_commit(kvempty);
             tc_commit(b_key);
-          } else {
-            pend = u;
-            pend_ch = ch;
           }
         }
         if (ok) ++nkeys;
@@ -387,7 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
     const int q4 = warp & 3;               // this warp's 32 keys (E1, KL) / 32 d (E2)
     const uint8_t* sKi = sm + L::kKi;
-    float* sTeach = reinterpret_cast<float*>(sm + L::kTeach);
     uint8_t* sDZ = sm + L::kDZ;
     double kl = 0.0;
     int u = 0, nkeys = 0;
@@ -411,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* s_li = reinterpret_cast<const float*>(ss + L::kSLi);
         const uint8_t* sQi = ss + L::kSQi;
         ok = __all_sync(0xffffffffu, mbar_wait(&qfull[s], (u >> 1) & 1, p.wait_ns, abort_flag) &&
-                                         mbar_wait(b_s, u & 1, p.wait_ns, abort_flag));
+                                         mbar_wait(b_s, u & 1, p.wait_ns, abort_flag) &&
+                                         mbar_wait(b_z, u & 1, p.wait_ns, abort_flag));
         if (!ok) break;
         tc_fence_after();
         // ---- E1: this warpgroup's 32 rows of key tl: P^T, dS^T, teacher ----
@@ -459,76 +454,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                   make_uint4(dk2[4 * cc], dk2[4 * cc + 1], dk2[4 * cc + 2], dk2[4 * cc + 3]);
             }
           }
+          // ---- KL for key tl and this warpgroup's QH query slots (teacher in registers) ----
+          uint32_t zr[QH];
+          if constexpr (QH == 8) {
+            tmem_ld_32x32b_x8(tmem + lb + cZ + QH * wg, zr);
+          } else {
+            tmem_ld_32x32b_x4(tmem + lb + cZ + QH * wg, zr);
+          }
+          tmem_wait_ld();
+          float klc = 0.f;
+          uint32_t dzp[QH / 2];
 #pragma unroll
-          for (int q = 0; q < QH; ++q) sTeach[tl * kTS + wg * QH + q] = pt[q] * (1.f / G);
+          for (int q2 = 0; q2 < QH; q2 += 2) {
+            float dz[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int q = q2 + e, sl = QH * wg + q;
+              const bool valid = j <= s_qi[sl];  // s_qi = -1 for padding slots
+              const float zl2 = __uint_as_float(zr[q]) * p.sidx_log2 - s_li[sl] * kLog2e;  // log2 p_I
+              const float pI = valid ? ex2_fast(zl2) : 0.f;
+              const float pT = pt[q] * (1.f / G);  // group-averaged main probability
+              if (valid && pT > 0.f) klc += pT * (__log2f(pT) - zl2);
+              dz[e] = valid ? p.w * (pI - pT) : 0.f;
+            }
+            dzp[q2 / 2] = pack_bf16(dz[0], dz[1]);
+          }
+          kl += (double)(klc * kLn2);
+          if constexpr (QH == 8) {  // slots 8 wg .. 8 wg + 7: one 16-byte chunk of the dz row
+            *reinterpret_cast<uint4*>(sDZ + swz32(tl, wg)) = make_uint4(dzp[0], dzp[1], dzp[2], dzp[3]);
+          } else {                  // slots 4 wg .. 4 wg + 3: half of chunk 0
+            *reinterpret_cast<uint2*>(sDZ + swz32(tl, 0) + 8 * wg) = make_uint2(dzp[0], dzp[1]);
+          }
         }
         fence_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_p);
-        // ---- KL on mma.sync (overlaps the MMAs (3)-(5)) ----
-        // This warp: keys 32 q4 .. 32 q4 + 31 (its own E1 lanes, so the teacher it reads
-        // was written by this warp) x the query slots of its warpgroup (n8 tile nt).
-        constexpr int NT = (G == 4) ? 1 : 0;  // slots per n8 tile belong to one warpgroup (G=4)
-        const int nt = NT ? wg : 0;
-        if (u > 0) {  // the previous chunk's dk_idx MMA must be done reading dz
-          ok = __all_sync(0xffffffffu, mbar_wait(zfree, (u - 1) & 1, p.wait_ns, abort_flag));
-          if (!ok) break;
-        }
-        __syncwarp();  // teacher rows of this warp's lanes
-        {
-          float zt[2][4];
-#pragma unroll
-          for (int m = 0; m < 2; ++m) zt[m][0] = zt[m][1] = zt[m][2] = zt[m][3] = 0.f;
-#pragma unroll
-          for (int kp = 0; kp < 2; ++kp) {  // two d_idx steps of 16 per x4 load (zero-padded to 64)
-            uint32_t bq[4];
-            ldmatrix_x4(bq, sQi + sw128(8 * nt + (lane & 7), 4 * kp + (lane >> 3)));
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int kc = 2 * kp + h;
-#pragma unroll
-              for (int m = 0; m < 2; ++m) {
-                uint32_t a[4];
-                ldmatrix_x4(a, sKi + sw128(32 * q4 + 16 * m + (lane & 15), kc * 2 + (lane >> 4)));
-                mma_bf16_16816(zt[m], a, bq[2 * h], bq[2 * h + 1]);
-              }
-            }
-          }
-          const int qs0 = 8 * nt + (lane & 3) * 2;  // this lane's slot pair
-          const bool mine = NT ? true : ((lane & 3) >> 1) == wg;  // G=8: 4 slots per warpgroup
-          float klc = 0.f;
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            const int kl0 = 32 * q4 + 16 * m + (lane >> 2);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int qs = qs0 + (e & 1);
-              const int kloc = kl0 + ((e >> 1) << 3);
-              const bool valid = mine && c * 128 + kloc <= s_qi[qs];  // s_qi = -1 for padding
-              const float zl2 = zt[m][e] * p.sidx_log2 - s_li[qs] * kLog2e;  // log2 p_I
-              const float pI = valid ? ex2_fast(zl2) : 0.f;
-              const float pT = valid ? sTeach[kloc * kTS + qs] : 0.f;
-              if (pT > 0.f) klc += pT * (__log2f(pT) - zl2);
-              zt[m][e] = valid ? p.w * (pI - pT) : 0.f;  // dz
-            }
-            if (mine) {
-              *reinterpret_cast<uint32_t*>(sDZ + swz32(kl0, nt) + (lane & 3) * 4) =
-                  pack_bf16(zt[m][0], zt[m][1]);
-              *reinterpret_cast<uint32_t*>(sDZ + swz32(kl0 + 8, nt) + (lane & 3) * 4) =
-                  pack_bf16(zt[m][2], zt[m][3]);
-            }
-          }
-          kl += (double)(klc * kLn2);
-        }
-        fence_async_smem();  // dz is read by the dk_idx MMA (async proxy)
+        // dz of this warpgroup's slots complete for every key (dq_idx below reads all keys)
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(e_sync2);
-          mbar_arrive(&e_wg[wg]);
-        }
+        if (lane == 0) mbar_arrive(&e_wg[wg]);
         ok = __all_sync(0xffffffffu, mbar_wait(&e_wg[wg], u & 1, p.wait_ns, abort_flag));
         if (!ok) break;
+        // this warpgroup's slots are n8 tile nt of dz (G = 4); with G = 8 both warpgroups
+        // share tile 0 and each keeps its own four slots
+        constexpr int NT = (G == 4) ? 1 : 0;
+        const int nt = NT ? wg : 0;
         if (16 * q4 < p.DI) {
           // dq_idx^T (16 d x 8 slots of this warpgroup) = k_idx^T dz^T   (k = 128 keys)
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
