@@ -303,25 +303,43 @@ def run_ours(args, cfg, rank, world):
     total_flops = sum(flops.values())
 
     # ---- end to end through the public API with host buffers ----
+    # Every step copies its own inputs from pinned host memory (h2d bytes below) and
+    # reads its KL back to the host.  Two device input sets: the copy of step s+1 runs
+    # on a second stream while step s computes, as a training loop feeds its GPU.
     pinned = {n: torch.from_numpy(host[n].view(np.int16)).pin_memory() for n in names}
-    dbuf = {n: torch.empty_like(d[n]) for n in names}
-    kl_host = torch.empty(1, dtype=torch.float32).pin_memory()
-    h2d = sum(pinned[n].numel() * 2 for n in names)
+    bufs = [{n: torch.empty_like(d[n]) for n in names} for _ in range(2)]
     e2e_steps = max(1, min(K, args.e2e_steps))
+    kl_host = torch.empty(e2e_steps, dtype=torch.float32).pin_memory()
+    h2d = sum(pinned[n].numel() * 2 for n in names)
+    copy_stream = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event() for _ in range(2)]    # inputs of set i have landed
+    consumed = [torch.cuda.Event() for _ in range(2)]  # the step reading set i is done
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+
+    def h2d_into(i, first):
+        copy_stream.wait_event(e0 if first else consumed[i])
+        with torch.cuda.stream(copy_stream):
+            for n in names:
+                bufs[i][n].view(torch.int16).copy_(pinned[n], non_blocking=True)
+        copied[i].record(copy_stream)
+
     torch.cuda.synchronize()
     barrier()
     e0.record(stream)
-    for _ in range(e2e_steps):
-        for n in names:
-            dbuf[n].view(torch.int16).copy_(pinned[n], non_blocking=True)
-        _, g = step(dbuf)
-        kl_host.copy_(g["kl"], non_blocking=True)
+    h2d_into(0, True)
+    for si in range(e2e_steps):
+        i = si % 2
+        if si + 1 < e2e_steps:
+            h2d_into((si + 1) % 2, si == 0)
+        stream.wait_event(copied[i])
+        _, g = step(bufs[i])
+        consumed[i].record(stream)
+        kl_host[si:si + 1].copy_(g["kl"], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms, e2e_val = job_rate(e0.elapsed_time(e1) / e2e_steps, cfg.B * cfg.N, world, dev)
-    del pinned, dbuf
+    del pinned, bufs
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     cpu = None
