@@ -29,7 +29,8 @@ EXPORTS = ("msa_workspace_size", "msa_index_topk", "msa_fwd", "msa_bwd",
            "msa_get_device_status", "msa_status_string", "msa_debug_set",
            "msa_set_kernel_events", "msa_kernel_launch_count", "msa_index_topk_noalloc",
            "msa_noalloc_scratch_bytes", "msa_version", "msa_workspace_size_varlen",
-           "msa_index_topk_varlen", "msa_fwd_varlen", "msa_bwd_varlen")
+           "msa_index_topk_varlen", "msa_fwd_varlen", "msa_bwd_varlen",
+           "msa_decode_workspace_size", "msa_decode")
 
 MSA_KERNEL_INDEX = 0
 MSA_KERNEL_FWD = 1
@@ -98,6 +99,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_bwd_varlen.argtypes = [P, ip, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp,
                                    vp, vp, vp, vp, vp, sz, vp]
     lib.msa_bwd_varlen.restype = i32
+    lib.msa_decode_workspace_size.argtypes = [P]
+    lib.msa_decode_workspace_size.restype = sz
+    lib.msa_decode.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.msa_decode.restype = i32
     _lib = lib
     return lib
 
@@ -190,6 +195,15 @@ def msa_bwd_varlen(prob, cu_seqlens, q, k, v, o, lse, dO, q_idx, k_idx, block_id
     return load().msa_bwd_varlen(ctypes.byref(prob), arr, n, q, k, v, o, lse, dO, q_idx, k_idx,
                                  block_idx, lse_idx, float(kl_weight), dq, dk, dv, dq_idx, dk_idx,
                                  kl_out, ws, ws_bytes, stream)
+
+
+def msa_decode_workspace_size(prob: Problem) -> int:
+    return int(load().msa_decode_workspace_size(ctypes.byref(prob)))
+
+
+def msa_decode(prob, q, q_idx, k, v, k_idx, lens, block_idx, o, lse, ws, ws_bytes, stream) -> int:
+    return load().msa_decode(ctypes.byref(prob), q, q_idx, k, v, k_idx, lens, block_idx, o, lse,
+                             ws, ws_bytes, stream)
 
 
 def msa_version() -> int:

@@ -96,6 +96,11 @@ bool encode_tiled(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* 
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Shape checks shared by every entry point (msa_api.cu) and the device context of the
+// current device (status word, wait limit, SM count; MSA_ERR_UNSUPPORTED off sm_103).
+int validate_problem(const msa_problem_t* p, Shape* s);
+int device_ctx(Ctx* cx);
+
 // Launch bookkeeping (msa_api.cu): counts launches and records the profiling
 // events of msa_set_kernel_events around the named kernels.
 void note_launch(int n = 1);

@@ -109,6 +109,9 @@ cudaEvent_t g_ev[4][2] = {};
 
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+int validate_problem(const msa_problem_t* p, Shape* s) { return check_problem(p, s); }
+int device_ctx(Ctx* cx) { return make_ctx(cx); }
+
 void kernel_event(int kernel, bool before, cudaStream_t st) {
   cudaEvent_t ev = nullptr;
   {

@@ -274,3 +274,35 @@ def msa_bwd_varlen(q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx, kl_wei
                              _ptr(out["dk_idx"]), _ptr(out["kl"]), _ptr(ws), nws, _stream(dev))
     _lib.check(rc, "msa_bwd_varlen")
     return out
+
+
+# ---------------------------------------------------------------------------
+# Decode: one new token per sequence against its KV cache (see include/msa.h).
+# ---------------------------------------------------------------------------
+def msa_decode(q, q_idx, k, v, k_idx, lens, topk: int = 16, *, scale=None, Bk: int = 128):
+    """q [B,H_q,d], q_idx [B,H_kv,d_idx] (new token); k, v [B,Lmax,H_kv,d] and
+    k_idx [B,Lmax,d_idx] (caches); lens int32 [B] on the device (cache lengths including
+    the new token).  Returns (block_idx [B,H_kv,topk] int32, o [B,H_q,d] bf16,
+    lse [B,H_q] f32)."""
+    _need(q, "q", ndim=3)
+    _need(q_idx, "q_idx", ndim=3)
+    _need(k, "k", ndim=4)
+    _need(v, "v", ndim=4)
+    _need(k_idx, "k_idx", ndim=3)
+    _need(lens, "lens", torch.int32, ndim=1)
+    B, H_q, d = q.shape
+    _, Lmax, H_kv, _ = k.shape
+    d_idx = q_idx.shape[2]
+    if tuple(v.shape) != tuple(k.shape) or tuple(k_idx.shape) != (B, Lmax, d_idx) or lens.numel() != B:
+        raise ValueError("cache shapes must agree: k, v [B,Lmax,H_kv,d], k_idx [B,Lmax,d_idx], lens [B]")
+    prob = make_problem(B, Lmax, H_q, H_kv, d, d_idx, topk, Bk, True, scale, None)
+    dev = q.device
+    block_idx = torch.empty((B, H_kv, topk), dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H_q), dtype=torch.float32, device=dev)
+    nws = _lib.msa_decode_workspace_size(prob)
+    ws = _workspace(nws, dev)
+    rc = _lib.msa_decode(prob, _ptr(q), _ptr(q_idx), _ptr(k), _ptr(v), _ptr(k_idx), _ptr(lens),
+                         _ptr(block_idx), _ptr(o), _ptr(lse), _ptr(ws), nws, _stream(dev))
+    _lib.check(rc, "msa_decode")
+    return block_idx, o, lse

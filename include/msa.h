@@ -167,6 +167,30 @@ int msa_bwd_varlen(const msa_problem_t* p, const int32_t* cu_seqlens, int num_se
                    void* dq_idx, void* dk_idx, float* kl_out, void* workspace,
                    size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Decode (inference): one new query token per sequence against its KV cache.
+ *   The index branch scores the new token against the cached index keys, max-pools
+ *   them per Bk-token block, keeps the topk-1 best blocks wholly before its own block
+ *   plus its own block ("Cómo funcionan las dos ramas" ¶1-2; the block indices are then
+ *   reused by the main branch, Flash-MSA article ¶3), and the main branch attends over
+ *   those blocks' causally visible tokens.  The result is row lens[b]-1 of
+ *   msa_index_topk + msa_fwd run on the cache (up to rounding; near-tied blocks may be
+ *   chosen either way).
+ *   p->N is the cache capacity Lmax, p->B the number of sequences.
+ * In:  q [B][H_q][d], q_idx [B][H_kv][d_idx] (the new token's projections, bf16);
+ *      k, v [B][Lmax][H_kv][d], k_idx [B][Lmax][d_idx] (caches, bf16; the new token's
+ *      own k, v, k_idx already at row lens[b]-1);
+ *      lens: device int32 [B], 1 <= lens[b] <= Lmax (an invalid length is recorded as
+ *      MSA_ERR_ARG in the status word and treated as 1).
+ * Out: block_idx [B][H_kv][topk] (int32, ascending, -1 padded), o [B][H_q][d] (bf16),
+ *      lse [B][H_q] (float32).
+ * Workspace: msa_decode_workspace_size(p) bytes, 256-byte aligned.
+ */
+size_t msa_decode_workspace_size(const msa_problem_t* p);
+int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const void* k,
+               const void* v, const void* k_idx, const int32_t* lens, int32_t* block_idx, void* o,
+               float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status word
  * (MSA_OK or the first MSA_ERR_* a kernel recorded since the last read). */
 int msa_get_device_status(cudaStream_t stream, int* status);
