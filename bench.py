@@ -68,6 +68,44 @@ def job_rate(local_ms, units_per_rank, world, device=None):
     return ms, units_per_rank * world / (ms / 1000.0)
 
 
+def decode_leg(torch, ops, d, cfg, dev, stream, hbm_peak, calls=20):
+    """Decode (one new token per sequence) over 8 caches of the workload's length: mean
+    device time per call with L2 flushed before each call, and the algorithmic HBM bytes
+    a call must move (every cached index key, the K/V rows of the selected blocks, the
+    new token's q and the output)."""
+    Bd, L = 8, cfg.N
+    k = d["k"].expand(Bd, -1, -1, -1).contiguous()
+    v = d["v"].expand(Bd, -1, -1, -1).contiguous()
+    k_idx = d["k_idx"].expand(Bd, -1, -1).contiguous()
+    q_new = d["q"][0, L - 1].expand(Bd, -1, -1).contiguous()
+    qi_new = d["q_idx"][0, L - 1].expand(Bd, -1, -1).contiguous()
+    lens = torch.full((Bd,), L, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        ops.msa_decode(q_new, qi_new, k, v, k_idx, lens, cfg.topk, scale=cfg.scale)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(calls)]
+    for a, b in evs:
+        flush.zero_()
+        # keep the GPU busy while the host enqueues the call, so the events bracket the
+        # decode kernels only (not the host's launch latency)
+        torch.cuda._sleep(1_000_000)
+        a.record(stream)
+        ops.msa_decode(q_new, qi_new, k, v, k_idx, lens, cfg.topk, scale=cfg.scale)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    per_seq = (L * cfg.d_idx * 2 + cfg.H_kv * cfg.topk * cfg.Bk * cfg.d * 2 * 2
+               + (cfg.H_q * cfg.d + cfg.H_kv * cfg.d_idx) * 2 + cfg.H_q * cfg.d * 2)
+    nbytes = Bd * per_seq
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    del k, v, k_idx, flush
+    return {"batch": Bd, "cache_len": L, "ms_per_call": ms, "tokens_per_s": Bd / (ms / 1000.0),
+            "bound": "hbm", "bytes_per_call": nbytes, "achieved_gbs": gbs, "peak_gbs": hbm_peak,
+            "frac": gbs / hbm_peak, "l2": "flushed before each call",
+            "timing": "CUDA events around each call, queued behind a GPU spin"}
+
+
 # ----------------------------------------------------------------------------
 # algorithmic work (what the method must compute, not what a kernel happens to do)
 # ----------------------------------------------------------------------------
@@ -341,6 +379,12 @@ def run_ours(args, cfg, rank, world):
     e2e_ms, e2e_val = job_rate(e0.elapsed_time(e1) / e2e_steps, cfg.B * cfg.N, world, dev)
     del pinned, bufs
 
+    # ---- decode (inference) leg ----
+    dec = None
+    if not args.no_decode:
+        dec = decode_leg(torch, ops, d, cfg, dev, stream,
+                         float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))
+
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -367,6 +411,7 @@ def run_ours(args, cfg, rank, world):
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": 4, "steps": e2e_steps},
             "cpu_baseline": cpu,
+            "decode": dec,
             "gpu_launches": launches,
             "clocks": clk,
         }
@@ -384,6 +429,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=96)
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -8,14 +8,15 @@
 // over those blocks, split across blocks and combined.  For a cache of length L the
 // result equals row L-1 of the training path (msa_index_topk + msa_fwd) on the cache.
 //
-// Decode moves the cache from HBM once and does little arithmetic per byte, so these
-// kernels run on the CUDA cores with coalesced 16-byte loads:
-//   decode_pool_kernel    one warp per earlier key block, all groups: pooled scores;
-//   decode_select_kernel  one CTA per (sequence, group): exact top-(k-1) by repeated
-//                         block-wide argmax (ties -> lower block), plus the own block;
+// Decode moves the cache from HBM once and does little arithmetic per byte; the small
+// products run on mma.sync so that the loads, not shared-memory traffic, set the pace:
+//   decode_pool_kernel    one warp per earlier key block: pooled scores of up to 16
+//                         groups (mma.sync, k_idx fragments straight from HBM);
+//   decode_select_kernel  one CTA per (sequence, group): exact top-(k-1) (ties -> lower
+//                         block) by per-lane lists, warp rounds and a counting rank;
 //   decode_attn_kernel    one CTA per (sequence, group, slot): the block's K/V in smem,
-//                         scores, softmax partial (lse) and P V for every head;
-//   decode_combine_kernel one CTA per (sequence, head): merges the k partials.
+//                         scores and P V on mma.sync, softmax partial (lse); the
+//                         group's last CTA merges its k partials into o and lse.
 #include <math.h>
 
 #include "common.cuh"
@@ -35,6 +36,7 @@ struct DecodeParams {
   float* pooled;               // [B][H_kv][nbm]
   float* o_part;               // [B][H_kv][topk][G][d]
   float* lse_part;             // [B][H_kv][topk][G]
+  int* arrive;                 // [B][H_kv] finished attention CTAs
   __nv_bfloat16* o;            // [B][H_q][d]
   float* lse;                  // [B][H_q]
   int B, Lmax, H_kv, G, d, d_idx, topk, nbm;
@@ -52,227 +54,364 @@ __device__ __forceinline__ int seq_len(const DecodeParams& p, int b, int* status
 }
 
 // pooled[b][g][c] = max over the 128 keys j of block c of q_idx[b,g] . k_idx[b,j], for
-// every block wholly before the query's block.  Grid (ceil(nbm / 8), B), 8 warps.
-template <int DI>
+// every block wholly before the query's block.  The scores of a block are a small
+// contraction (128 keys x H_kv groups x d_idx) done with mma.sync m16n8k16: A = the
+// block's k_idx rows straight from global memory, B = the query index vectors (held in
+// registers for the whole warp).  Grid (ceil(nbm / 8), B, ceil(H_kv / (8 NT))), 8 warps,
+// one key block per warp, 8 NT groups per CTA.
+//
+// Each lane reads 16 contiguous bytes of a key row per load.  The fragment slots of a
+// 16-wide k step are filled from those bytes in a fixed order (a0: elements 0-1, a2:
+// 2-3 of the first k step, 4-7 for the second), and the query fragments are read with
+// the same order, so every product pairs matching d; the dot product is order-free.
+template <int DI, int NT>
 __global__ void __launch_bounds__(256) decode_pool_kernel(const DecodeParams p) {
-  extern __shared__ float sq[];  // [H_kv][DI] query index vectors
   const int b = blockIdx.y;
-  for (int x = threadIdx.x; x < p.H_kv * DI; x += blockDim.x)
-    sq[x] = __bfloat162float(p.q_idx[(int64_t)b * p.H_kv * DI + x]);
-  __syncthreads();
   const int L = seq_len(p, b, p.status);
   const int c_own = (L - 1) / 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * 8 + warp;
   if (c >= c_own) return;
-  // the lane's keys c*128 + lane + 32 i (i < 4); groups outer, one key row in registers
-  // at a time (the re-reads for later groups hit L1)
-  for (int g = 0; g < p.H_kv; ++g) {
-    const float* qg = sq + g * DI;
-    float m = -INFINITY;
-#pragma unroll 1
-    for (int i = 0; i < 4; ++i) {
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.k_idx + ((int64_t)b * p.Lmax + c * 128 + lane + 32 * i) * DI);
-      float sacc = 0.f;
+  const int gq = lane >> 2, tq = lane & 3;  // fragment row / column group
+  constexpr int NP = DI / 32;                // 32-wide d chunks: two k steps each
+  // query fragments: group n = gq of each n tile, d = 32 j + 8 tq + 0..7
+  uint4 bq[NT][NP];
 #pragma unroll
-      for (int x = 0; x < DI / 8; ++x) {
-        const uint4 w = __ldg(&src[x]);
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+  for (int nt = 0; nt < NT; ++nt) {
+    const int grp = blockIdx.z * 8 * NT + nt * 8 + gq;
+    const uint4* qrow = reinterpret_cast<const uint4*>(p.q_idx + ((int64_t)b * p.H_kv + grp) * DI);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          sacc = fmaf(qg[8 * x + 2 * e], __low2float(h2[e]), sacc);
-          sacc = fmaf(qg[8 * x + 2 * e + 1], __high2float(h2[e]), sacc);
-        }
-      }
-      m = fmaxf(m, sacc);
+    for (int j = 0; j < NP; ++j) bq[nt][j] = grp < p.H_kv ? __ldg(&qrow[j * 4 + tq]) : make_uint4(0, 0, 0, 0);
+  }
+  float mx[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) mx[nt][0] = mx[nt][1] = -INFINITY;
+  const uint4* kb = reinterpret_cast<const uint4*>(p.k_idx + ((int64_t)b * p.Lmax + c * 128) * DI);
+#pragma unroll 2
+  for (int mt = 0; mt < 8; ++mt) {  // 16 keys per tile: rows gq and gq + 8
+    uint4 w0[NP], w1[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      w0[j] = __ldg(&kb[(mt * 16 + gq) * (DI / 8) + j * 4 + tq]);
+      w1[j] = __ldg(&kb[(mt * 16 + gq + 8) * (DI / 8) + j * 4 + tq]);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) p.pooled[((int64_t)b * p.H_kv + g) * p.nbm + c] = m;
+    for (int nt = 0; nt < NT; ++nt) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        const uint32_t a0[4] = {w0[j].x, w1[j].x, w0[j].y, w1[j].y};
+        const uint32_t a1[4] = {w0[j].z, w1[j].z, w0[j].w, w1[j].w};
+        mma_bf16_16816(acc, a0, bq[nt][j].x, bq[nt][j].y);
+        mma_bf16_16816(acc, a1, bq[nt][j].z, bq[nt][j].w);
+      }
+      mx[nt][0] = fmax3(mx[nt][0], acc[0], acc[2]);  // group 2 tq, keys gq and gq + 8
+      mx[nt][1] = fmax3(mx[nt][1], acc[1], acc[3]);  // group 2 tq + 1
+    }
   }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float m = mx[nt][e];
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+      const int grp = blockIdx.z * 8 * NT + nt * 8 + 2 * tq + e;
+      if (gq == 0 && grp < p.H_kv) p.pooled[((int64_t)b * p.H_kv + grp) * p.nbm + c] = m;
+    }
 }
 
+// Block scores as sortable 64-bit keys: larger key = larger score, equal scores -> the
+// lower block id first.  Keys of distinct blocks are distinct.
+__device__ __forceinline__ uint64_t rank_key(float v, int id) {
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // order-preserving map to unsigned
+  return ((uint64_t)u << 32) | (uint32_t)(0x7fffffff - id);
+}
+__device__ __forceinline__ int key_id(uint64_t key) { return 0x7fffffff - (int)(uint32_t)key; }
+
 // block_idx[b][g][:] = the k-1 best earlier blocks (pooled descending, lower id first on
-// ties) and the own block, ascending, -1 padded.  One CTA (256 threads) per (b, g).
+// ties) and the own block, ascending, -1 padded.  One CTA of 8 warps per (b, g):
+//   1. every lane keeps a sorted list of its own best KM candidates (registers);
+//   2. each warp takes its best M = min(k-1, c_own) in M rounds of a warp-wide max over
+//      the lanes' list heads, into shared memory;
+//   3. each of the 8 M survivors counts the survivors above it: rank < M is selected,
+//      and the selected ids are placed in ascending order by a second count.
+template <int KM>
 __global__ void __launch_bounds__(256) decode_select_kernel(const DecodeParams p) {
-  extern __shared__ float sp[];  // [nbm] candidate scores; selected ones set to -inf
-  __shared__ float rv[8];
-  __shared__ int ri[8];
-  __shared__ int chosen[32];
+  __shared__ uint64_t s_top[8 * KM];  // warp w's best M at [w M, w M + M)
+  __shared__ int s_sel[KM];
   const int b = blockIdx.y, g = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = seq_len(p, b, p.status);
   const int c_own = (L - 1) / 128;
   const float* src = p.pooled + ((int64_t)b * p.H_kv + g) * p.nbm;
-  for (int c = threadIdx.x; c < c_own; c += blockDim.x) sp[c] = src[c];
-  __syncthreads();
   const int M = min(p.topk - 1, c_own);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = 0; r < M; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int c = threadIdx.x; c < c_own; c += blockDim.x) {
-      const float v = sp[c];
-      if (v > bv || (v == bv && c < bi)) {
-        bv = v;
-        bi = c;
+  uint64_t top[KM];
+#pragma unroll
+  for (int s = 0; s < KM; ++s) top[s] = 0;  // below every real key
+  for (int c0 = warp * 32 + lane; c0 < c_own; c0 += 4 * 256) {
+    float v4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v4[u] = c0 + 256 * u < c_own ? __ldg(&src[c0 + 256 * u]) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (c0 + 256 * u >= c_own) break;
+      uint64_t x = rank_key(v4[u], c0 + 256 * u);
+      if (x <= top[KM - 1]) continue;
+#pragma unroll
+      for (int s = 0; s < KM; ++s) {  // sorted insert, descending
+        const uint64_t hi = x > top[s] ? x : top[s];
+        x = x > top[s] ? top[s] : x;
+        top[s] = hi;
       }
     }
+  }
+  // warp's best M
+  for (int r = 0; r < M; ++r) {
+    uint64_t best = top[0];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
+      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
     }
-    if (lane == 0) {
-      rv[warp] = bv;
-      ri[warp] = bi;
+    if (lane == 0) s_top[warp * M + r] = best;  // 0 when the warp had fewer than M candidates
+    if (best != 0 && top[0] == best) {
+#pragma unroll
+      for (int s = 0; s + 1 < KM; ++s) top[s] = top[s + 1];
+      top[KM - 1] = 0;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float v = rv[0];
-      int id = ri[0];
-      for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
-        if (rv[w] > v || (rv[w] == v && ri[w] < id)) {
-          v = rv[w];
-          id = ri[w];
-        }
-      if (id < 0 || id >= c_own) id = 0;  // only when every candidate is -inf/NaN
-      chosen[r] = id;
-      sp[id] = -INFINITY;
-    }
-    __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    int v[32];
-    for (int s = 0; s < M; ++s) v[s] = chosen[s];
-    v[M] = c_own;
-    for (int a = 1; a <= M; ++a)  // insertion sort, at most 32 entries
-      for (int s = a; s > 0 && v[s - 1] > v[s]; --s) {
-        const int t = v[s - 1];
-        v[s - 1] = v[s];
-        v[s] = t;
-      }
-    int32_t* dst = p.block_idx + ((int64_t)b * p.H_kv + g) * p.topk;
-    for (int s = 0; s < p.topk; ++s) dst[s] = s <= M ? v[s] : -1;
+  __syncthreads();
+  // selection among the 8 M survivors, then ascending order of the selected ids
+  const int n = 8 * M;
+  const int t = threadIdx.x;
+  uint64_t mine = 0;
+  int above = n;
+  if (t < n) {
+    mine = s_top[t];
+    above = 0;
+    for (int u = 0; u < n; ++u) above += s_top[u] > mine ? 1 : 0;
   }
+  const bool sel = mine != 0 && above < M;
+  if (sel) s_sel[above] = key_id(mine);
+  __syncthreads();
+  int32_t* dst = p.block_idx + ((int64_t)b * p.H_kv + g) * p.topk;
+  if (t < M) {
+    const int id = s_sel[t];
+    int pos = 0;
+    for (int u = 0; u < M; ++u) pos += s_sel[u] < id ? 1 : 0;
+    dst[pos] = id;
+  }
+  if (t == 0) {
+    dst[M] = c_own;  // every selected block lies before the own block
+    p.arrive[(int64_t)b * p.H_kv + g] = 0;  // arrival count of the attention CTAs
+  }
+  for (int s = M + 1 + t; s < p.topk; s += blockDim.x) dst[s] = -1;
 }
 
-// Softmax partial of every head of group g over the selected block in slot s.
-// Grid (topk, H_kv, B), 256 threads.
-template <int D>
-__global__ void __launch_bounds__(256) decode_attn_kernel(const DecodeParams p) {
-  constexpr int KS = D + 8;  // padded K/V row (bf16): conflict-free row-wise 16-byte reads
-  extern __shared__ __align__(16) uint8_t dsm[];
+// Softmax partial of every head of group g over block c (slot `part`): K and V rows
+// staged in shared memory (cp.async, rows past the cache end zero-filled; V in its own
+// copy group, still landing while the scores run); both products are mma.sync
+// m16n8k16 contractions with the group's heads as the 8-wide n dimension:
+//   S^T[key][h] = K[key][:] . q_h              (warp w: keys 16w..16w+15)
+//   O^T[dd][h]  = sum_key V[key][dd] P[h][key] (warp w: dd = 16w..16w+15)
+// The scores go through shared memory for the per-head softmax; P is rounded to bf16
+// for the second product, its row sum l stays fp32.  Writes lse_part and the
+// normalised o_part of the slot.
+template <int D, int NT>
+__device__ __forceinline__ void block_partial(const DecodeParams& p, uint8_t* dsm, int64_t part,
+                                              int c, int b, int g, float* s_l) {
+  constexpr int KS = D + 8;    // padded K/V row (bf16): conflict-free ldmatrix phases
+  constexpr int PS = 128 + 8;  // padded P row (bf16)
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(dsm);
   __nv_bfloat16* sV = sK + 128 * KS;
-  float* sQ = reinterpret_cast<float*>(sV + 128 * KS);  // [G][D]
-  float* sP = sQ + p.G * D;                               // [G][128]
-  float* sM = sP + p.G * 128;                             // [G] max, [G] sum
-  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // after the scores, the K region holds S [8 NT][128] fp32 and P [8 NT][PS] bf16
+  float* sS = reinterpret_cast<float*>(dsm);
+  __nv_bfloat16* sP = reinterpret_cast<__nv_bfloat16*>(sS + 8 * NT * 128);
   const int G = p.G;
-  const int64_t part = (((int64_t)b * p.H_kv + g) * p.topk + s) * G;
-  const int c = __ldg(&p.block_idx[((int64_t)b * p.H_kv + g) * p.topk + s]);
-  if (c < 0) {
-    for (int h = threadIdx.x; h < G; h += blockDim.x) p.lse_part[part + h] = -INFINITY;
-    return;
-  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
   const int L = seq_len(p, b, p.status);
   const int jmax = min(L - 1, c * 128 + 127) - c * 128;  // last visible row of the block
-  // K, V rows of the block and the group's query heads
   for (int x = threadIdx.x; x < 128 * (D / 8); x += blockDim.x) {
     const int r = x / (D / 8), ch = x % (D / 8);
-    const int j = c * 128 + r;
-    uint4 kw = make_uint4(0u, 0u, 0u, 0u), vw = kw;
-    if (j < p.Lmax && r <= jmax) {
-      const int64_t off = (((int64_t)b * p.Lmax + j) * p.H_kv + g) * D + ch * 8;
-      kw = __ldg(reinterpret_cast<const uint4*>(p.k + off));
-      vw = __ldg(reinterpret_cast<const uint4*>(p.v + off));
-    }
-    *reinterpret_cast<uint4*>(sK + r * KS + ch * 8) = kw;
-    *reinterpret_cast<uint4*>(sV + r * KS + ch * 8) = vw;
+    const bool ok = r <= jmax;  // row c 128 + r < L <= Lmax
+    const int64_t off = ok ? (((int64_t)b * p.Lmax + c * 128 + r) * p.H_kv + g) * D + ch * 8 : 0;
+    cp_async_16(sK + r * KS + ch * 8, p.k + off, ok);
   }
-  for (int x = threadIdx.x; x < G * D; x += blockDim.x)
-    sQ[x] = __bfloat162float(p.q[((int64_t)b * p.H_kv * G + g * G) * D + x]);
+  cp_async_commit();
+  for (int x = threadIdx.x; x < 128 * (D / 8); x += blockDim.x) {
+    const int r = x / (D / 8), ch = x % (D / 8);
+    const bool ok = r <= jmax;
+    const int64_t off = ok ? (((int64_t)b * p.Lmax + c * 128 + r) * p.H_kv + g) * D + ch * 8 : 0;
+    cp_async_16(sV + r * KS + ch * 8, p.v + off, ok);
+  }
+  cp_async_commit();
+  // B fragments of the scores: B[k = dd][n = h] = q[b][g G + h][dd], zero for h >= G
+  uint32_t bq[NT][D / 16][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = nt * 8 + gq;
+    const uint32_t* qrow =
+        reinterpret_cast<const uint32_t*>(p.q + ((int64_t)b * p.H_kv * G + (int64_t)g * G + h) * D);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      bq[nt][ks][0] = h < G ? __ldg(&qrow[ks * 8 + tq]) : 0u;
+      bq[nt][ks][1] = h < G ? __ldg(&qrow[ks * 8 + 4 + tq]) : 0u;
+    }
+  }
+  cp_async_wait<1>();  // K landed
   __syncthreads();
-  // scores: thread -> (key r, heads h = hs, hs + 2, ...)
+  float sc[NT][4];
   {
-    const int r = threadIdx.x & 127;
-    for (int h = threadIdx.x >> 7; h < G; h += 2) {
-      float acc = 0.f;
-      const float* qh = sQ + h * D;
-#pragma unroll 4
-      for (int x = 0; x < D; x += 8) {
-        const uint4 w = *reinterpret_cast<const uint4*>(sK + r * KS + x);
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+    const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix, row
+    const __nv_bfloat16* arow = sK + (warp * 16 + (mi & 1) * 8 + ri) * KS + (mi >> 1) * 8;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc = fmaf(qh[x + 2 * e], __low2float(h2[e]), acc);
-          acc = fmaf(qh[x + 2 * e + 1], __high2float(h2[e]), acc);
-        }
-      }
-      sP[h * 128 + r] = r <= jmax ? acc * p.scale : -INFINITY;
+    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t a[4];
+      ldmatrix_x4(a, arow + ks * 16);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], a, bq[nt][ks][0], bq[nt][ks][1]);
     }
   }
-  __syncthreads();
-  // per head: max, exp, sum (one warp per head)
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int h = warp; h < G; h += (int)(blockDim.x >> 5)) {
-    float m = -INFINITY;
+  __syncthreads();  // K no longer read: its region takes S and P
 #pragma unroll
-    for (int i = 0; i < 4; ++i) m = fmaxf(m, sP[h * 128 + lane + 32 * i]);
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int h = nt * 8 + 2 * tq + (e & 1), r = warp * 16 + gq + (e >> 1) * 8;
+      sS[h * 128 + r] = r <= jmax ? sc[nt][e] * p.scale : -INFINITY;
+    }
+  __syncthreads();
+  // per head: max, exp, sum (one warp per head); padding heads get P = 0
+  for (int h = warp; h < 8 * NT; h += 8) {
+    if (h >= G) {
+      for (int r = lane; r < PS; r += 32) sP[h * PS + r] = __float2bfloat16(0.f);
+      continue;
+    }
+    float v[4], m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[i] = sS[h * 128 + lane + 32 * i];
+      m = fmaxf(m, v[i]);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float l = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float e = expf(sP[h * 128 + lane + 32 * i] - m);  // masked: exp(-inf) = 0
-      sP[h * 128 + lane + 32 * i] = e;
+      const float e = expf(v[i] - m);  // masked: exp(-inf) = 0
+      sP[h * PS + lane + 32 * i] = __float2bfloat16(e);
       l += e;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     if (lane == 0) {
-      sM[h] = m;
-      sM[G + h] = l;
+      s_l[h] = l;
       p.lse_part[part + h] = m + logf(l);
     }
   }
+  cp_async_wait<0>();  // V landed
   __syncthreads();
-  // O partial (normalised): thread -> (head, d)
-  for (int x = threadIdx.x; x < G * D; x += blockDim.x) {
-    const int h = x / D, dd = x % D;
+  if (warp < D / 16) {
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    const int mi = lane >> 3, ri = lane & 7;
+    // ldmatrix.trans of V rows (keys) gives the A fragment of V^T: matrix mi covers
+    // keys (mi >> 1) * 8 + 0..7 and columns dd = 16 warp + (mi & 1) * 8 + 0..7
+    const __nv_bfloat16* vrow = sV + ((mi >> 1) * 8 + ri) * KS + warp * 16 + (mi & 1) * 8;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      uint32_t a[4];
+      ldmatrix_x4_trans(a, vrow + ks * 16 * KS);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const __nv_bfloat16* prow = sP + (nt * 8 + gq) * PS + ks * 16 + 2 * tq;
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(prow);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(prow + 8);
+        mma_bf16_16816(acc[nt], a, b0, b1);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int h = nt * 8 + 2 * tq + (e & 1), dd = warp * 16 + gq + (e >> 1) * 8;
+        if (h < G) p.o_part[(part + h) * D + dd] = acc[nt][e] / s_l[h];
+      }
+  }
+}
+
+// o[b][g G + h] and lse[b][g G + h] for every head of group g from the group's k
+// partials (log-sum-exp merge).  The filled slots come first (block ids ascending, then
+// -1 padding with lse = -inf).  Run by one CTA after all partials are written; reads
+// them through L2, every slot's load of an output element issued together.
+__device__ __forceinline__ void combine_group(const DecodeParams& p, int b, int g, float* s_w) {
+  const int G = p.G, K = p.topk;
+  const int64_t base = ((int64_t)b * p.H_kv + g) * K;
+  const int64_t head0 = (int64_t)b * p.H_kv * G + (int64_t)g * G;
+  __shared__ int s_n;
+  for (int i = threadIdx.x; i < K * G; i += blockDim.x) s_w[i] = __ldcg(&p.lse_part[base * G + i]);
+  __syncthreads();
+  for (int h = threadIdx.x; h < G; h += blockDim.x) {
+    int n = 0;
+    float m = -INFINITY;
+    for (int s = 0; s < K; ++s) {
+      const float ls = s_w[s * G + h];
+      if (ls != -INFINITY) n = s + 1;
+      m = fmaxf(m, ls);
+    }
+    float l = 0.f;
+    for (int s = 0; s < n; ++s) l += expf(s_w[s * G + h] - m);
+    for (int s = 0; s < n; ++s) s_w[s * G + h] = expf(s_w[s * G + h] - m) / l;
+    p.lse[head0 + h] = m + logf(l);
+    if (h == 0) s_n = n;
+  }
+  __syncthreads();
+  const int n = s_n;  // the same for every head: the group's filled slots
+  const float* op = p.o_part + base * G * p.d;
+  for (int x = threadIdx.x; x < G * p.d; x += blockDim.x) {
+    const int h = x / p.d;
     float acc = 0.f;
-    const float* ph = sP + h * 128;
-    for (int r = 0; r <= jmax; ++r) acc = fmaf(ph[r], __bfloat162float(sV[r * KS + dd]), acc);
-    p.o_part[(part + h) * D + dd] = acc / sM[G + h];
+#pragma unroll 8
+    for (int s = 0; s < n; ++s) acc = fmaf(s_w[s * G + h], __ldcg(&op[(int64_t)s * G * p.d + x]), acc);
+    p.o[head0 * p.d + x] = __float2bfloat16(acc);
   }
 }
 
-// o[b][h] and lse[b][h] from the k partials of head h.  One CTA (D threads) per (b, h).
-__global__ void decode_combine_kernel(const DecodeParams p) {
-  const int bh = blockIdx.x;
-  const int b = bh / (p.H_kv * p.G), h = bh % (p.H_kv * p.G);
-  const int g = h / p.G, hh = h % p.G;
-  const int64_t base = ((int64_t)b * p.H_kv + g) * p.topk;
-  float m = -INFINITY;
-  for (int s = 0; s < p.topk; ++s) m = fmaxf(m, p.lse_part[(base + s) * p.G + hh]);
-  float l = 0.f, acc = 0.f;
-  for (int s = 0; s < p.topk; ++s) {
-    const float ls = p.lse_part[(base + s) * p.G + hh];
-    if (ls == -INFINITY) continue;
-    const float w = expf(ls - m);
-    l += w;
-    acc = fmaf(w, p.o_part[((base + s) * p.G + hh) * p.d + threadIdx.x], acc);
+// Grid (topk, H_kv, B), 256 threads: CTA (s, g, b) computes the partial of slot s of
+// group g; the last of the group's topk CTAs to finish (an arrival count that the
+// selection kernel zeroed) merges the group's partials into o and lse.
+template <int D, int NT>
+__global__ void __launch_bounds__(256) decode_attn_kernel(const DecodeParams p) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  __shared__ float s_l[8 * NT];
+  __shared__ float s_w[32 * 16];  // [topk][G] merge weights
+  __shared__ int s_last;
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int64_t part = (((int64_t)b * p.H_kv + g) * p.topk + s) * p.G;
+  const int c = __ldg(&p.block_idx[((int64_t)b * p.H_kv + g) * p.topk + s]);
+  if (c < 0) {
+    for (int h = threadIdx.x; h < p.G; h += blockDim.x) p.lse_part[part + h] = -INFINITY;
+  } else {
+    block_partial<D, NT>(p, dsm, part, c, b, g, s_l);
   }
-  p.o[((int64_t)b * p.H_kv * p.G + h) * p.d + threadIdx.x] = __float2bfloat16(l > 0.f ? acc / l : 0.f);
-  if (threadIdx.x == 0) p.lse[(int64_t)b * p.H_kv * p.G + h] = m + logf(l);
+  __threadfence();  // this CTA's partial is visible before its arrival
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&p.arrive[(int64_t)b * p.H_kv + g], 1) == p.topk - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  combine_group(p, b, g, s_w);
 }
 
-size_t decode_ws_parts(const Shape& s, size_t* off_pooled, size_t* off_o, size_t* off_lse) {
+size_t decode_ws_parts(const Shape& s, size_t* off_pooled, size_t* off_o, size_t* off_lse,
+                       size_t* off_arrive) {
   const int nbm = s.nb;
   size_t off = 0;
   *off_pooled = off;
@@ -281,6 +420,8 @@ size_t decode_ws_parts(const Shape& s, size_t* off_pooled, size_t* off_o, size_t
   off += align256((size_t)s.B * s.H_kv * s.topk * s.G * s.d * 4);
   *off_lse = off;
   off += align256((size_t)s.B * s.H_kv * s.topk * s.G * 4);
+  *off_arrive = off;
+  off += align256((size_t)s.B * s.H_kv * 4);
   return off;
 }
 
@@ -294,8 +435,8 @@ extern "C" {
 size_t msa_decode_workspace_size(const msa_problem_t* p) {
   Shape s;
   if (validate_problem(p, &s) != MSA_OK) return 0;
-  size_t a, b, c;
-  return decode_ws_parts(s, &a, &b, &c);
+  size_t a, b, c, d;
+  return decode_ws_parts(s, &a, &b, &c, &d);
 }
 
 int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const void* k,
@@ -309,8 +450,8 @@ int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const v
   const void* ptrs[] = {q, q_idx, k, v, k_idx, lens, block_idx, o, lse};
   for (const void* x : ptrs)
     if (!x || (reinterpret_cast<uintptr_t>(x) & 15) != 0) return MSA_ERR_ARG;
-  size_t off_pooled, off_o, off_lse;
-  const size_t need = decode_ws_parts(s, &off_pooled, &off_o, &off_lse);
+  size_t off_pooled, off_o, off_lse, off_arrive;
+  const size_t need = decode_ws_parts(s, &off_pooled, &off_o, &off_lse, &off_arrive);
   if (!workspace || workspace_bytes < need) return MSA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MSA_ERR_ARG;
   Ctx cx;
@@ -327,6 +468,7 @@ int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const v
   dp.pooled = reinterpret_cast<float*>(w + off_pooled);
   dp.o_part = reinterpret_cast<float*>(w + off_o);
   dp.lse_part = reinterpret_cast<float*>(w + off_lse);
+  dp.arrive = reinterpret_cast<int*>(w + off_arrive);
   dp.o = static_cast<__nv_bfloat16*>(o);
   dp.lse = lse;
   dp.B = s.B;
@@ -339,35 +481,36 @@ int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const v
   dp.nbm = s.nb;
   dp.scale = s.scale;
   dp.status = cx.status;
-  const size_t pool_smem = (size_t)s.H_kv * s.d_idx * sizeof(float);
-  if (pool_smem > 48 * 1024) return MSA_ERR_UNSUPPORTED;
-  const dim3 gpool((unsigned)((s.nb + 7) / 8), (unsigned)s.B);
-  if (s.d_idx == 64) decode_pool_kernel<64><<<gpool, 256, pool_smem, stream>>>(dp);
-  else decode_pool_kernel<32><<<gpool, 256, pool_smem, stream>>>(dp);
-  note_launch();
-  const size_t sel_smem = (size_t)s.nb * sizeof(float);
-  if (sel_smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(decode_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sel_smem) != cudaSuccess)
-      return MSA_ERR_CUDA;
-  }
-  decode_select_kernel<<<dim3((unsigned)s.H_kv, (unsigned)s.B), 256, sel_smem, stream>>>(dp);
-  note_launch();
-  const size_t attn_smem = (size_t)2 * 128 * (s.d + 8) * 2 + (size_t)s.G * (s.d + 128 + 2) * 4;
-  const dim3 gattn((unsigned)s.topk, (unsigned)s.H_kv, (unsigned)s.B);
-  cudaError_t e;
-  if (s.d == 128) {
-    e = cudaFuncSetAttribute(decode_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)attn_smem);
-    if (e == cudaSuccess) decode_attn_kernel<128><<<gattn, 256, attn_smem, stream>>>(dp);
+  const int pool_nt = s.H_kv > 8 ? 2 : 1;
+  const dim3 gpool((unsigned)((s.nb + 7) / 8), (unsigned)s.B, (unsigned)((s.H_kv + 8 * pool_nt - 1) / (8 * pool_nt)));
+#define MSA_POOL(DI, NT) decode_pool_kernel<DI, NT><<<gpool, 256, 0, stream>>>(dp)
+  if (s.d_idx == 64) {
+    if (pool_nt == 1) MSA_POOL(64, 1); else MSA_POOL(64, 2);
   } else {
-    e = cudaFuncSetAttribute(decode_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)attn_smem);
-    if (e == cudaSuccess) decode_attn_kernel<64><<<gattn, 256, attn_smem, stream>>>(dp);
+    if (pool_nt == 1) MSA_POOL(32, 1); else MSA_POOL(32, 2);
   }
-  if (e != cudaSuccess) return MSA_ERR_CUDA;
+#undef MSA_POOL
   note_launch();
-  decode_combine_kernel<<<(unsigned)(s.B * s.H_q), (unsigned)s.d, 0, stream>>>(dp);
+  const dim3 gsel((unsigned)s.H_kv, (unsigned)s.B);
+  if (s.topk - 1 <= 15) decode_select_kernel<15><<<gsel, 256, 0, stream>>>(dp);
+  else decode_select_kernel<31><<<gsel, 256, 0, stream>>>(dp);
+  note_launch();
+  const size_t attn_smem = (size_t)2 * 128 * (s.d + 8) * 2;
+  const dim3 gattn((unsigned)s.topk, (unsigned)s.H_kv, (unsigned)s.B);
+  cudaError_t e = cudaSuccess;
+#define MSA_ATTN(D, NT)                                                                      \
+  do {                                                                                       \
+    e = cudaFuncSetAttribute(decode_attn_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             (int)attn_smem);                                                \
+    if (e == cudaSuccess) decode_attn_kernel<D, NT><<<gattn, 256, attn_smem, stream>>>(dp);  \
+  } while (0)
+  if (s.d == 128) {
+    if (s.G <= 8) MSA_ATTN(128, 1); else MSA_ATTN(128, 2);
+  } else {
+    if (s.G <= 8) MSA_ATTN(64, 1); else MSA_ATTN(64, 2);
+  }
+#undef MSA_ATTN
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
