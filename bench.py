@@ -248,6 +248,16 @@ def run_ours(args, cfg, rank, world):
     d = {n: to_dev(host[n]) for n in names}
     w = cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N)
     stream = torch.cuda.current_stream(dev)
+    if args.decode_only:  # the decode leg alone (e.g. for a profiler's launch list)
+        peaks, _ = load_peaks()
+        dec = decode_leg(torch, ops, d, cfg, dev, stream,
+                         float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))
+        if ops.device_status() != 0:
+            raise RuntimeError("device status after decode: "
+                               + _lib.status_string(ops.device_status()))
+        if rank == 0:
+            print(json.dumps({"decode": dec}), flush=True)
+        return
 
     def step(t, phase_ev=None):
         if phase_ev:
@@ -426,10 +436,12 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default="128k", choices=sorted(synth.CONFIGS))
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--cpu-rows", type=int, default=96)
-    ap.add_argument("--ref-rows", type=int, default=16)
+    ap.add_argument("--cpu-rows", type=int, default=1400)
+    ap.add_argument("--ref-rows", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode leg")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="run only the decode leg and print its JSON object")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
