@@ -106,6 +106,46 @@ def decode_leg(torch, ops, d, cfg, dev, stream, hbm_peak, calls=20):
             "timing": "CUDA events around each call, queued behind a GPU spin"}
 
 
+def warmup_leg(torch, ops, cfg, dev, stream, peak_tf, steps=5, warm=3):
+    """Indexer warm-up (dense set, topk >= nb): the workload's heads at N = 16384 with
+    topk = 128 = nb, so both branches attend every visible token and the KL runs over
+    all of them.  One step = index call (dense set + lse_idx), forward, backward; mean
+    device time over `steps` steps after `warm` untimed ones (inputs > L2)."""
+    wc = cfg.with_(name="warmup-16k", B=1, N=16384, topk=128, n_needle=4)
+    host = synth.make_inputs(wc)
+    t = {n: torch.from_numpy(host[n].view(np.int16)).to(dev).view(torch.bfloat16)
+         for n in ("q", "k", "v", "q_idx", "k_idx", "dO")}
+    w = wc.kl_coef / (wc.B * wc.H_kv * wc.N)
+
+    def step():
+        bi, li = ops.msa_index_topk(t["q_idx"], t["k_idx"], wc.topk, H_q=wc.H_q, d=wc.d)
+        o, lse = ops.msa_fwd(t["q"], t["k"], t["v"], bi, scale=wc.scale, d_idx=wc.d_idx)
+        g = ops.msa_bwd(t["q"], t["k"], t["v"], o, lse, t["dO"], t["q_idx"], t["k_idx"], bi, li,
+                        w, scale=wc.scale)
+        return bi, g
+
+    for _ in range(warm):
+        bi, _ = step()
+    torch.cuda.synchronize()
+    sum_T = token_set_total(wc, bi.cpu().numpy())
+    f = algorithmic_flops(wc, sum_T)
+    flops = f["index_lse"] + f["fwd"] + f["bwd"]  # no block scoring: the set is forced
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    tf = flops / (ms / 1000.0) / 1e12
+    del t
+    return {"workload": workload_name(wc) + " (dense set: every visible block)",
+            "ms_per_step": ms, "tokens_per_s": wc.B * wc.N / (ms / 1000.0),
+            "algorithmic_tflop_per_step": flops / 1e12, "tflops": tf, "peak_tflops": peak_tf,
+            "frac": tf / peak_tf, "steps": steps}
+
+
 # ----------------------------------------------------------------------------
 # algorithmic work (what the method must compute, not what a kernel happens to do)
 # ----------------------------------------------------------------------------
@@ -248,6 +288,16 @@ def run_ours(args, cfg, rank, world):
     d = {n: to_dev(host[n]) for n in names}
     w = cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N)
     stream = torch.cuda.current_stream(dev)
+    if args.warmup_only:  # the indexer warm-up leg alone
+        peaks, _ = load_peaks()
+        wu = warmup_leg(torch, ops, cfg, dev, stream, float(
+            peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])))
+        if ops.device_status() != 0:
+            raise RuntimeError("device status after warm-up leg: "
+                               + _lib.status_string(ops.device_status()))
+        if rank == 0:
+            print(json.dumps({"warmup": wu}), flush=True)
+        return
     if args.decode_only:  # the decode leg alone (e.g. for a profiler's launch list)
         peaks, _ = load_peaks()
         dec = decode_leg(torch, ops, d, cfg, dev, stream,
@@ -395,6 +445,14 @@ def run_ours(args, cfg, rank, world):
         dec = decode_leg(torch, ops, d, cfg, dev, stream,
                          float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))
 
+    # ---- indexer warm-up leg (dense set) ----
+    wu = None
+    if not args.no_warmup_leg:
+        wu = warmup_leg(torch, ops, cfg, dev, stream, peak_tf)
+        st = ops.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status after warm-up leg: {_lib.status_string(st)}")
+
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -422,6 +480,7 @@ def run_ours(args, cfg, rank, world):
                     "d2h_bytes_per_step": 4, "steps": e2e_steps},
             "cpu_baseline": cpu,
             "decode": dec,
+            "warmup": wu,
             "gpu_launches": launches,
             "clocks": clk,
         }
@@ -442,6 +501,10 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode leg")
     ap.add_argument("--decode-only", action="store_true",
                     help="run only the decode leg and print its JSON object")
+    ap.add_argument("--no-warmup-leg", action="store_true",
+                    help="skip the indexer warm-up (dense set) leg")
+    ap.add_argument("--warmup-only", action="store_true",
+                    help="run only the indexer warm-up leg and print its JSON object")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int qi = r / G, h = r % G;
           const int ent = __shfl_sync(0xffffffffu, my_ent, qi);
           const bool ok = ent >= 0;
-          const int i = ok ? (ent >> 5) : 0;
+          const int i = ok ? (ent >> kSlotBits) : 0;
           const int64_t src = (((int64_t)b * p.N + i) * p.H_kv * G + g * G + h) * D + cc * 8;
           const uint32_t o = (cc >> 3) * L::kQH + sw128(r, cc);
           cp_async_16(st + L::kSQ + o, p.q + src, ok);
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int qi = x / 8, cc = x % 8;
           const int ent = __shfl_sync(0xffffffffu, my_ent, qi);
           const bool ok = ent >= 0 && cc * 8 < p.DI;
-          const int i = ok ? (ent >> 5) : 0;
+          const int i = ok ? (ent >> kSlotBits) : 0;
           const int64_t src = (((int64_t)b * p.N + i) * p.H_kv + g) * p.DI + (ok ? cc * 8 : 0);
           cp_async_16(ss + L::kSQi + sw128(qi, cc), p.q_idx + src, ok);
         }
@@ -271,19 +271,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = lt, qi = r / G, h = r % G;  // one row per loader thread
           const int ent = __shfl_sync(0xffffffffu, my_ent, qi);
           const bool ok = ent >= 0;
-          const int ri = ok ? (ent >> 5) : -1;
+          const int ri = ok ? (ent >> kSlotBits) : -1;
           const int64_t x = ((int64_t)b * p.H_kv * G + g * G + h) * p.N + (ok ? ri : 0);
           cp_async_4(ss + L::kSLse + 4 * r, p.lse + x, ok);
           cp_async_4(ss + L::kSD + 4 * r, p.Dv + x, ok);
           reinterpret_cast<int*>(ss + L::kSRi)[r] = ri;
           reinterpret_cast<int*>(ss + L::kSRp)[r] =
-              ok ? (int)((((int64_t)bg * p.N + ri) * p.topk + (ent & 31)) * G + h) : -1;
+              ok ? (int)((((int64_t)bg * p.N + ri) * p.topk + (ent & kSlotMask)) * G + h) : -1;
           if (lt < kQS) {
             const bool okq = my_ent >= 0;
-            const int iq = okq ? (my_ent >> 5) : 0;
+            const int iq = okq ? (my_ent >> kSlotBits) : 0;
             reinterpret_cast<int*>(ss + L::kSQiq)[lt] = okq ? iq : -1;
             reinterpret_cast<int*>(ss + L::kSQp)[lt] =
-                okq ? (int)(((int64_t)bg * p.N + iq) * p.topk + (my_ent & 31)) : -1;
+                okq ? (int)(((int64_t)bg * p.N + iq) * p.topk + (my_ent & kSlotMask)) : -1;
             cp_async_4(ss + L::kSLi + 4 * lt, p.lse_idx + (int64_t)bg * p.N + iq, okq);
           }
         }

@@ -17,8 +17,8 @@ namespace {
 
 // o[b,i,h] and lse[b,h,i] from the k partials of each (b, g, i) row.  One warp per
 // row: the partials of one slot are G*D contiguous bf16 (all heads of the group), read
-// as 16-byte chunks; the per-(slot, head) weights exp(lse_s - lse) come from shared
-// memory, computed by G lanes.
+// as 16-byte chunks.  G lanes find each head's max and sum over the slots (any number
+// of slots); every lane then forms the weight exp(lse_s - m) / l of its chunk's head.
 template <int D, int G>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(
     const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
     float* __restrict__ lse, int64_t rows, int N, int H_kv, int topk, int nb) {
   constexpr int TC = G * D / 8;              // 16-byte chunks per slot
   constexpr int CPL = (TC + 31) / 32;        // chunks per lane
-  __shared__ float wts[8][32 * G];
+  __shared__ float s_mi[8][2 * G];           // per head: max, 1 / sum
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t rkv = (int64_t)blockIdx.x * 8 + wib;  // (b*H_kv + g)*N + i
   if (rkv >= rows) return;
@@ -35,7 +35,6 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
   const int g = (int)(bg % H_kv);
   const int64_t b = bg / H_kv;
   const int32_t* sel = block_idx + rkv * topk;
-  float* w = wts[wib];
   if (lane < G) {
     const int h = lane;
     float m = -INFINITY;
@@ -47,12 +46,10 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
     for (int s = 0; s < topk; ++s) {
       const int c = __ldg(&sel[s]);
       const float ls = (c >= 0 && c < nb) ? __ldg(&lse_part[(rkv * topk + s) * G + h]) : -INFINITY;
-      const float e = ls == -INFINITY ? 0.f : __expf(ls - m);
-      w[s * G + h] = e;
-      l += e;
+      l += ls == -INFINITY ? 0.f : __expf(ls - m);
     }
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    for (int s = 0; s < topk; ++s) w[s * G + h] *= inv;
+    s_mi[wib][h] = m;
+    s_mi[wib][G + h] = l > 0.f ? 1.f / l : 0.f;
     lse[(b * H_kv * G + g * G + h) * N + i] = m + logf(l);
   }
   __syncwarp();
@@ -69,7 +66,9 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
     for (int x = 0; x < CPL; ++x) {
       const int ch = lane + 32 * x;
       if (ch < TC) {
-        const float wt = w[s * G + (ch * 8) / D];
+        const int h = (ch * 8) / D;
+        const float wt = __expf(__ldg(&lse_part[(rkv * topk + s) * G + h]) - s_mi[wib][h]) *
+                         s_mi[wib][G + h];
         const uint4 raw = __ldg(&src[ch]);
         const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll

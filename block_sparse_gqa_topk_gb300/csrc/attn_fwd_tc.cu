@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if ((qi >> 5) == m) ent = v;
           }
           const bool ok = ent >= 0;
-          const int i = ok ? (ent >> 5) : 0;
+          const int i = ok ? (ent >> kSlotBits) : 0;
           const int64_t src = (((int64_t)b * p.N + i) * p.H_kv * G + g * G + h) * D + ch * 8;
           cp_async_16(dq + kmaj_off<D>(r, ch), p.q + src, ok);
         }
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int ne = min(QPT, __ldg(&p.off[key + 1]) - e0);
         const int qi = row / G;
         const int ent = qi < ne ? __ldg(&p.entries[e0 + qi]) : -1;
-        const int i = ent >> 5;
+        const int i = ent >> kSlotBits;
         const int rowv = opaque(row), lanev = opaque(lane);
         bool ok = __all_sync(0xffffffffu, mbar_wait(&sfull[b], (u >> 1) & 1, p.wait_ns, abort_flag));
         if (!ok) {
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float inv = l > 0.f ? 1.f / l : 0.f;
         int prow = -1;
         if (ent >= 0) {
-          prow = (int)((((int64_t)bg * p.N + i) * p.topk + (ent & 31)) * G + row % G);
+          prow = (int)((((int64_t)bg * p.N + i) * p.topk + (ent & kSlotMask)) * G + row % G);
           p.lse_part[prow] = l > 0.f ? (ms + log2f(l)) * kLn2 : -INFINITY;
         }
         // Stage 64 columns at a time in this warp's own (now free) P rows, swizzled,

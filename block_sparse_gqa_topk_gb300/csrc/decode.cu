@@ -447,6 +447,7 @@ int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const v
   if (rc) return rc;
   if (s.B == 0) return MSA_OK;
   if (s.N == 0) return MSA_ERR_SHAPE;  // N is the cache capacity Lmax
+  if (s.topk > kMaxSelect) return MSA_ERR_UNSUPPORTED;
   const void* ptrs[] = {q, q_idx, k, v, k_idx, lens, block_idx, o, lse};
   for (const void* x : ptrs)
     if (!x || (reinterpret_cast<uintptr_t>(x) & 15) != 0) return MSA_ERR_ARG;

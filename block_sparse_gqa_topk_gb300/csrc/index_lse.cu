@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = x / CH, ch = x % CH;
           const int ent = r < ne ? __ldg(&p.entries[e0 + r]) : -1;
           const bool ok = ent >= 0;
-          const int i = ok ? (ent >> 5) : 0;
+          const int i = ok ? (ent >> kSlotBits) : 0;
           const int64_t src = (((int64_t)b * p.N + i) * p.H_kv + g) * DI + ch * 8;
           cp_async_16(dq + swz<RB>(r, ch), p.q_idx + src, ok);
         }
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * 128;
         const int ne = min(128, __ldg(&p.off[key + 1]) - e0);
         const int ent = row < ne ? __ldg(&p.entries[e0 + row]) : -1;
-        const int i = ent >> 5;
+        const int i = ent >> kSlotBits;
         const bool ok =
             __all_sync(0xffffffffu, mbar_wait(&sfull[sl], (u / kSlots) & 1, p.wait_ns, abort_flag));
         if (!ok) {
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ent >= 0) {
           const float l = l0 + l1;
-          p.lse_part[((int64_t)bg * p.N + i) * p.topk + (ent & 31)] =
+          p.lse_part[((int64_t)bg * p.N + i) * p.topk + (ent & kSlotMask)] =
               l > 0.f ? (m * sl2 + log2f(l)) * kLn2 : -INFINITY;
         }
       }

@@ -317,14 +317,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// topk == 1 or a single block: every row gets only its own block.
-__global__ void local_only_kernel(int32_t* __restrict__ block_idx, int64_t rows, int N, int topk) {
+// Sets that need no scoring.  topk == 1: every row gets only its own block.
+// topk >= nb: every visible block is selected (blocks 0..i/128 ascending, then -1) --
+// the dense set of the indexer warm-up, where both branches see the full causal
+// context ("Cómo se entrena MSA" ¶3: warm-up with full attention in both branches).
+__global__ void forced_set_kernel(int32_t* __restrict__ block_idx, int64_t rows, int N, int topk,
+                                  int all) {
   const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (t >= rows * topk) return;
   const int64_t r = t / topk;
   const int s = (int)(t % topk);
-  const int i = (int)(r % N);
-  block_idx[t] = s == 0 ? i / 128 : -1;
+  const int c = (int)(r % N) / 128;
+  block_idx[t] = all ? (s <= c ? s : -1) : (s == 0 ? c : -1);
 }
 
 template <int DI, int KM>
@@ -356,13 +360,14 @@ cudaError_t launch_di(const Shape& s, const CUtensorMap& tq, const CUtensorMap& 
 cudaError_t launch_index_topk(const Shape& s, const void* q_idx, const void* k_idx,
                               int32_t* block_idx, const Ctx& cx, cudaStream_t st) {
   if (s.B == 0 || s.N == 0 || s.H_kv == 0) return cudaSuccess;
-  if (s.topk == 1 || s.nb == 1) {
+  if (s.topk == 1 || s.topk >= s.nb) {
     const int64_t n = s.rows_kv() * s.topk;
-    local_only_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(block_idx, s.rows_kv(), s.N,
-                                                                   s.topk);
+    forced_set_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(block_idx, s.rows_kv(), s.N,
+                                                                   s.topk, s.topk >= s.nb);
     note_launch();
     return cudaGetLastError();
   }
+  if (s.topk > kMaxSelect) return cudaErrorNotSupported;  // callers reject this case first
   const int DI = s.d_idx;
   const CUtensorMapSwizzle swz = DI == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap tq, tk;

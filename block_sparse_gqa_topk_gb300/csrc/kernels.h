@@ -11,6 +11,15 @@
 
 namespace msa {
 
+// Slots per (b, g, i) row: up to kMaxSlots block ids.  Inverted-list entries pack
+// (query << kSlotBits) | slot into a non-negative int (query < 2^24).  The block
+// selection kernel keeps its candidates in registers and picks at most kMaxSelect
+// blocks; more slots are used only by the dense set (every visible block, topk >= nb).
+constexpr int kSlotBits = 7;
+constexpr int kSlotMask = (1 << kSlotBits) - 1;
+constexpr int kMaxSlots = 1 << kSlotBits;
+constexpr int kMaxSelect = 32;
+
 // Validated problem, with derived sizes.
 struct Shape {
   int B, N, H_q, H_kv, d, d_idx, Bk, topk, causal;
@@ -36,7 +45,7 @@ struct Plan {
   int* cnt;      // [keys]      counts, reused as fill cursors
   int* off;      // [keys + 1]  CSR offsets into entries
   int* toff;     // [keys + 1]  tile offsets; toff[keys] = number of tiles
-  int* entries;  // [rows_kv * topk]  (i << 5) | slot
+  int* entries;  // [rows_kv * topk]  (i << kSlotBits) | slot
 };
 
 size_t plan_bytes(const Shape& s);

@@ -71,7 +71,7 @@ int check_problem(const msa_problem_t* p, Shape* s) {
   if (p->Bk != 128) return MSA_ERR_UNSUPPORTED;
   if (p->d != 64 && p->d != 128) return MSA_ERR_UNSUPPORTED;
   if (p->d_idx != 32 && p->d_idx != 64) return MSA_ERR_UNSUPPORTED;
-  if (p->topk > 32) return MSA_ERR_UNSUPPORTED;
+  if (p->topk > kMaxSlots) return MSA_ERR_UNSUPPORTED;
   if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return MSA_ERR_UNSUPPORTED;
   if (p->N > (1 << 24)) return MSA_ERR_UNSUPPORTED;
   s->B = p->B;
@@ -201,6 +201,8 @@ int msa_index_topk(const msa_problem_t* p, const void* q_idx, const void* k_idx,
   if (s.B == 0 || s.N == 0) return MSA_OK;
   if (!q_idx || !k_idx || !block_idx) return MSA_ERR_ARG;
   if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(block_idx)) return MSA_ERR_ARG;
+  // selection keeps at most kMaxSelect candidates; more slots only for the dense set
+  if (s.topk > kMaxSelect && s.topk < s.nb) return MSA_ERR_UNSUPPORTED;
   if (lse_idx) {
     if (!workspace || workspace_bytes < ws_index(s)) return MSA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MSA_ERR_ARG;

@@ -9,7 +9,7 @@
 // kernel", second idea).  This file builds the lists from block_idx:
 //   count  -> per-list sizes (shared-memory histograms per row chunk),
 //   scan   -> CSR offsets and tile offsets (one CTA, decoupled chunks),
-//   fill   -> (query << 5 | slot) entries.
+//   fill   -> (query << kSlotBits | slot) entries.
 // HBM-bound integer work: block_idx is read twice, entries written once.
 #include "common.cuh"
 #include "kernels.h"
@@ -113,7 +113,7 @@ __global__ void plan_fill_kernel(const int32_t* __restrict__ block_idx, int64_t 
   const int i = (int)(r - bg * N);
   const int64_t key = bg * nb + c;
   const int pos = off[key] + atomicAdd(&cursor[key], 1);
-  entries[pos] = (i << 5) | slot;
+  entries[pos] = (i << kSlotBits) | slot;
 }
 
 // Shared-memory variants: one CTA takes kRowsPerCta consecutive rows of one
@@ -176,7 +176,7 @@ __global__ void plan_fill_smem_kernel(const int32_t* __restrict__ block_idx, int
     if (c < 0 || c >= nb) continue;
     const int q = e / topk;
     const int pos = atomicAdd(&hist[c], 1);
-    entries[pos] = ((i0 + q) << 5) | (e - q * topk);
+    entries[pos] = ((i0 + q) << kSlotBits) | (e - q * topk);
   }
 }
 

@@ -32,8 +32,11 @@
  *    recorded in a per-device status word, read with msa_get_device_status().
  *  - No exception, trap or abort crosses this boundary.
  *  - Supported (this build): causal = 1, Bk = 128, d in {64, 128},
- *    d_idx in {32, 64}, 1 <= topk <= 32, H_q % H_kv == 0 with G = H_q / H_kv in
- *    {1, 2, 4, 8, 16}, N <= 2^24.  N need not be a multiple of Bk.
+ *    d_idx in {32, 64}, 1 <= topk <= 128, H_q % H_kv == 0 with G = H_q / H_kv in
+ *    {1, 2, 4, 8, 16}, N <= 2^24.  N need not be a multiple of Bk.  Block selection
+ *    (msa_index_topk, msa_decode) picks at most 32 blocks; topk > 32 is accepted by
+ *    msa_index_topk only when topk >= nb = ceil(N / Bk) (the dense set below), and by
+ *    msa_fwd / msa_bwd for any valid caller-given set.
  */
 #ifndef MSA_H_
 #define MSA_H_
@@ -86,6 +89,11 @@ size_t msa_workspace_size(const msa_problem_t* p, int which);
  *   the raw scores, no exp ("El codiseño del kernel", first idea).  Ties rank the
  *   lower block id first.  When fewer than topk blocks are visible all are taken
  *   and the remaining slots are -1.
+ *   Dense set (indexer warm-up): with topk >= nb every visible block is taken
+ *   (0 .. i/Bk, then -1) without scoring, so msa_fwd, msa_bwd and lse_idx cover the
+ *   full causal context in both branches and the KL is taken over every visible
+ *   token ("Cómo se entrena MSA" ¶3: the warm-up gives both branches full attention
+ *   while the indexer learns from the KL alone).
  *   If lse_idx is not NULL it also writes the index log-sum-exp over the selected
  *   tokens (the cheap recompute of "Accelerating Million-Token Training", ¶4):
  *   lse_idx[b,g,i] = log sum_{j in T(b,g,i)} exp(scale_idx * s[b,g,i,j]), where
@@ -183,7 +191,7 @@ int msa_bwd_varlen(const msa_problem_t* p, const int32_t* cu_seqlens, int num_se
  *      lens: device int32 [B], 1 <= lens[b] <= Lmax (an invalid length is recorded as
  *      MSA_ERR_ARG in the status word and treated as 1).
  * Out: block_idx [B][H_kv][topk] (int32, ascending, -1 padded), o [B][H_q][d] (bf16),
- *      lse [B][H_q] (float32).
+ *      lse [B][H_q] (float32).  topk <= 32.
  * Workspace: msa_decode_workspace_size(p) bytes, 256-byte aligned.
  */
 size_t msa_decode_workspace_size(const msa_problem_t* p);

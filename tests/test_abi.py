@@ -53,7 +53,7 @@ def test_status_strings_and_version():
     (dict(Bk=64), _lib.MSA_ERR_UNSUPPORTED),
     (dict(d=96), _lib.MSA_ERR_UNSUPPORTED),
     (dict(d_idx=16), _lib.MSA_ERR_UNSUPPORTED),
-    (dict(topk=33), _lib.MSA_ERR_UNSUPPORTED),
+    (dict(topk=129), _lib.MSA_ERR_UNSUPPORTED),
     (dict(causal=0), _lib.MSA_ERR_UNSUPPORTED),
     (dict(scale=0.0), _lib.MSA_ERR_ARG),
     (dict(scale=float("nan")), _lib.MSA_ERR_ARG),
@@ -63,6 +63,18 @@ def test_bad_problems_are_rejected_on_the_host(kw, code):
     assert _lib.msa_workspace_size(p, _lib.MSA_WS_FWD) == 0
     assert _lib.msa_index_topk(p, 16, 16, 16, None, None, 0, None) == code
     assert _lib.msa_fwd(p, 16, 16, 16, 16, 16, 16, None, 0, None) == code
+
+
+def test_more_than_32_slots_only_for_the_dense_set():
+    # selection keeps at most 32 blocks: topk = 33 < nb = 64 is refused by the index
+    # entry point on the host, while the forward accepts any caller-given set
+    p = _prob(N=8192, topk=33)
+    assert _lib.msa_index_topk(p, 16, 16, 16, None, None, 0, None) == _lib.MSA_ERR_UNSUPPORTED
+    assert _lib.msa_workspace_size(p, _lib.MSA_WS_FWD) > 0
+    # topk >= nb (every visible block): a valid problem for every entry point
+    p = _prob(N=8192, topk=64)
+    for which in (_lib.MSA_WS_INDEX, _lib.MSA_WS_FWD, _lib.MSA_WS_BWD):
+        assert _lib.msa_workspace_size(p, which) > 0
 
 
 def test_null_and_misaligned_pointers_are_rejected():
