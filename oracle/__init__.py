@@ -4,6 +4,9 @@ TEST INFRASTRUCTURE ONLY: imported by the tests, by the package smoke check and 
 the CPU-baseline leg of the benchmark.  The library under
 block_sparse_gqa_topk_gb300/ never imports it; the two share no code.
 
+fp8.py holds the FP8 (E4M3) KV-cache quantiser and the decode attention over the
+dequantised cache (numpy).
+
 All arrays in and out are numpy.  Inputs are bf16 bit patterns (uint16) from
 block_sparse_gqa_topk_gb300.synth; outputs are float64 (int32 for block ids).
 """
