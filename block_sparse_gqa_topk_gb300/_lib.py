@@ -30,7 +30,8 @@ EXPORTS = ("msa_workspace_size", "msa_index_topk", "msa_fwd", "msa_bwd",
            "msa_set_kernel_events", "msa_kernel_launch_count", "msa_index_topk_noalloc",
            "msa_noalloc_scratch_bytes", "msa_version", "msa_workspace_size_varlen",
            "msa_index_topk_varlen", "msa_fwd_varlen", "msa_bwd_varlen",
-           "msa_decode_workspace_size", "msa_decode")
+           "msa_decode_workspace_size", "msa_decode", "msa_quantize_kv_fp8",
+           "msa_decode_fp8")
 
 MSA_KERNEL_INDEX = 0
 MSA_KERNEL_FWD = 1
@@ -103,6 +104,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_decode_workspace_size.restype = sz
     lib.msa_decode.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.msa_decode.restype = i32
+    lib.msa_quantize_kv_fp8.argtypes = [P, vp, vp, vp, vp]
+    lib.msa_quantize_kv_fp8.restype = i32
+    lib.msa_decode_fp8.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.msa_decode_fp8.restype = i32
     _lib = lib
     return lib
 
@@ -204,6 +209,16 @@ def msa_decode_workspace_size(prob: Problem) -> int:
 def msa_decode(prob, q, q_idx, k, v, k_idx, lens, block_idx, o, lse, ws, ws_bytes, stream) -> int:
     return load().msa_decode(ctypes.byref(prob), q, q_idx, k, v, k_idx, lens, block_idx, o, lse,
                              ws, ws_bytes, stream)
+
+
+def msa_quantize_kv_fp8(prob, x, x8, scale, stream) -> int:
+    return load().msa_quantize_kv_fp8(ctypes.byref(prob), x, x8, scale, stream)
+
+
+def msa_decode_fp8(prob, q, q_idx, k8, v8, k_scale, v_scale, k_idx, lens, block_idx, o, lse, ws,
+                   ws_bytes, stream) -> int:
+    return load().msa_decode_fp8(ctypes.byref(prob), q, q_idx, k8, v8, k_scale, v_scale, k_idx,
+                                 lens, block_idx, o, lse, ws, ws_bytes, stream)
 
 
 def msa_version() -> int:

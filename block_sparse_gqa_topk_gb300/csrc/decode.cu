@@ -17,6 +17,7 @@
 //   decode_attn_kernel    one CTA per (sequence, group, slot): the block's K/V in smem,
 //                         scores and P V on mma.sync, softmax partial (lse); the
 //                         group's last CTA merges its k partials into o and lse.
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -31,6 +32,10 @@ struct DecodeParams {
   const __nv_bfloat16* k;      // [B][Lmax][H_kv][d]
   const __nv_bfloat16* v;      // [B][Lmax][H_kv][d]
   const __nv_bfloat16* k_idx;  // [B][Lmax][d_idx]
+  const uint8_t* k8;           // [B][Lmax][H_kv][d] E4M3 codes (FP8 cache; else null)
+  const uint8_t* v8;
+  const float* k_scale;        // [B][Lmax][H_kv] per-row scales of k8, v8
+  const float* v_scale;
   const int32_t* lens;         // [B], 1 <= lens[b] <= Lmax
   int32_t* block_idx;          // [B][H_kv][topk]
   float* pooled;               // [B][H_kv][nbm]
@@ -220,9 +225,10 @@ __global__ void __launch_bounds__(256) decode_select_kernel(const DecodeParams p
 // The scores go through shared memory for the per-head softmax; P is rounded to bf16
 // for the second product, its row sum l stays fp32.  Writes lse_part and the
 // normalised o_part of the slot.
-template <int D, int NT>
+template <int D, int NT, bool F8>
 __device__ __forceinline__ void block_partial(const DecodeParams& p, uint8_t* dsm, int64_t part,
-                                              int c, int b, int g, float* s_l) {
+                                              int c, int b, int g, float* s_l, float* s_sk,
+                                              float* s_sv) {
   constexpr int KS = D + 8;    // padded K/V row (bf16): conflict-free ldmatrix phases
   constexpr int PS = 128 + 8;  // padded P row (bf16)
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(dsm);
@@ -235,20 +241,67 @@ __device__ __forceinline__ void block_partial(const DecodeParams& p, uint8_t* ds
   const int gq = lane >> 2, tq = lane & 3;
   const int L = seq_len(p, b, p.status);
   const int jmax = min(L - 1, c * 128 + 127) - c * 128;  // last visible row of the block
-  for (int x = threadIdx.x; x < 128 * (D / 8); x += blockDim.x) {
-    const int r = x / (D / 8), ch = x % (D / 8);
-    const bool ok = r <= jmax;  // row c 128 + r < L <= Lmax
-    const int64_t off = ok ? (((int64_t)b * p.Lmax + c * 128 + r) * p.H_kv + g) * D + ch * 8 : 0;
-    cp_async_16(sK + r * KS + ch * 8, p.k + off, ok);
+  if constexpr (F8) {
+    // E4M3 rows: 16 codes per 16-byte load, widened exactly to bf16 in shared memory
+    // (every E4M3 value is a bf16 value); rows past the visible end are zero with
+    // scale 0.  The row scales go to s_sk, s_sv.
+    constexpr int CH = D / 16;                // 16-byte chunks per row
+    constexpr int PER = 128 * CH / 256;       // chunks per thread (256 threads)
+    uint4 kw[PER], vw[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {           // every load in flight before any use
+      const int x = threadIdx.x + u * 256;
+      const int r = x / CH, ch = x % CH;
+      const bool ok = r <= jmax;              // row c 128 + r < L <= Lmax
+      const int64_t off = (((int64_t)b * p.Lmax + c * 128 + r) * p.H_kv + g) * D + ch * 16;
+      kw[u] = ok ? __ldg(reinterpret_cast<const uint4*>(p.k8 + off)) : make_uint4(0, 0, 0, 0);
+      vw[u] = ok ? __ldg(reinterpret_cast<const uint4*>(p.v8 + off)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int x = threadIdx.x + u * 256;
+      const int r = x / CH, ch = x % CH;
+      const uint32_t kk[4] = {kw[u].x, kw[u].y, kw[u].z, kw[u].w};
+      const uint32_t vv[4] = {vw[u].x, vw[u].y, vw[u].z, vw[u].w};
+      uint32_t ko[8], vo[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const __nv_fp8x2_storage_t k2 = (__nv_fp8x2_storage_t)(kk[e >> 1] >> (16 * (e & 1)));
+        const __nv_fp8x2_storage_t v2 = (__nv_fp8x2_storage_t)(vv[e >> 1] >> (16 * (e & 1)));
+        const float2 kf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(k2, __NV_E4M3)));
+        const float2 vf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(v2, __NV_E4M3)));
+        ko[e] = pack_bf16(kf.x, kf.y);
+        vo[e] = pack_bf16(vf.x, vf.y);
+      }
+      uint4* kd = reinterpret_cast<uint4*>(sK + r * KS + ch * 16);
+      uint4* vd = reinterpret_cast<uint4*>(sV + r * KS + ch * 16);
+      kd[0] = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+      kd[1] = make_uint4(ko[4], ko[5], ko[6], ko[7]);
+      vd[0] = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+      vd[1] = make_uint4(vo[4], vo[5], vo[6], vo[7]);
+    }
+    for (int r = threadIdx.x; r < 128; r += blockDim.x) {
+      const bool ok = r <= jmax;
+      const int64_t row = ((int64_t)b * p.Lmax + c * 128 + r) * p.H_kv + g;
+      s_sk[r] = ok ? __ldg(&p.k_scale[row]) : 0.f;
+      s_sv[r] = ok ? __ldg(&p.v_scale[row]) : 0.f;
+    }
+  } else {
+    for (int x = threadIdx.x; x < 128 * (D / 8); x += blockDim.x) {
+      const int r = x / (D / 8), ch = x % (D / 8);
+      const bool ok = r <= jmax;  // row c 128 + r < L <= Lmax
+      const int64_t off = ok ? (((int64_t)b * p.Lmax + c * 128 + r) * p.H_kv + g) * D + ch * 8 : 0;
+      cp_async_16(sK + r * KS + ch * 8, p.k + off, ok);
+    }
+    cp_async_commit();
+    for (int x = threadIdx.x; x < 128 * (D / 8); x += blockDim.x) {
+      const int r = x / (D / 8), ch = x % (D / 8);
+      const bool ok = r <= jmax;
+      const int64_t off = ok ? (((int64_t)b * p.Lmax + c * 128 + r) * p.H_kv + g) * D + ch * 8 : 0;
+      cp_async_16(sV + r * KS + ch * 8, p.v + off, ok);
+    }
+    cp_async_commit();
   }
-  cp_async_commit();
-  for (int x = threadIdx.x; x < 128 * (D / 8); x += blockDim.x) {
-    const int r = x / (D / 8), ch = x % (D / 8);
-    const bool ok = r <= jmax;
-    const int64_t off = ok ? (((int64_t)b * p.Lmax + c * 128 + r) * p.H_kv + g) * D + ch * 8 : 0;
-    cp_async_16(sV + r * KS + ch * 8, p.v + off, ok);
-  }
-  cp_async_commit();
   // B fragments of the scores: B[k = dd][n = h] = q[b][g G + h][dd], zero for h >= G
   uint32_t bq[NT][D / 16][2];
 #pragma unroll
@@ -262,7 +315,7 @@ __device__ __forceinline__ void block_partial(const DecodeParams& p, uint8_t* ds
       bq[nt][ks][1] = h < G ? __ldg(&qrow[ks * 8 + 4 + tq]) : 0u;
     }
   }
-  cp_async_wait<1>();  // K landed
+  if constexpr (!F8) cp_async_wait<1>();  // K landed
   __syncthreads();
   float sc[NT][4];
   {
@@ -284,7 +337,8 @@ __device__ __forceinline__ void block_partial(const DecodeParams& p, uint8_t* ds
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int h = nt * 8 + 2 * tq + (e & 1), r = warp * 16 + gq + (e >> 1) * 8;
-      sS[h * 128 + r] = r <= jmax ? sc[nt][e] * p.scale : -INFINITY;
+      const float raw = F8 ? sc[nt][e] * s_sk[r] : sc[nt][e];  // K row scale
+      sS[h * 128 + r] = r <= jmax ? raw * p.scale : -INFINITY;
     }
   __syncthreads();
   // per head: max, exp, sum (one warp per head); padding heads get P = 0
@@ -305,7 +359,8 @@ __device__ __forceinline__ void block_partial(const DecodeParams& p, uint8_t* ds
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float e = expf(v[i] - m);  // masked: exp(-inf) = 0
-      sP[h * PS + lane + 32 * i] = __float2bfloat16(e);
+      // FP8 cache: the V row scale folds into P (o = sum_j e_j s_j v8_j / l)
+      sP[h * PS + lane + 32 * i] = __float2bfloat16(F8 ? e * s_sv[lane + 32 * i] : e);
       l += e;
     }
 #pragma unroll
@@ -315,7 +370,7 @@ __device__ __forceinline__ void block_partial(const DecodeParams& p, uint8_t* ds
       p.lse_part[part + h] = m + logf(l);
     }
   }
-  cp_async_wait<0>();  // V landed
+  if constexpr (!F8) cp_async_wait<0>();  // V landed
   __syncthreads();
   if (warp < D / 16) {
     float acc[NT][4];
@@ -387,10 +442,11 @@ __device__ __forceinline__ void combine_group(const DecodeParams& p, int b, int 
 // Grid (topk, H_kv, B), 256 threads: CTA (s, g, b) computes the partial of slot s of
 // group g; the last of the group's topk CTAs to finish (an arrival count that the
 // selection kernel zeroed) merges the group's partials into o and lse.
-template <int D, int NT>
+template <int D, int NT, bool F8>
 __global__ void __launch_bounds__(256) decode_attn_kernel(const DecodeParams p) {
   extern __shared__ __align__(16) uint8_t dsm[];
   __shared__ float s_l[8 * NT];
+  __shared__ float s_sk[F8 ? 128 : 1], s_sv[F8 ? 128 : 1];  // FP8 row scales
   __shared__ float s_w[32 * 16];  // [topk][G] merge weights
   __shared__ int s_last;
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -399,7 +455,7 @@ __global__ void __launch_bounds__(256) decode_attn_kernel(const DecodeParams p) 
   if (c < 0) {
     for (int h = threadIdx.x; h < p.G; h += blockDim.x) p.lse_part[part + h] = -INFINITY;
   } else {
-    block_partial<D, NT>(p, dsm, part, c, b, g, s_l);
+    block_partial<D, NT, F8>(p, dsm, part, c, b, g, s_l, s_sk, s_sv);
   }
   __threadfence();  // this CTA's partial is visible before its arrival
   __syncthreads();
@@ -425,32 +481,78 @@ size_t decode_ws_parts(const Shape& s, size_t* off_pooled, size_t* off_o, size_t
   return off;
 }
 
-}  // namespace
-}  // namespace msa
-
-using namespace msa;
-
-extern "C" {
-
-size_t msa_decode_workspace_size(const msa_problem_t* p) {
-  Shape s;
-  if (validate_problem(p, &s) != MSA_OK) return 0;
-  size_t a, b, c, d;
-  return decode_ws_parts(s, &a, &b, &c, &d);
+// E4M3 codes and per-row scales of a [rows][D] bf16 tensor (the FP8 KV cache): one
+// warp per row; scale = amax / 448 (1 for an all-zero row), code = nearest E4M3 value
+// of x / scale with ties to even and saturation at 448.  Both divisions are IEEE
+// round-to-nearest so the codes are reproducible bit for bit.
+template <int D>
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x,
+                                                            uint8_t* __restrict__ x8,
+                                                            float* __restrict__ scale,
+                                                            int64_t rows) {
+  constexpr int E = D / 32;  // values per lane
+  const int lane = threadIdx.x & 31;
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (row >= rows) return;
+  float v[E];
+  const __nv_bfloat16* src = x + row * D + lane * E;
+  if constexpr (E == 4) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
+    v[0] = __low2float(a); v[1] = __high2float(a); v[2] = __low2float(c); v[3] = __high2float(c);
+  } else {
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src));
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&w);
+    v[0] = __low2float(a); v[1] = __high2float(a);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(v[e]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float sc = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  uint32_t packed = 0;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    const float2 f = make_float2(__fdiv_rn(v[e], sc), __fdiv_rn(v[e + 1], sc));
+    const uint32_t two = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+    packed |= (two & 0xFFFFu) << (8 * e);
+  }
+  uint8_t* dst = x8 + row * D + lane * E;
+  if constexpr (E == 4) *reinterpret_cast<uint32_t*>(dst) = packed;
+  else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+  if (lane == 0) scale[row] = sc;
 }
 
-int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const void* k,
-               const void* v, const void* k_idx, const int32_t* lens, int32_t* block_idx, void* o,
-               float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+// The cache a decode call reads: bf16 k, v, or E4M3 codes with their row scales.
+struct DecodeCache {
+  const void* k;
+  const void* v;
+  const uint8_t* k8;
+  const uint8_t* v8;
+  const float* k_scale;
+  const float* v_scale;
+};
+
+// Shared driver of msa_decode and msa_decode_fp8: index pooling and selection
+// (bf16 index branch), then the split attention over the selected blocks.
+int run_decode(const msa_problem_t* p, const void* q, const void* q_idx, const DecodeCache& kv,
+               const void* k_idx, const int32_t* lens, int32_t* block_idx, void* o, float* lse,
+               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   Shape s;
   int rc = validate_problem(p, &s);
   if (rc) return rc;
   if (s.B == 0) return MSA_OK;
   if (s.N == 0) return MSA_ERR_SHAPE;  // N is the cache capacity Lmax
   if (s.topk > kMaxSelect) return MSA_ERR_UNSUPPORTED;
-  const void* ptrs[] = {q, q_idx, k, v, k_idx, lens, block_idx, o, lse};
+  const bool f8 = kv.k8 != nullptr;
+  const void* ptrs[] = {q, q_idx, f8 ? (const void*)kv.k8 : kv.k, f8 ? (const void*)kv.v8 : kv.v,
+                        k_idx, lens, block_idx, o, lse};
   for (const void* x : ptrs)
     if (!x || (reinterpret_cast<uintptr_t>(x) & 15) != 0) return MSA_ERR_ARG;
+  if (f8 && ((reinterpret_cast<uintptr_t>(kv.k_scale) & 3) || (reinterpret_cast<uintptr_t>(kv.v_scale) & 3)))
+    return MSA_ERR_ARG;
   size_t off_pooled, off_o, off_lse, off_arrive;
   const size_t need = decode_ws_parts(s, &off_pooled, &off_o, &off_lse, &off_arrive);
   if (!workspace || workspace_bytes < need) return MSA_ERR_WORKSPACE;
@@ -461,8 +563,12 @@ int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const v
   DecodeParams dp;
   dp.q = static_cast<const __nv_bfloat16*>(q);
   dp.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
-  dp.k = static_cast<const __nv_bfloat16*>(k);
-  dp.v = static_cast<const __nv_bfloat16*>(v);
+  dp.k = static_cast<const __nv_bfloat16*>(kv.k);
+  dp.v = static_cast<const __nv_bfloat16*>(kv.v);
+  dp.k8 = kv.k8;
+  dp.v8 = kv.v8;
+  dp.k_scale = kv.k_scale;
+  dp.v_scale = kv.v_scale;
   dp.k_idx = static_cast<const __nv_bfloat16*>(k_idx);
   dp.lens = lens;
   dp.block_idx = block_idx;
@@ -483,7 +589,8 @@ int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const v
   dp.scale = s.scale;
   dp.status = cx.status;
   const int pool_nt = s.H_kv > 8 ? 2 : 1;
-  const dim3 gpool((unsigned)((s.nb + 7) / 8), (unsigned)s.B, (unsigned)((s.H_kv + 8 * pool_nt - 1) / (8 * pool_nt)));
+  const dim3 gpool((unsigned)((s.nb + 7) / 8), (unsigned)s.B,
+                   (unsigned)((s.H_kv + 8 * pool_nt - 1) / (8 * pool_nt)));
 #define MSA_POOL(DI, NT) decode_pool_kernel<DI, NT><<<gpool, 256, 0, stream>>>(dp)
   if (s.d_idx == 64) {
     if (pool_nt == 1) MSA_POOL(64, 1); else MSA_POOL(64, 2);
@@ -499,19 +606,80 @@ int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const v
   const size_t attn_smem = (size_t)2 * 128 * (s.d + 8) * 2;
   const dim3 gattn((unsigned)s.topk, (unsigned)s.H_kv, (unsigned)s.B);
   cudaError_t e = cudaSuccess;
-#define MSA_ATTN(D, NT)                                                                      \
-  do {                                                                                       \
-    e = cudaFuncSetAttribute(decode_attn_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             (int)attn_smem);                                                \
-    if (e == cudaSuccess) decode_attn_kernel<D, NT><<<gattn, 256, attn_smem, stream>>>(dp);  \
+#define MSA_ATTN(D, NT, F8)                                                                   \
+  do {                                                                                        \
+    e = cudaFuncSetAttribute(decode_attn_kernel<D, NT, F8>,                                   \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem);    \
+    if (e == cudaSuccess) decode_attn_kernel<D, NT, F8><<<gattn, 256, attn_smem, stream>>>(dp); \
   } while (0)
-  if (s.d == 128) {
-    if (s.G <= 8) MSA_ATTN(128, 1); else MSA_ATTN(128, 2);
+  if (f8) {
+    if (s.d == 128) {
+      if (s.G <= 8) MSA_ATTN(128, 1, true); else MSA_ATTN(128, 2, true);
+    } else {
+      if (s.G <= 8) MSA_ATTN(64, 1, true); else MSA_ATTN(64, 2, true);
+    }
   } else {
-    if (s.G <= 8) MSA_ATTN(64, 1); else MSA_ATTN(64, 2);
+    if (s.d == 128) {
+      if (s.G <= 8) MSA_ATTN(128, 1, false); else MSA_ATTN(128, 2, false);
+    } else {
+      if (s.G <= 8) MSA_ATTN(64, 1, false); else MSA_ATTN(64, 2, false);
+    }
   }
 #undef MSA_ATTN
   if (e != cudaSuccess) return MSA_ERR_CUDA;
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+size_t msa_decode_workspace_size(const msa_problem_t* p) {
+  Shape s;
+  if (validate_problem(p, &s) != MSA_OK) return 0;
+  size_t a, b, c, d;
+  return decode_ws_parts(s, &a, &b, &c, &d);
+}
+
+int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const void* k,
+               const void* v, const void* k_idx, const int32_t* lens, int32_t* block_idx, void* o,
+               float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  DecodeCache kv = {k, v, nullptr, nullptr, nullptr, nullptr};
+  return run_decode(p, q, q_idx, kv, k_idx, lens, block_idx, o, lse, workspace, workspace_bytes,
+                    stream);
+}
+
+int msa_decode_fp8(const msa_problem_t* p, const void* q, const void* q_idx, const uint8_t* k8,
+                   const uint8_t* v8, const float* k_scale, const float* v_scale, const void* k_idx,
+                   const int32_t* lens, int32_t* block_idx, void* o, float* lse, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+  if (!k8 || !v8 || !k_scale || !v_scale) return MSA_ERR_ARG;
+  DecodeCache kv = {nullptr, nullptr, k8, v8, k_scale, v_scale};
+  return run_decode(p, q, q_idx, kv, k_idx, lens, block_idx, o, lse, workspace, workspace_bytes,
+                    stream);
+}
+
+int msa_quantize_kv_fp8(const msa_problem_t* p, const void* x, uint8_t* x8, float* scale,
+                        cudaStream_t stream) {
+  Shape s;
+  int rc = validate_problem(p, &s);
+  if (rc) return rc;
+  const int64_t rows = (int64_t)s.B * s.N * s.H_kv;
+  if (rows == 0) return MSA_OK;
+  const void* ptrs[] = {x, x8, scale};
+  for (const void* t : ptrs)
+    if (!t || (reinterpret_cast<uintptr_t>(t) & 15) != 0) return MSA_ERR_ARG;
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  if (s.d == 128)
+    quantize_fp8_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), x8,
+                                                        scale, rows);
+  else
+    quantize_fp8_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), x8,
+                                                       scale, rows);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }

@@ -306,3 +306,51 @@ def msa_decode(q, q_idx, k, v, k_idx, lens, topk: int = 16, *, scale=None, Bk: i
                          _ptr(block_idx), _ptr(o), _ptr(lse), _ptr(ws), nws, _stream(dev))
     _lib.check(rc, "msa_decode")
     return block_idx, o, lse
+
+
+def msa_quantize_kv_fp8(x, *, Bk: int = 128):
+    """x [B,Lmax,H_kv,d] bf16 (a k or v cache) -> (codes [B,Lmax,H_kv,d] uint8 E4M3,
+    scale [B,Lmax,H_kv] f32): one scale amax/448 per (sequence, token, head) row."""
+    _need(x, "x", ndim=4)
+    B, Lmax, H_kv, d = x.shape
+    prob = make_problem(B, Lmax, H_kv, H_kv, d, 64, 1, Bk, True, None, None)
+    x8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scale = torch.empty((B, Lmax, H_kv), dtype=torch.float32, device=x.device)
+    rc = _lib.msa_quantize_kv_fp8(prob, _ptr(x), _ptr(x8), _ptr(scale), _stream(x.device))
+    _lib.check(rc, "msa_quantize_kv_fp8")
+    return x8, scale
+
+
+def msa_decode_fp8(q, q_idx, k8, v8, k_scale, v_scale, k_idx, lens, topk: int = 16, *,
+                   scale=None, Bk: int = 128):
+    """msa_decode over an FP8 cache: k8, v8 [B,Lmax,H_kv,d] uint8 codes and k_scale,
+    v_scale [B,Lmax,H_kv] f32 from msa_quantize_kv_fp8.  Returns (block_idx [B,H_kv,topk]
+    int32, o [B,H_q,d] bf16, lse [B,H_q] f32)."""
+    _need(q, "q", ndim=3)
+    _need(q_idx, "q_idx", ndim=3)
+    _need(k8, "k8", torch.uint8, ndim=4)
+    _need(v8, "v8", torch.uint8, ndim=4)
+    _need(k_scale, "k_scale", torch.float32, ndim=3)
+    _need(v_scale, "v_scale", torch.float32, ndim=3)
+    _need(k_idx, "k_idx", ndim=3)
+    _need(lens, "lens", torch.int32, ndim=1)
+    B, H_q, d = q.shape
+    _, Lmax, H_kv, _ = k8.shape
+    d_idx = q_idx.shape[2]
+    if (tuple(v8.shape) != tuple(k8.shape) or tuple(k_scale.shape) != (B, Lmax, H_kv)
+            or tuple(v_scale.shape) != (B, Lmax, H_kv) or tuple(k_idx.shape) != (B, Lmax, d_idx)
+            or lens.numel() != B):
+        raise ValueError("cache shapes must agree: k8, v8 [B,Lmax,H_kv,d], scales [B,Lmax,H_kv], "
+                         "k_idx [B,Lmax,d_idx], lens [B]")
+    prob = make_problem(B, Lmax, H_q, H_kv, d, d_idx, topk, Bk, True, scale, None)
+    dev = q.device
+    block_idx = torch.empty((B, H_kv, topk), dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H_q), dtype=torch.float32, device=dev)
+    nws = _lib.msa_decode_workspace_size(prob)
+    ws = _workspace(nws, dev)
+    rc = _lib.msa_decode_fp8(prob, _ptr(q), _ptr(q_idx), _ptr(k8), _ptr(v8), _ptr(k_scale),
+                             _ptr(v_scale), _ptr(k_idx), _ptr(lens), _ptr(block_idx), _ptr(o),
+                             _ptr(lse), _ptr(ws), nws, _stream(dev))
+    _lib.check(rc, "msa_decode_fp8")
+    return block_idx, o, lse

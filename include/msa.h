@@ -199,6 +199,29 @@ int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const v
                const void* v, const void* k_idx, const int32_t* lens, int32_t* block_idx, void* o,
                float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * FP8 KV cache (E4M3).  The pages name FP8 as one of the precisions of the MSA
+ * attention kernels ("El codiseño del kernel", fmha_sm100 paragraph) and give no
+ * recipe; this build takes one float32 scale per (sequence, token, KV head) row:
+ *   scale = amax |x| / 448 (1 for an all-zero row),
+ *   code  = the E4M3 value nearest to x / scale (ties to even, |.| > 448 saturates),
+ *   value seen by attention = decode(code) * scale.
+ * Both divisions are IEEE round-to-nearest, so the codes are reproducible bit for bit.
+ *
+ * msa_quantize_kv_fp8: x [B][N][H_kv][d] bf16 (a k or v cache, p->N its capacity)
+ *   -> x8 [B][N][H_kv][d] uint8 codes, scale [B][N][H_kv] float32.  Call once for k,
+ *   once for v.  Pointers 16-byte aligned.
+ * msa_decode_fp8: msa_decode with the cache given as k8, v8 (codes) and k_scale,
+ *   v_scale (row scales) instead of bf16 k, v; the index branch (q_idx, k_idx) stays
+ *   bf16.  Same outputs, workspace (msa_decode_workspace_size) and errors.
+ */
+int msa_quantize_kv_fp8(const msa_problem_t* p, const void* x, uint8_t* x8, float* scale,
+                        cudaStream_t stream);
+int msa_decode_fp8(const msa_problem_t* p, const void* q, const void* q_idx, const uint8_t* k8,
+                   const uint8_t* v8, const float* k_scale, const float* v_scale, const void* k_idx,
+                   const int32_t* lens, int32_t* block_idx, void* o, float* lse, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status word
  * (MSA_OK or the first MSA_ERR_* a kernel recorded since the last read). */
 int msa_get_device_status(cudaStream_t stream, int* status);
