@@ -317,7 +317,7 @@ def run_ours(args, cfg, rank, world):
             raise RuntimeError("device status after warm-up leg: "
                                + _lib.status_string(ops.device_status()))
         if rank == 0:
-            print(json.dumps({"warmup": wu}), flush=True)
+            print(json.dumps({"indexer_warmup": wu}), flush=True)
         return
     if args.decode_only:  # the decode leg alone (e.g. for a profiler's launch list)
         peaks, _ = load_peaks()
@@ -501,7 +501,7 @@ def run_ours(args, cfg, rank, world):
                     "d2h_bytes_per_step": 4, "steps": e2e_steps},
             "cpu_baseline": cpu,
             "decode": dec,
-            "warmup": wu,
+            "indexer_warmup": wu,
             "gpu_launches": launches,
             "clocks": clk,
         }
@@ -515,7 +515,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default="128k", choices=sorted(synth.CONFIGS))
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-rows", type=int, default=1400)
     ap.add_argument("--ref-rows", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")

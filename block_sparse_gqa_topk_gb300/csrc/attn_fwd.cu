@@ -17,8 +17,8 @@ namespace {
 
 // o[b,i,h] and lse[b,h,i] from the k partials of each (b, g, i) row.  One warp per
 // row: the partials of one slot are G*D contiguous bf16 (all heads of the group), read
-// as 16-byte chunks.  G lanes find each head's max and sum over the slots (any number
-// of slots); every lane then forms the weight exp(lse_s - m) / l of its chunk's head.
+// as 16-byte chunks; the per-(slot, head) weights exp(lse_s - lse) come from shared
+// memory, computed by G lanes.  Up to 32 slots (every selected set).
 template <int D, int G>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(
     const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
     float* __restrict__ lse, int64_t rows, int N, int H_kv, int topk, int nb) {
   constexpr int TC = G * D / 8;              // 16-byte chunks per slot
   constexpr int CPL = (TC + 31) / 32;        // chunks per lane
-  __shared__ float s_mi[8][2 * G];           // per head: max, 1 / sum
+  __shared__ float wts[8][32 * G];
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t rkv = (int64_t)blockIdx.x * 8 + wib;  // (b*H_kv + g)*N + i
   if (rkv >= rows) return;
@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
   const int g = (int)(bg % H_kv);
   const int64_t b = bg / H_kv;
   const int32_t* sel = block_idx + rkv * topk;
+  float* w = wts[wib];
   if (lane < G) {
     const int h = lane;
     float m = -INFINITY;
@@ -46,10 +47,12 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
     for (int s = 0; s < topk; ++s) {
       const int c = __ldg(&sel[s]);
       const float ls = (c >= 0 && c < nb) ? __ldg(&lse_part[(rkv * topk + s) * G + h]) : -INFINITY;
-      l += ls == -INFINITY ? 0.f : __expf(ls - m);
+      const float e = ls == -INFINITY ? 0.f : __expf(ls - m);
+      w[s * G + h] = e;
+      l += e;
     }
-    s_mi[wib][h] = m;
-    s_mi[wib][G + h] = l > 0.f ? 1.f / l : 0.f;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    for (int s = 0; s < topk; ++s) w[s * G + h] *= inv;
     lse[(b * H_kv * G + g * G + h) * N + i] = m + logf(l);
   }
   __syncwarp();
@@ -66,15 +69,106 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
     for (int x = 0; x < CPL; ++x) {
       const int ch = lane + 32 * x;
       if (ch < TC) {
-        const int h = (ch * 8) / D;
-        const float wt = __expf(__ldg(&lse_part[(rkv * topk + s) * G + h]) - s_mi[wib][h]) *
-                         s_mi[wib][G + h];
+        const float wt = w[s * G + (ch * 8) / D];
         const uint4 raw = __ldg(&src[ch]);
         const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           acc[x][2 * e] += wt * __low2float(pr[e]);
           acc[x][2 * e + 1] += wt * __high2float(pr[e]);
+        }
+      }
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(o + ((b * N + i) * H_kv * G + (int64_t)g * G) * D);
+#pragma unroll
+  for (int x = 0; x < CPL; ++x) {
+    const int ch = lane + 32 * x;
+    if (ch < TC) {
+      uint4 out;
+      uint32_t* pw = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pw[e] = pack_bf16(acc[x][2 * e], acc[x][2 * e + 1]);
+      dst[ch] = out;
+    }
+  }
+}
+
+// The same merge for rows of more than 32 slots (the dense set of the indexer
+// warm-up): G lanes find each head's max m and sum l over the slots and lay the
+// weights exp(lse_s - m) / l out in shared memory 32 slots at a time (the first 32
+// from the sum pass, later ones recomputed).
+template <int D, int G>
+__global__ void __launch_bounds__(256) fwd_combine_wide_kernel(
+    const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
+    const int32_t* __restrict__ block_idx, __nv_bfloat16* __restrict__ o,
+    float* __restrict__ lse, int64_t rows, int N, int H_kv, int topk, int nb) {
+  constexpr int TC = G * D / 8;              // 16-byte chunks per slot
+  constexpr int CPL = (TC + 31) / 32;        // chunks per lane
+  __shared__ float wts[8][32 * G];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t rkv = (int64_t)blockIdx.x * 8 + wib;  // (b*H_kv + g)*N + i
+  if (rkv >= rows) return;
+  const int i = (int)(rkv % N);
+  const int64_t bg = rkv / N;
+  const int g = (int)(bg % H_kv);
+  const int64_t b = bg / H_kv;
+  const int32_t* sel = block_idx + rkv * topk;
+  float* w = wts[wib];
+  float m = -INFINITY, inv = 0.f;
+  if (lane < G) {
+    const int h = lane;
+    for (int s = 0; s < topk; ++s) {
+      const int c = __ldg(&sel[s]);
+      if (c >= 0 && c < nb) m = fmaxf(m, __ldg(&lse_part[(rkv * topk + s) * G + h]));
+    }
+    float l = 0.f;
+    for (int s = 0; s < topk; ++s) {
+      const int c = __ldg(&sel[s]);
+      const float ls = (c >= 0 && c < nb) ? __ldg(&lse_part[(rkv * topk + s) * G + h]) : -INFINITY;
+      const float e = ls == -INFINITY ? 0.f : __expf(ls - m);
+      if (s < 32) w[s * G + h] = e;  // the first chunk's weights, scaled below
+      l += e;
+    }
+    inv = l > 0.f ? 1.f / l : 0.f;
+    for (int s = 0; s < min(32, topk); ++s) w[s * G + h] *= inv;
+    lse[(b * H_kv * G + g * G + h) * N + i] = m + logf(l);
+  }
+  float acc[CPL][8];
+#pragma unroll
+  for (int x = 0; x < CPL; ++x)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[x][e] = 0.f;
+  for (int s0 = 0; s0 < topk; s0 += 32) {
+    const int ns = min(32, topk - s0);
+    __syncwarp();  // the previous chunk's weights are consumed
+    if (s0 > 0 && lane < G) {  // slots beyond the first 32 (the dense set only)
+      const int h = lane;
+      for (int t = 0; t < ns; ++t) {
+        const int c = __ldg(&sel[s0 + t]);
+        const float ls =
+            (c >= 0 && c < nb) ? __ldg(&lse_part[(rkv * topk + s0 + t) * G + h]) : -INFINITY;
+        w[t * G + h] = ls == -INFINITY ? 0.f : __expf(ls - m) * inv;
+      }
+    }
+    __syncwarp();
+    for (int t = 0; t < ns; ++t) {
+      const int s = s0 + t;
+      const int c = __ldg(&sel[s]);
+      if (c < 0 || c >= nb) continue;  // same for every lane
+      const uint4* src = reinterpret_cast<const uint4*>(o_part + (rkv * topk + s) * G * D);
+#pragma unroll
+      for (int x = 0; x < CPL; ++x) {
+        const int ch = lane + 32 * x;
+        if (ch < TC) {
+          const float wt = w[t * G + (ch * 8) / D];
+          const uint4 raw = __ldg(&src[ch]);
+          const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[x][2 * e] += wt * __low2float(pr[e]);
+            acc[x][2 * e + 1] += wt * __high2float(pr[e]);
+          }
         }
       }
     }
@@ -103,9 +197,16 @@ cudaError_t launch_attn_fwd(const Shape& s, const void* q, const void* k, const 
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((s.rows_kv() + 7) / 8);
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
-#define MSA_COMBINE(DD, GG)                                                                 \
-  fwd_combine_kernel<DD, GG><<<grid, 256, 0, st>>>(o_part, lse_part, block_idx, ob, lse,     \
-                                                   s.rows_kv(), s.N, s.H_kv, s.topk, s.nb)
+#define MSA_COMBINE(DD, GG)                                                                   \
+  do {                                                                                         \
+    if (s.topk <= 32)                                                                          \
+      fwd_combine_kernel<DD, GG><<<grid, 256, 0, st>>>(o_part, lse_part, block_idx, ob, lse,   \
+                                                       s.rows_kv(), s.N, s.H_kv, s.topk, s.nb); \
+    else                                                                                       \
+      fwd_combine_wide_kernel<DD, GG><<<grid, 256, 0, st>>>(o_part, lse_part, block_idx, ob,   \
+                                                            lse, s.rows_kv(), s.N, s.H_kv,     \
+                                                            s.topk, s.nb);                     \
+  } while (0)
   if (s.d == 128) {
     switch (s.G) {
       case 1: MSA_COMBINE(128, 1); break;
