@@ -665,16 +665,20 @@ int msa_decode_fp8(const msa_problem_t* p, const void* q, const void* q_idx, con
 
 int msa_quantize_kv_fp8(const msa_problem_t* p, const void* x, uint8_t* x8, float* scale,
                         cudaStream_t stream) {
-  Shape s;
-  int rc = validate_problem(p, &s);
-  if (rc) return rc;
-  const int64_t rows = (int64_t)s.B * s.N * s.H_kv;
+  // only the cache's sizes matter here: B, N (capacity), H_kv, d
+  if (!p) return MSA_ERR_ARG;
+  if (p->B < 0 || p->N < 0 || p->H_kv <= 0) return MSA_ERR_SHAPE;
+  if (p->d != 64 && p->d != 128) return MSA_ERR_UNSUPPORTED;
+  const int64_t rows = (int64_t)p->B * p->N * p->H_kv;
   if (rows == 0) return MSA_OK;
+  if (rows > ((int64_t)1 << 40)) return MSA_ERR_UNSUPPORTED;
   const void* ptrs[] = {x, x8, scale};
   for (const void* t : ptrs)
     if (!t || (reinterpret_cast<uintptr_t>(t) & 15) != 0) return MSA_ERR_ARG;
-  const unsigned grid = (unsigned)((rows + 7) / 8);
-  if (s.d == 128)
+  const int64_t blocks = (rows + 7) / 8;
+  if (blocks > 0x7fffffffLL) return MSA_ERR_UNSUPPORTED;
+  const unsigned grid = (unsigned)blocks;
+  if (p->d == 128)
     quantize_fp8_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), x8,
                                                         scale, rows);
   else

@@ -210,7 +210,8 @@ int msa_decode(const msa_problem_t* p, const void* q, const void* q_idx, const v
  *
  * msa_quantize_kv_fp8: x [B][N][H_kv][d] bf16 (a k or v cache, p->N its capacity)
  *   -> x8 [B][N][H_kv][d] uint8 codes, scale [B][N][H_kv] float32.  Call once for k,
- *   once for v.  Pointers 16-byte aligned.
+ *   once for v.  Only p->B, p->N, p->H_kv and p->d (64 or 128) are read.  Pointers
+ *   16-byte aligned; the output buffers are overwritten.
  * msa_decode_fp8: msa_decode with the cache given as k8, v8 (codes) and k_scale,
  *   v_scale (row scales) instead of bf16 k, v; the index branch (q_idx, k_idx) stays
  *   bf16.  Same outputs, workspace (msa_decode_workspace_size) and errors.

@@ -87,6 +87,25 @@ def test_null_and_misaligned_pointers_are_rejected():
     assert _lib.msa_fwd(p, 16, 16, 16, 16, 16, 16, 256, small, None) == _lib.MSA_ERR_WORKSPACE
 
 
+def test_decode_and_fp8_entry_points_reject_bad_arguments_on_the_host():
+    p = _prob()
+    ws = _lib.msa_decode_workspace_size(p)
+    assert ws > 0
+    # decode: null / misaligned pointers, missing FP8 scales, too many slots to select
+    assert _lib.msa_decode(p, None, 16, 16, 16, 16, 16, 16, 16, 16, 256, ws, None) == _lib.MSA_ERR_ARG
+    assert _lib.msa_decode(p, 16, 16, 24, 16, 16, 16, 16, 16, 16, 256, ws, None) == _lib.MSA_ERR_ARG
+    assert _lib.msa_decode_fp8(p, 16, 16, 16, 16, None, 16, 16, 16, 16, 16, 16, 256, ws,
+                               None) == _lib.MSA_ERR_ARG
+    assert _lib.msa_decode(_prob(topk=40), 16, 16, 16, 16, 16, 16, 16, 16, 16, 256, 1 << 30,
+                           None) == _lib.MSA_ERR_UNSUPPORTED
+    # quantiser: only the cache sizes matter; d must be 64 or 128, pointers aligned
+    assert _lib.msa_quantize_kv_fp8(_prob(d=96), 16, 16, 16, None) == _lib.MSA_ERR_UNSUPPORTED
+    assert _lib.msa_quantize_kv_fp8(p, 16, None, 16, None) == _lib.MSA_ERR_ARG
+    assert _lib.msa_quantize_kv_fp8(p, 16, 20, 16, None) == _lib.MSA_ERR_ARG
+    assert _lib.msa_quantize_kv_fp8(_prob(N=0), None, None, None, None) == _lib.MSA_OK
+    assert _lib.msa_quantize_kv_fp8(_prob(H_kv=0, H_q=0), 16, 16, 16, None) == _lib.MSA_ERR_SHAPE
+
+
 def test_empty_problem_is_a_no_op():
     p = _prob(N=0)
     assert _lib.msa_index_topk(p, None, None, None, None, None, 0, None) == _lib.MSA_OK
