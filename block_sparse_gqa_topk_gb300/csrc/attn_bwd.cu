@@ -194,18 +194,19 @@ cudaError_t run_bwd(const Shape& s, const void* q, const void* k, const void* v,
       const int64_t warps = (R + rpw - 1) / rpw;
       return (unsigned)((warps + 7) / 8);
     };
-    if (s.d == 128 && s.G == 4)
-      slot_reduce_kernel<128, 4><<<grid_for(64), 256, 0, st>>>(w.dq_part, block_idx, dqb, R, s.N,
-                                                              s.H_kv, s.topk, s.nb);
-    else if (s.d == 128)
-      slot_reduce_kernel<128, 8><<<grid_for(128), 256, 0, st>>>(w.dq_part, block_idx, dqb, R, s.N,
-                                                               s.H_kv, s.topk, s.nb);
-    else if (s.G == 4)
-      slot_reduce_kernel<64, 4><<<grid_for(32), 256, 0, st>>>(w.dq_part, block_idx, dqb, R, s.N,
-                                                             s.H_kv, s.topk, s.nb);
-    else
-      slot_reduce_kernel<64, 8><<<grid_for(64), 256, 0, st>>>(w.dq_part, block_idx, dqb, R, s.N,
-                                                             s.H_kv, s.topk, s.nb);
+#define MSA_SLOT_REDUCE(W, GG)                                                                \
+  slot_reduce_kernel<W, GG><<<grid_for(GG * W / 8), 256, 0, st>>>(w.dq_part, block_idx, dqb, R, \
+                                                                  s.N, s.H_kv, s.topk, s.nb)
+    if (s.d == 128) {
+      if (s.G == 4) MSA_SLOT_REDUCE(128, 4);
+      else if (s.G == 8) MSA_SLOT_REDUCE(128, 8);
+      else MSA_SLOT_REDUCE(128, 16);
+    } else {
+      if (s.G == 4) MSA_SLOT_REDUCE(64, 4);
+      else if (s.G == 8) MSA_SLOT_REDUCE(64, 8);
+      else MSA_SLOT_REDUCE(64, 16);
+    }
+#undef MSA_SLOT_REDUCE
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (s.d_idx == 64)

@@ -458,8 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t zr[QH];
           if constexpr (QH == 8) {
             tmem_ld_32x32b_x8(tmem + lb + cZ + QH * wg, zr);
-          } else {
+          } else if constexpr (QH == 4) {
             tmem_ld_32x32b_x4(tmem + lb + cZ + QH * wg, zr);
+          } else {
+            tmem_ld_32x32b_x2(tmem + lb + cZ + QH * wg, zr);
           }
           tmem_wait_ld();
           float klc = 0.f;
@@ -482,8 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           kl += (double)(klc * kLn2);
           if constexpr (QH == 8) {  // slots 8 wg .. 8 wg + 7: one 16-byte chunk of the dz row
             *reinterpret_cast<uint4*>(sDZ + swz32(tl, wg)) = make_uint4(dzp[0], dzp[1], dzp[2], dzp[3]);
-          } else {                  // slots 4 wg .. 4 wg + 3: half of chunk 0
+          } else if constexpr (QH == 4) {  // slots 4 wg .. 4 wg + 3: half of chunk 0
             *reinterpret_cast<uint2*>(sDZ + swz32(tl, 0) + 8 * wg) = make_uint2(dzp[0], dzp[1]);
+          } else {                         // slots 2 wg, 2 wg + 1: a quarter of chunk 0
+            *reinterpret_cast<uint32_t*>(sDZ + swz32(tl, 0) + 4 * wg) = dzp[0];
           }
         }
         fence_async_smem();
@@ -495,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&e_wg[wg]);
         ok = __all_sync(0xffffffffu, mbar_wait(&e_wg[wg], u & 1, p.wait_ns, abort_flag));
         if (!ok) break;
-        // this warpgroup's slots are n8 tile nt of dz (G = 4); with G = 8 both warpgroups
-        // share tile 0 and each keeps its own four slots
+        // this warpgroup's slots are n8 tile nt of dz (G = 4); with G = 8 or 16 both
+        // warpgroups share tile 0 and each keeps its own QH slots
         constexpr int NT = (G == 4) ? 1 : 0;
         const int nt = NT ? wg : 0;
         if (16 * q4 < p.DI) {
@@ -520,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qs = 8 * nt + (lane & 3) * 2 + (e & 1);
             const int dd = 16 * q4 + (lane >> 2) + ((e >> 1) << 3);
             const int qp = s_qp[qs];
-            if ((NT || ((lane & 3) >> 1) == wg) && qp >= 0)
+            if ((NT || qs / QH == wg) && qp >= 0)
               p.dqi_part[(int64_t)qp * p.DI + dd] = __float2bfloat16(acc[e] * p.sidx);
           }
         }
@@ -708,8 +712,12 @@ cudaError_t launch_attn_bwd_tc(const Shape& s, const void* q, const void* k, con
   p.w = kl_weight;
   p.wait_ns = cx.wait_ns;
   p.status = cx.status;
-  if (s.d == 128) return s.G == 4 ? launch_dg<128, 4>(p, tk, tv, cx, st) : launch_dg<128, 8>(p, tk, tv, cx, st);
-  return s.G == 4 ? launch_dg<64, 4>(p, tk, tv, cx, st) : launch_dg<64, 8>(p, tk, tv, cx, st);
+  if (s.d == 128) {
+    if (s.G == 4) return launch_dg<128, 4>(p, tk, tv, cx, st);
+    return s.G == 8 ? launch_dg<128, 8>(p, tk, tv, cx, st) : launch_dg<128, 16>(p, tk, tv, cx, st);
+  }
+  if (s.G == 4) return launch_dg<64, 4>(p, tk, tv, cx, st);
+  return s.G == 8 ? launch_dg<64, 8>(p, tk, tv, cx, st) : launch_dg<64, 16>(p, tk, tv, cx, st);
 }
 
 }  // namespace msa
