@@ -51,3 +51,28 @@ def test_decode_matches_oracle_last_row(name):
         eo = np.abs(o[b] - o_ref[0]).max()
         el = np.abs(lse[b] - lse_ref[0]).max()
         assert eo <= O_TOL and el <= LSE_TOL, (name, b, eo, el)
+
+
+def test_decode_invalid_length_is_reported_and_bounded():
+    """A cache length outside [1, Lmax] is recorded as MSA_ERR_ARG in the status word and
+    the row is served as a one-token cache (no access past the cache)."""
+    from block_sparse_gqa_topk_gb300 import _lib
+    cfg = T.with_(name="dec-bad-len", B=2, N=1024, seed=65)
+    h = host_inputs(cfg)
+    d = {n: to_dev(h[n]) for n in ("q", "k", "v", "q_idx", "k_idx")}
+    q_new = d["q"][:, 0].contiguous()
+    qi_new = d["q_idx"][:, 0].contiguous()
+    for bad in (0, cfg.N + 1):
+        lens_t = torch.tensor([bad, 1], dtype=torch.int32, device="cuda")
+        bi, o, lse = ops.msa_decode(q_new, qi_new, d["k"], d["v"], d["k_idx"], lens_t, cfg.topk,
+                                    scale=cfg.scale)
+        assert ops.device_status() == _lib.MSA_ERR_ARG
+        bi = bi.cpu().numpy()
+        assert (bi[:, :, 0] == 0).all() and (bi[:, :, 1:] == -1).all()
+        # both rows: attention over token 0 alone, o = v[b, 0] of the head's group
+        o = f64(o)
+        for b in range(cfg.B):
+            for hq in range(cfg.H_q):
+                ref = f64(d["v"][b, 0, hq // cfg.G])
+                assert np.abs(o[b, hq] - ref).max() <= O_TOL
+    assert ops.device_status() == 0
