@@ -198,13 +198,21 @@ cudaError_t run_bwd(const Shape& s, const void* q, const void* k, const void* v,
   slot_reduce_kernel<W, GG><<<grid_for(GG * W / 8), 256, 0, st>>>(w.dq_part, block_idx, dqb, R, \
                                                                   s.N, s.H_kv, s.topk, s.nb)
     if (s.d == 128) {
-      if (s.G == 4) MSA_SLOT_REDUCE(128, 4);
-      else if (s.G == 8) MSA_SLOT_REDUCE(128, 8);
-      else MSA_SLOT_REDUCE(128, 16);
+      switch (s.G) {
+        case 1: MSA_SLOT_REDUCE(128, 1); break;
+        case 2: MSA_SLOT_REDUCE(128, 2); break;
+        case 4: MSA_SLOT_REDUCE(128, 4); break;
+        case 8: MSA_SLOT_REDUCE(128, 8); break;
+        default: MSA_SLOT_REDUCE(128, 16); break;
+      }
     } else {
-      if (s.G == 4) MSA_SLOT_REDUCE(64, 4);
-      else if (s.G == 8) MSA_SLOT_REDUCE(64, 8);
-      else MSA_SLOT_REDUCE(64, 16);
+      switch (s.G) {
+        case 1: MSA_SLOT_REDUCE(64, 1); break;
+        case 2: MSA_SLOT_REDUCE(64, 2); break;
+        case 4: MSA_SLOT_REDUCE(64, 4); break;
+        case 8: MSA_SLOT_REDUCE(64, 8); break;
+        default: MSA_SLOT_REDUCE(64, 16); break;
+      }
     }
 #undef MSA_SLOT_REDUCE
     note_launch();

@@ -9,16 +9,17 @@
 //
 // Work: one CTA owns one key block (b, g, c) at a time (static round-robin over keys
 // in block-major order, heaviest blocks first) and walks the block's inverted list in
-// chunks of 64 rows (64/G gathered queries x G heads; 16 query slots).
+// chunks of R rows (R/G gathered queries x G heads; R = 64 for G >= 4, 16 G for G = 1, 2,
+// so a chunk holds at most the 16 query slots of the z and dk_idx products).
 //   tcgen05 (one MMA thread, accumulators in TMEM, every M = 128):
-//     (1) S^T  = K Q^T          M=128 keys, N=64 rows, K=d
-//     (2) dP^T = V dO^T         M=128 keys, N=64 rows, K=d
+//     (1) S^T  = K Q^T          M=128 keys, N=R rows, K=d
+//     (2) dP^T = V dO^T         M=128 keys, N=R rows, K=d
 //     (z) z^T  = k_idx q_idx^T  M=128 keys, N=16 slots, K=d_idx   (into the dQ^T columns)
-//     (3) dV  += P^T dO         M=128 keys, N=d,  K=64 rows   (dO as MN-major B)
-//     (4) dK  += dS^T Q         M=128 keys, N=d,  K=64 rows   (Q as MN-major B)
-//     (5) dQ^T = K^T dS^T       M=d, N=64 rows, K=128 keys    (both MN-major)
+//     (3) dV  += P^T dO         M=128 keys, N=d,  K=R rows    (dO as MN-major B)
+//     (4) dK  += dS^T Q         M=128 keys, N=d,  K=R rows    (Q as MN-major B)
+//     (5) dQ^T = K^T dS^T       M=d, N=R rows, K=128 keys     (both MN-major)
 //     (6) dk_idx += dz^T q_idx  M=128 keys, N=d_idx, K=16 slots
-//   epilogue warps 0-7 (two warpgroups, each owning 32 of the 64 row columns; thread =
+//   epilogue warps 0-7 (two warpgroups, each owning R/2 of the R row columns; thread =
 //   key):
 //     E1  P^T = exp(scale S^T - lse), dS^T = P^T (dP^T - D) -> smem; the teacher p_T
 //         (group mean of P) stays in registers; with z^T from TMEM: p_I, the KL and
@@ -41,7 +42,9 @@ namespace {
 constexpr int kThreads = 352;  // 11 warps
 constexpr int kEpiWarps = 8;
 constexpr int kLoadThreads = 64;
-constexpr int kRows = 64;  // rows per chunk
+// rows per chunk: 64 (64/G queries) for G >= 4; 16 G (16 queries) for G = 1, 2, so a
+// chunk never holds more than the 16 query slots of the z and dk_idx MMAs
+__host__ __device__ constexpr int rows_per_chunk(int G) { return G >= 4 ? 64 : 16 * G; }
 constexpr int kQS = 16;    // query slots per chunk
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -61,13 +64,13 @@ struct BwdTcParams {
   int* status;
 };
 
-template <int D>
+template <int D, int R>
 struct BL {
   static constexpr int kKH = 128 * 128;             // [128][64] bf16 block
   static constexpr int kK = 0;
   static constexpr int kV = kK + (D / 64) * kKH;
   static constexpr int kKi = kV + (D / 64) * kKH;   // k_idx [128][64], zero-padded
-  static constexpr int kQH = 64 * 128;              // [64][64] bf16 block
+  static constexpr int kQH = R * 128;               // [R][64] bf16 block
   // big stage (2 slots): q and dO rows of a chunk, released by the MMAs (3)-(5)
   static constexpr int kSQ = 0;
   static constexpr int kSdO = kSQ + (D / 64) * kQH;
@@ -129,9 +132,12 @@ template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const BwdTcParams p) {
-  using L = BL<D>;
-  constexpr int QC = kRows / G;  // real queries per chunk
-  constexpr int QH = 32 / G;     // queries per warpgroup half (32 rows)
+  constexpr int R = rows_per_chunk(G);  // rows per chunk
+  constexpr int RW = R / 2;             // rows per warpgroup
+  constexpr int RB = RW < 16 ? RW : 16; // rows per TMEM load step in E1
+  using L = BL<D, R>;
+  constexpr int QC = R / G;   // real queries per chunk
+  constexpr int QH = RW / G;  // queries per warpgroup half
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -248,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nq1 = min(QC, e_end - q1);
           next_ent = (ch + 1 < nch && lane < nq1) ? __ldg(&p.entries[q1 + lane]) : -1;
         }
-        for (int x = lt; x < kRows * (D / 8); x += kLoadThreads) {
+        for (int x = lt; x < R * (D / 8); x += kLoadThreads) {
           const int r = x / (D / 8), cc = x % (D / 8);
           const int qi = r / G, h = r % G;
           const int ent = __shfl_sync(0xffffffffu, my_ent, qi);
@@ -268,8 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           cp_async_16(ss + L::kSQi + sw128(qi, cc), p.q_idx + src, ok);
         }
         {
-          const int r = lt, qi = r / G, h = r % G;  // one row per loader thread
-          const int ent = __shfl_sync(0xffffffffu, my_ent, qi);
+          const int r = lt, qi = (r / G) & 31, h = r % G;  // one row per loader thread
+          const int ent0 = __shfl_sync(0xffffffffu, my_ent, qi);
+          const int ent = r < R ? ent0 : -1;  // rows past the chunk: padding
           const bool ok = ent >= 0;
           const int ri = ok ? (ent >> kSlotBits) : -1;
           const int64_t x = ((int64_t)b * p.H_kv * G + g * G + h) * p.N + (ok ? ri : 0);
@@ -300,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t aK = smem_u32(sm + L::kK), aV = smem_u32(sm + L::kV);
       const uint32_t aPT = smem_u32(sm + L::kPT), adST = smem_u32(sm + L::kdST);
-      constexpr uint32_t i12 = idesc(128, 64, 0, 0), i34 = idesc(128, D, 0, 1);
-      constexpr uint32_t i5 = idesc(128, 64, 1, 1);
+      constexpr uint32_t i12 = idesc(128, R, 0, 0), i34 = idesc(128, D, 0, 1);
+      constexpr uint32_t i5 = idesc(128, R, 1, 1);
       constexpr uint32_t iki = idesc(128, 64, 0, 1);  // dk_idx += dz^T q_idx (K = 16 slots)
       constexpr uint32_t iz = idesc(128, 16, 0, 0);   // z^T = k_idx q_idx^T (K = d_idx)
       const uint32_t aDZ = smem_u32(sm + L::kDZ), aKi = smem_u32(sm + L::kKi);
@@ -345,9 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(b_z);
           if (!(ok = mbar_wait(b_p, u & 1, p.wait_ns, abort_flag))) break;
           tc_fence_after();
-          // (3) dV += P^T dO, (4) dK += dS^T Q     (K = 64 rows)
+          // (3) dV += P^T dO, (4) dK += dS^T Q     (K = R rows)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < R / 16; ++k) {
             const uint32_t acc = (ch > 0 || k > 0) ? 1u : 0u;
             tc_mma_bf16(tmem + cDV, desc_k(aPT + k * 32), desc_mn(adO + k * 2048, L::kQH), i34, acc);
             tc_mma_bf16(tmem + cDK, desc_k(adST + k * 32), desc_mn(aQ + k * 2048, L::kQH), i34, acc);
@@ -415,15 +422,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < QH; ++q) pt[q] = 0.f;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {  // 16 rows at a time
-            uint32_t a[16], d2[16];
-            tmem_ld_32x32b_x16(tmem + lb + cST + 32 * wg + 16 * hh, a);
-            tmem_ld_32x32b_x16(tmem + lb + cDPT + 32 * wg + 16 * hh, d2);
+          for (int hh = 0; hh < RW / RB; ++hh) {  // RB rows at a time
+            uint32_t a[RB], d2[RB];
+            if constexpr (RB == 16) {
+              tmem_ld_32x32b_x16(tmem + lb + cST + RW * wg + RB * hh, a);
+              tmem_ld_32x32b_x16(tmem + lb + cDPT + RW * wg + RB * hh, d2);
+            } else {
+              tmem_ld_32x32b_x8(tmem + lb + cST + RW * wg + RB * hh, a);
+              tmem_ld_32x32b_x8(tmem + lb + cDPT + RW * wg + RB * hh, d2);
+            }
             tmem_wait_ld();
-            uint32_t pk[8], dk2[8];  // bf16 pairs
+            uint32_t pk[RB / 2], dk2[RB / 2];  // bf16 pairs
 #pragma unroll
-            for (int x4 = 0; x4 < 16; x4 += 4) {
-              const int r0 = 32 * wg + 16 * hh + x4;
+            for (int x4 = 0; x4 < RB; x4 += 4) {
+              const int r0 = RW * wg + RB * hh + x4;
               const int4 ri4 = *reinterpret_cast<const int4*>(s_ri + r0);
               const float4 ls4 = *reinterpret_cast<const float4*>(s_lse + r0);
               const float4 dd4 = *reinterpret_cast<const float4*>(s_D + r0);
@@ -438,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     j <= ri[e] ? ex2_fast(__uint_as_float(a[x]) * p.scale_log2 - ls[e]) : 0.f;
                 pv[e] = v;
                 dv2[e] = v * (__uint_as_float(d2[x]) - dd[e]);
-                pt[(16 * hh + x) / G] += v;
+                pt[(RB * hh + x) / G] += v;
               }
               pk[x4 / 2] = pack_bf16(pv[0], pv[1]);
               pk[x4 / 2 + 1] = pack_bf16(pv[2], pv[3]);
@@ -446,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               dk2[x4 / 2 + 1] = pack_bf16(dv2[2], dv2[3]);
             }
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const uint32_t o = sw128(tl, 4 * wg + 2 * hh + cc);
+            for (int cc = 0; cc < RB / 8; ++cc) {
+              const uint32_t o = sw128(tl, (RW * wg + RB * hh) / 8 + cc);
               *reinterpret_cast<uint4*>(sm + L::kPT + o) =
                   make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
               *reinterpret_cast<uint4*>(sm + L::kdST + o) =
@@ -499,9 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&e_wg[wg]);
         ok = __all_sync(0xffffffffu, mbar_wait(&e_wg[wg], u & 1, p.wait_ns, abort_flag));
         if (!ok) break;
-        // this warpgroup's slots are n8 tile nt of dz (G = 4); with G = 8 or 16 both
-        // warpgroups share tile 0 and each keeps its own QH slots
-        constexpr int NT = (G == 4) ? 1 : 0;
+        // this warpgroup's slots are n8 tile nt of dz (8 slots each, G <= 4); with G = 8
+        // or 16 both warpgroups share tile 0 and each keeps its own QH slots
+        constexpr int NT = (QH == 8) ? 1 : 0;
         const int nt = NT ? wg : 0;
         if (16 * q4 < p.DI) {
           // dq_idx^T (16 d x 8 slots of this warpgroup) = k_idx^T dz^T   (k = 128 keys)
@@ -533,15 +545,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         if (tl < D) {  // warp-uniform
-          uint32_t a[32];
-          tmem_ld_32x32b_x32(tmem + lb + cDQT + 32 * wg, a);
+          uint32_t a[RW];
+          if constexpr (RW == 32) {
+            tmem_ld_32x32b_x32(tmem + lb + cDQT + RW * wg, a);
+          } else if constexpr (RW == 16) {
+            tmem_ld_32x32b_x16(tmem + lb + cDQT + RW * wg, a);
+          } else {
+            tmem_ld_32x32b_x8(tmem + lb + cDQT + RW * wg, a);
+          }
           tmem_wait_ld();
-          // stage this warp's [32 rows][32 d] block so the global stores below write
+          // stage this warp's [RW rows][32 d] block so the global stores below write
           // 64-byte row segments; lanes (2m, 2m+1) swap one value so each stores a pair
           uint8_t* stg = sm + L::kStg + warp * (32 * 64);
           const bool odd = lane & 1;
 #pragma unroll
-          for (int x = 0; x < 32; x += 2) {
+          for (int x = 0; x < RW; x += 2) {
             const float v0 = __uint_as_float(a[x]) * p.scale;
             const float v1 = __uint_as_float(a[x + 1]) * p.scale;
             const float mine = odd ? v1 : v0;
@@ -552,10 +570,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < RW / 8; ++i) {
             const int k = lane + 32 * i;
             const int r = k >> 2, cc = k & 3;
-            const int rp = s_rp[32 * wg + r];
+            const int rp = s_rp[RW * wg + r];
             const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 64 + cc * 16);
             if (rp >= 0) *reinterpret_cast<uint4*>(p.dq_part + (int64_t)rp * D + 32 * q4 + cc * 8) = v;
           }
@@ -653,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int G>
 cudaError_t launch_dg(const BwdTcParams& prm, const CUtensorMap& tk, const CUtensorMap& tv,
                       const Ctx& cx, cudaStream_t st) {
-  using L = BL<D>;
+  using L = BL<D, rows_per_chunk(G)>;
   auto kern = bwd_tc_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
@@ -712,12 +730,17 @@ cudaError_t launch_attn_bwd_tc(const Shape& s, const void* q, const void* k, con
   p.w = kl_weight;
   p.wait_ns = cx.wait_ns;
   p.status = cx.status;
-  if (s.d == 128) {
-    if (s.G == 4) return launch_dg<128, 4>(p, tk, tv, cx, st);
-    return s.G == 8 ? launch_dg<128, 8>(p, tk, tv, cx, st) : launch_dg<128, 16>(p, tk, tv, cx, st);
+#define MSA_BWD_G(DD)                                                  \
+  switch (s.G) {                                                       \
+    case 1: return launch_dg<DD, 1>(p, tk, tv, cx, st);                \
+    case 2: return launch_dg<DD, 2>(p, tk, tv, cx, st);                \
+    case 4: return launch_dg<DD, 4>(p, tk, tv, cx, st);                \
+    case 8: return launch_dg<DD, 8>(p, tk, tv, cx, st);                \
+    default: return launch_dg<DD, 16>(p, tk, tv, cx, st);              \
   }
-  if (s.G == 4) return launch_dg<64, 4>(p, tk, tv, cx, st);
-  return s.G == 8 ? launch_dg<64, 8>(p, tk, tv, cx, st) : launch_dg<64, 16>(p, tk, tv, cx, st);
+  if (s.d == 128) MSA_BWD_G(128)
+  MSA_BWD_G(64)
+#undef MSA_BWD_G
 }
 
 }  // namespace msa

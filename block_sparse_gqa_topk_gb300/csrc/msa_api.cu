@@ -259,8 +259,6 @@ int msa_bwd(const msa_problem_t* p, const void* q, const void* k, const void* v,
                        dq, dk, dv, dq_idx, dk_idx};
   for (const void* x : ins)
     if (!x || !aligned16(x)) return MSA_ERR_ARG;
-  // the fused backward's 64-row chunks hold 64 / G queries in 16 query slots
-  if (s.G != 4 && s.G != 8 && s.G != 16) return MSA_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < bwd_ws_bytes(s)) return MSA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MSA_ERR_ARG;
   Ctx cx;

@@ -132,8 +132,6 @@ int msa_fwd(const msa_problem_t* p, const void* q, const void* k, const void* v,
  * In:  q, k, v, o, dO, q_idx, k_idx (bf16), lse, lse_idx (float32), block_idx.
  * Out: dq, dk, dv, dq_idx, dk_idx (bf16, overwritten); kl_out (one float32 on the
  *      device, overwritten with the KL value; may be NULL).
- * Supported group sizes: G = H_q / H_kv in {4, 8, 16} (the fused kernel's 64-row chunks
- * hold 64 / G queries in 16 query slots); other G return MSA_ERR_UNSUPPORTED.
  */
 int msa_bwd(const msa_problem_t* p, const void* q, const void* k, const void* v, const void* o,
             const float* lse, const void* dO, const void* q_idx, const void* k_idx,

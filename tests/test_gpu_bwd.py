@@ -20,8 +20,8 @@ from test_gpu_index_fwd import EDGE, cfg_of
 
 pytestmark = pytest.mark.gpu
 
-FULL = ["tiny", "ragged", "one_block", "k1", "k3", "dense", "odd_groups", "g8", "g16", "g16_d128",
-        "k8_d128", "8k"]
+FULL = ["tiny", "ragged", "one_block", "k1", "k3", "dense", "odd_groups", "g1", "g2", "g2_d128",
+        "g8", "g16", "g16_d128", "k8_d128", "8k"]
 SAMPLED = [("32k", 512), ("128k", 256), ("1m", 128)]
 
 

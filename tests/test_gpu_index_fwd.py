@@ -25,6 +25,8 @@ EDGE = {
     "g8": T.with_(H_q=16, H_kv=2, seed=38),
     "g16": T.with_(H_q=32, H_kv=2, N=1024, seed=39),
     "g16_d128": T.with_(d=128, d_idx=64, H_q=32, H_kv=2, N=2048, seed=42),
+    "g2": T.with_(H_q=4, H_kv=2, seed=43),
+    "g2_d128": T.with_(d=128, d_idx=64, H_q=8, H_kv=4, N=2048, seed=44),
     "k8_d128": T.with_(d=128, d_idx=64, topk=8, N=4096, H_q=8, H_kv=2, seed=40, n_needle=2,
                        needle_seed=41),
 }
