@@ -26,32 +26,47 @@
 namespace msa {
 namespace {
 
-// D[b,h,i] = dO[b,i,h,:] . o[b,i,h,:]; one warp per (b, i, h).
+// D[b,h,i] = dO[b,i,h,:] . o[b,i,h,:].  One CTA per 64 consecutive queries i of one
+// (b, h): TPR = D / 8 threads per row (16-byte loads), every pass's loads issued before
+// the sums, and D written along i.
 template <int D>
-__global__ void bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
-                               const __nv_bfloat16* __restrict__ dO, float* __restrict__ Dv,
-                               int64_t rows, int N, int H_q) {
-  const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= rows) return;  // rows = B*N*H_q, w = (b*N + i)*H_q + h
-  constexpr int E = D / 32;
-  const __nv_bfloat16* a = o + w * D + lane * E;
-  const __nv_bfloat16* bb = dO + w * D + lane * E;
-  float s = 0.f;
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                      const __nv_bfloat16* __restrict__ dO,
+                                                      float* __restrict__ Dv, int N, int H_q) {
+  constexpr int TPR = D / 8;      // threads per row
+  constexpr int RPP = 256 / TPR;  // rows per pass
+  constexpr int NP = 64 / RPP;    // passes
+  const int chunks = (N + 63) / 64;
+  const int64_t bh = blockIdx.x / chunks;  // b * H_q + h
+  const int i0 = (int)(blockIdx.x % chunks) * 64;
+  const int h = (int)(bh % H_q);
+  const int64_t b = bh / H_q;
+  const int t = threadIdx.x % TPR, rr = threadIdx.x / TPR;
+  uint4 xa[NP], xb[NP];
 #pragma unroll
-  for (int e = 0; e < E; e += 2) {
-    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(a + e);
-    const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(bb + e);
-    s += __low2float(x) * __low2float(y) + __high2float(x) * __high2float(y);
+  for (int q = 0; q < NP; ++q) {
+    const int i = i0 + q * RPP + rr;
+    if (i < N) {
+      const int64_t off = ((b * N + i) * H_q + h) * D + t * 8;
+      xa[q] = __ldg(reinterpret_cast<const uint4*>(o + off));
+      xb[q] = __ldg(reinterpret_cast<const uint4*>(dO + off));
+    } else {
+      xa[q] = make_uint4(0u, 0u, 0u, 0u);
+      xb[q] = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) {
-    const int h = (int)(w % H_q);
-    const int64_t bi = w / H_q;
-    const int i = (int)(bi % N);
-    const int64_t b = bi / N;
-    Dv[(b * H_q + h) * N + i] = s;
+  for (int q = 0; q < NP; ++q) {
+    const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&xa[q]);
+    const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&xb[q]);
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      s += __low2float(x[e]) * __low2float(y[e]) + __high2float(x[e]) * __high2float(y[e]);
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    const int i = i0 + q * RPP + rr;
+    if (t == 0 && i < N) Dv[bh * N + i] = s;
   }
 }
 
@@ -169,16 +184,17 @@ cudaError_t run_bwd(const Shape& s, const void* q, const void* k, const void* v,
   if (e != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(w.counter, 0, 256, st)) != cudaSuccess) return e;  // counter + KL
   {
-    const int64_t rows = (int64_t)s.B * s.N * s.H_q;
-    const unsigned grid = (unsigned)((rows * 32 + 255) / 256);
+    const int64_t blocks = (int64_t)s.B * s.H_q * ((s.N + 63) / 64);
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)blocks;
     if (s.d == 128)
       bwd_pre_kernel<128><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
-                                                static_cast<const __nv_bfloat16*>(dO), w.Dv, rows,
-                                                s.N, s.H_q);
+                                                static_cast<const __nv_bfloat16*>(dO), w.Dv, s.N,
+                                                s.H_q);
     else
       bwd_pre_kernel<64><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
-                                               static_cast<const __nv_bfloat16*>(dO), w.Dv, rows,
-                                               s.N, s.H_q);
+                                               static_cast<const __nv_bfloat16*>(dO), w.Dv, s.N,
+                                               s.H_q);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
