@@ -216,130 +216,138 @@ __global__ void __launch_bounds__(256) decode_select_kernel(const DecodeParams p
   for (int s = M + 1 + t; s < p.topk; s += blockDim.x) dst[s] = -1;
 }
 
-// Softmax partial of every head of group g over block c (slot `part`): K and V rows
-// staged in shared memory (cp.async, rows past the cache end zero-filled; V in its own
-// copy group, still landing while the scores run); both products are mma.sync
-// m16n8k16 contractions with the group's heads as the 8-wide n dimension:
+// Softmax partial of every head of group g over block c (slot `part`); writes lse_part
+// and the normalised o_part of the slot.  Both products are mma.sync m16n8k16
+// contractions with the group's heads as the 8-wide n dimension:
 //   S^T[key][h] = K[key][:] . q_h              (warp w: keys 16w..16w+15)
 //   O^T[dd][h]  = sum_key V[key][dd] P[h][key] (warp w: dd = 16w..16w+15)
-// The scores go through shared memory for the per-head softmax; P is rounded to bf16
-// for the second product, its row sum l stays fp32.  Writes lse_part and the
-// normalised o_part of the slot.
+// K is read straight from global memory into A fragments: each lane loads 16 contiguous
+// bytes of a key row (8 for an FP8 row) per 32-wide d chunk, and the fragment slots of
+// the chunk's two k steps take them in a fixed order that the query fragments repeat,
+// so every product pairs matching d.  V rows are staged in shared memory (cp.async, or
+// 16-byte loads widened from E4M3) for ldmatrix.trans.  Rows past the visible end of
+// the block are zero.  The scores go through shared memory for the per-head softmax; P
+// is rounded to bf16 for the second product (with an FP8 cache the V row scale is
+// folded into it), its row sum l stays fp32.
 template <int D, int NT, bool F8>
 __device__ __forceinline__ void block_partial(const DecodeParams& p, uint8_t* dsm, int64_t part,
-                                              int c, int b, int g, float* s_l, float* s_sk,
-                                              float* s_sv) {
-  constexpr int KS = D + 8;    // padded K/V row (bf16): conflict-free ldmatrix phases
+                                              int c, int b, int g, float* s_l, float* s_sv) {
+  constexpr int KS = D + 8;    // padded V row (bf16): conflict-free ldmatrix phases
   constexpr int PS = 128 + 8;  // padded P row (bf16)
-  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(dsm);
-  __nv_bfloat16* sV = sK + 128 * KS;
-  // after the scores, the K region holds S [8 NT][128] fp32 and P [8 NT][PS] bf16
-  float* sS = reinterpret_cast<float*>(dsm);
-  __nv_bfloat16* sP = reinterpret_cast<__nv_bfloat16*>(sS + 8 * NT * 128);
+  constexpr int NP = D / 32;   // 32-wide d chunks (two k steps each)
+  __nv_bfloat16* sV = reinterpret_cast<__nv_bfloat16*>(dsm);
+  float* sS = reinterpret_cast<float*>(dsm + 128 * KS * 2);        // [8 NT][128]
+  __nv_bfloat16* sP = reinterpret_cast<__nv_bfloat16*>(sS + 8 * NT * 128);  // [8 NT][PS]
   const int G = p.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const int L = seq_len(p, b, p.status);
   const int jmax = min(L - 1, c * 128 + 127) - c * 128;  // last visible row of the block
-  if constexpr (F8) {
-    // E4M3 rows: 16 codes per 16-byte load, widened exactly to bf16 in shared memory
-    // (every E4M3 value is a bf16 value); rows past the visible end are zero with
-    // scale 0.  The row scales go to s_sk, s_sv.
-    constexpr int CH = D / 16;                // 16-byte chunks per row
-    constexpr int PER = 128 * CH / 256;       // chunks per thread (256 threads)
-    uint4 kw[PER], vw[PER];
+  const int64_t row0 = ((int64_t)b * p.Lmax + c * 128) * p.H_kv + g;  // (b, c 128, g)
+  // ---- V rows into shared memory ----
+  constexpr int CH = F8 ? D / 16 : D / 8;  // 16-byte chunks per V row
+  constexpr int PER = 128 * CH / 256;      // chunks per thread
+  uint4 vw[F8 ? PER : 1];
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {           // every load in flight before any use
-      const int x = threadIdx.x + u * 256;
-      const int r = x / CH, ch = x % CH;
-      const bool ok = r <= jmax;              // row c 128 + r < L <= Lmax
-      const int64_t off = (((int64_t)b * p.Lmax + c * 128 + r) * p.H_kv + g) * D + ch * 16;
-      kw[u] = ok ? __ldg(reinterpret_cast<const uint4*>(p.k8 + off)) : make_uint4(0, 0, 0, 0);
-      vw[u] = ok ? __ldg(reinterpret_cast<const uint4*>(p.v8 + off)) : make_uint4(0, 0, 0, 0);
+  for (int u = 0; u < PER; ++u) {
+    const int x = threadIdx.x + u * 256;
+    const int r = x / CH, ch = x % CH;
+    const bool ok = r <= jmax;  // row c 128 + r < L <= Lmax
+    const int64_t row = row0 + (int64_t)r * p.H_kv;
+    if constexpr (F8) {
+      vw[u] = ok ? __ldg(reinterpret_cast<const uint4*>(p.v8 + row * D + ch * 16))
+                 : make_uint4(0, 0, 0, 0);
+    } else {
+      cp_async_16(sV + r * KS + ch * 8, p.v + (ok ? row * D + ch * 8 : 0), ok);
     }
+  }
+  if constexpr (!F8) cp_async_commit();
+  // ---- K fragments (rows 16 warp + gq and + 8) and the query fragments ----
+  const int ka = warp * 16 + gq, kb = ka + 8;
+  uint4 wa[NP], wb[NP];
+#pragma unroll
+  for (int j = 0; j < NP; ++j) {
+    if constexpr (F8) {
+      const uint2 ca = ka <= jmax ? __ldg(reinterpret_cast<const uint2*>(p.k8 + (row0 + (int64_t)ka * p.H_kv) * D + 32 * j + 8 * tq))
+                                  : make_uint2(0, 0);
+      const uint2 cb = kb <= jmax ? __ldg(reinterpret_cast<const uint2*>(p.k8 + (row0 + (int64_t)kb * p.H_kv) * D + 32 * j + 8 * tq))
+                                  : make_uint2(0, 0);
+      uint32_t ta[4], tb[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {  // fp8 pairs (2e, 2e+1) -> bf16 pairs
+        const __nv_fp8x2_storage_t a2 = (__nv_fp8x2_storage_t)((e < 2 ? ca.x : ca.y) >> (16 * (e & 1)));
+        const __nv_fp8x2_storage_t b2 = (__nv_fp8x2_storage_t)((e < 2 ? cb.x : cb.y) >> (16 * (e & 1)));
+        const float2 fa = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(a2, __NV_E4M3)));
+        const float2 fb = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(b2, __NV_E4M3)));
+        ta[e] = pack_bf16(fa.x, fa.y);
+        tb[e] = pack_bf16(fb.x, fb.y);
+      }
+      wa[j] = make_uint4(ta[0], ta[1], ta[2], ta[3]);
+      wb[j] = make_uint4(tb[0], tb[1], tb[2], tb[3]);
+    } else {
+      wa[j] = ka <= jmax ? __ldg(reinterpret_cast<const uint4*>(p.k + (row0 + (int64_t)ka * p.H_kv) * D) + 4 * j + tq)
+                         : make_uint4(0, 0, 0, 0);
+      wb[j] = kb <= jmax ? __ldg(reinterpret_cast<const uint4*>(p.k + (row0 + (int64_t)kb * p.H_kv) * D) + 4 * j + tq)
+                         : make_uint4(0, 0, 0, 0);
+    }
+  }
+  float ska = 1.f, skb = 1.f;  // K row scales (FP8)
+  if constexpr (F8) {
+    ska = ka <= jmax ? __ldg(&p.k_scale[row0 + (int64_t)ka * p.H_kv]) : 0.f;
+    skb = kb <= jmax ? __ldg(&p.k_scale[row0 + (int64_t)kb * p.H_kv]) : 0.f;
+  }
+  // query fragments: head nt 8 + gq, d = 32 j + 8 tq + 0..7 (zero for heads >= G)
+  uint4 bq[NT][NP];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = nt * 8 + gq;
+    const uint4* qrow =
+        reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.H_kv * G + (int64_t)g * G + h) * D);
+#pragma unroll
+    for (int j = 0; j < NP; ++j) bq[nt][j] = h < G ? __ldg(&qrow[4 * j + tq]) : make_uint4(0, 0, 0, 0);
+  }
+  if constexpr (F8) {  // widen the staged V rows and keep their scales
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
       const int x = threadIdx.x + u * 256;
       const int r = x / CH, ch = x % CH;
-      const uint32_t kk[4] = {kw[u].x, kw[u].y, kw[u].z, kw[u].w};
       const uint32_t vv[4] = {vw[u].x, vw[u].y, vw[u].z, vw[u].w};
-      uint32_t ko[8], vo[8];
+      uint32_t vo[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const __nv_fp8x2_storage_t k2 = (__nv_fp8x2_storage_t)(kk[e >> 1] >> (16 * (e & 1)));
         const __nv_fp8x2_storage_t v2 = (__nv_fp8x2_storage_t)(vv[e >> 1] >> (16 * (e & 1)));
-        const float2 kf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(k2, __NV_E4M3)));
         const float2 vf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(v2, __NV_E4M3)));
-        ko[e] = pack_bf16(kf.x, kf.y);
         vo[e] = pack_bf16(vf.x, vf.y);
       }
-      uint4* kd = reinterpret_cast<uint4*>(sK + r * KS + ch * 16);
       uint4* vd = reinterpret_cast<uint4*>(sV + r * KS + ch * 16);
-      kd[0] = make_uint4(ko[0], ko[1], ko[2], ko[3]);
-      kd[1] = make_uint4(ko[4], ko[5], ko[6], ko[7]);
       vd[0] = make_uint4(vo[0], vo[1], vo[2], vo[3]);
       vd[1] = make_uint4(vo[4], vo[5], vo[6], vo[7]);
     }
-    for (int r = threadIdx.x; r < 128; r += blockDim.x) {
-      const bool ok = r <= jmax;
-      const int64_t row = ((int64_t)b * p.Lmax + c * 128 + r) * p.H_kv + g;
-      s_sk[r] = ok ? __ldg(&p.k_scale[row]) : 0.f;
-      s_sv[r] = ok ? __ldg(&p.v_scale[row]) : 0.f;
-    }
-  } else {
-    for (int x = threadIdx.x; x < 128 * (D / 8); x += blockDim.x) {
-      const int r = x / (D / 8), ch = x % (D / 8);
-      const bool ok = r <= jmax;  // row c 128 + r < L <= Lmax
-      const int64_t off = ok ? (((int64_t)b * p.Lmax + c * 128 + r) * p.H_kv + g) * D + ch * 8 : 0;
-      cp_async_16(sK + r * KS + ch * 8, p.k + off, ok);
-    }
-    cp_async_commit();
-    for (int x = threadIdx.x; x < 128 * (D / 8); x += blockDim.x) {
-      const int r = x / (D / 8), ch = x % (D / 8);
-      const bool ok = r <= jmax;
-      const int64_t off = ok ? (((int64_t)b * p.Lmax + c * 128 + r) * p.H_kv + g) * D + ch * 8 : 0;
-      cp_async_16(sV + r * KS + ch * 8, p.v + off, ok);
-    }
-    cp_async_commit();
+    for (int r = threadIdx.x; r < 128; r += blockDim.x)
+      s_sv[r] = r <= jmax ? __ldg(&p.v_scale[row0 + (int64_t)r * p.H_kv]) : 0.f;
   }
-  // B fragments of the scores: B[k = dd][n = h] = q[b][g G + h][dd], zero for h >= G
-  uint32_t bq[NT][D / 16][2];
+  // ---- scores ----
+  float sc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int h = nt * 8 + gq;
-    const uint32_t* qrow =
-        reinterpret_cast<const uint32_t*>(p.q + ((int64_t)b * p.H_kv * G + (int64_t)g * G + h) * D);
+    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      bq[nt][ks][0] = h < G ? __ldg(&qrow[ks * 8 + tq]) : 0u;
-      bq[nt][ks][1] = h < G ? __ldg(&qrow[ks * 8 + 4 + tq]) : 0u;
+    for (int j = 0; j < NP; ++j) {
+      const uint32_t a0[4] = {wa[j].x, wb[j].x, wa[j].y, wb[j].y};
+      const uint32_t a1[4] = {wa[j].z, wb[j].z, wa[j].w, wb[j].w};
+      mma_bf16_16816(sc[nt], a0, bq[nt][j].x, bq[nt][j].y);
+      mma_bf16_16816(sc[nt], a1, bq[nt][j].z, bq[nt][j].w);
     }
   }
-  if constexpr (!F8) cp_async_wait<1>();  // K landed
-  __syncthreads();
-  float sc[NT][4];
-  {
-    const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix, row
-    const __nv_bfloat16* arow = sK + (warp * 16 + (mi & 1) * 8 + ri) * KS + (mi >> 1) * 8;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t a[4];
-      ldmatrix_x4(a, arow + ks * 16);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], a, bq[nt][ks][0], bq[nt][ks][1]);
-    }
-  }
-  __syncthreads();  // K no longer read: its region takes S and P
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int h = nt * 8 + 2 * tq + (e & 1), r = warp * 16 + gq + (e >> 1) * 8;
-      const float raw = F8 ? sc[nt][e] * s_sk[r] : sc[nt][e];  // K row scale
+      const int h = nt * 8 + 2 * tq + (e & 1), r = (e >> 1) ? kb : ka;
+      const float raw = F8 ? sc[nt][e] * ((e >> 1) ? skb : ska) : sc[nt][e];
       sS[h * 128 + r] = r <= jmax ? raw * p.scale : -INFINITY;
     }
+  if constexpr (!F8) cp_async_wait<0>();  // V landed
   __syncthreads();
   // per head: max, exp, sum (one warp per head); padding heads get P = 0
   for (int h = warp; h < 8 * NT; h += 8) {
@@ -370,7 +378,6 @@ __device__ __forceinline__ void block_partial(const DecodeParams& p, uint8_t* ds
       p.lse_part[part + h] = m + logf(l);
     }
   }
-  if constexpr (!F8) cp_async_wait<0>();  // V landed
   __syncthreads();
   if (warp < D / 16) {
     float acc[NT][4];
@@ -446,7 +453,7 @@ template <int D, int NT, bool F8>
 __global__ void __launch_bounds__(256) decode_attn_kernel(const DecodeParams p) {
   extern __shared__ __align__(16) uint8_t dsm[];
   __shared__ float s_l[8 * NT];
-  __shared__ float s_sk[F8 ? 128 : 1], s_sv[F8 ? 128 : 1];  // FP8 row scales
+  __shared__ float s_sv[F8 ? 128 : 1];  // FP8 V row scales
   __shared__ float s_w[32 * 16];  // [topk][G] merge weights
   __shared__ int s_last;
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -455,7 +462,7 @@ __global__ void __launch_bounds__(256) decode_attn_kernel(const DecodeParams p) 
   if (c < 0) {
     for (int h = threadIdx.x; h < p.G; h += blockDim.x) p.lse_part[part + h] = -INFINITY;
   } else {
-    block_partial<D, NT, F8>(p, dsm, part, c, b, g, s_l, s_sk, s_sv);
+    block_partial<D, NT, F8>(p, dsm, part, c, b, g, s_l, s_sv);
   }
   __threadfence();  // this CTA's partial is visible before its arrival
   __syncthreads();
@@ -603,7 +610,9 @@ int run_decode(const msa_problem_t* p, const void* q, const void* q_idx, const D
   if (s.topk - 1 <= 15) decode_select_kernel<15><<<gsel, 256, 0, stream>>>(dp);
   else decode_select_kernel<31><<<gsel, 256, 0, stream>>>(dp);
   note_launch();
-  const size_t attn_smem = (size_t)2 * 128 * (s.d + 8) * 2;
+  const int attn_nt = s.G <= 8 ? 1 : 2;
+  const size_t attn_smem = (size_t)128 * (s.d + 8) * 2 + (size_t)8 * attn_nt * 128 * 4 +
+                           (size_t)8 * attn_nt * (128 + 8) * 2;
   const dim3 gattn((unsigned)s.topk, (unsigned)s.H_kv, (unsigned)s.B);
   cudaError_t e = cudaSuccess;
 #define MSA_ATTN(D, NT, F8)                                                                   \
