@@ -12,10 +12,10 @@
 namespace msa {
 
 // Slots per (b, g, i) row: up to kMaxSlots block ids.  Inverted-list entries pack
-// (query << kSlotBits) | slot into a non-negative int (query < 2^24).  The block
+// (query << kSlotBits) | slot into a non-negative int (query < 2^23).  The block
 // selection kernel keeps its candidates in registers and picks at most kMaxSelect
 // blocks; more slots are used only by the dense set (every visible block, topk >= nb).
-constexpr int kSlotBits = 7;
+constexpr int kSlotBits = 8;
 constexpr int kSlotMask = (1 << kSlotBits) - 1;
 constexpr int kMaxSlots = 1 << kSlotBits;
 constexpr int kMaxSelect = 32;

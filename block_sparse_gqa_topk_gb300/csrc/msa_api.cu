@@ -73,7 +73,7 @@ int check_problem(const msa_problem_t* p, Shape* s) {
   if (p->d_idx != 32 && p->d_idx != 64) return MSA_ERR_UNSUPPORTED;
   if (p->topk > kMaxSlots) return MSA_ERR_UNSUPPORTED;
   if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return MSA_ERR_UNSUPPORTED;
-  if (p->N > (1 << 24)) return MSA_ERR_UNSUPPORTED;
+  if (p->N > (1 << 23)) return MSA_ERR_UNSUPPORTED;  // (query << 8) | slot stays an int
   s->B = p->B;
   s->N = p->N;
   s->H_q = p->H_q;

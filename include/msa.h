@@ -32,8 +32,8 @@
  *    recorded in a per-device status word, read with msa_get_device_status().
  *  - No exception, trap or abort crosses this boundary.
  *  - Supported (this build): causal = 1, Bk = 128, d in {64, 128},
- *    d_idx in {32, 64}, 1 <= topk <= 128, H_q % H_kv == 0 with G = H_q / H_kv in
- *    {1, 2, 4, 8, 16}, N <= 2^24.  N need not be a multiple of Bk.  Block selection
+ *    d_idx in {32, 64}, 1 <= topk <= 256, H_q % H_kv == 0 with G = H_q / H_kv in
+ *    {1, 2, 4, 8, 16}, N <= 2^23.  N need not be a multiple of Bk.  Block selection
  *    (msa_index_topk, msa_decode) picks at most 32 blocks; topk > 32 is accepted by
  *    msa_index_topk only when topk >= nb = ceil(N / Bk) (the dense set below), and by
  *    msa_fwd / msa_bwd for any valid caller-given set.

@@ -53,7 +53,8 @@ def test_status_strings_and_version():
     (dict(Bk=64), _lib.MSA_ERR_UNSUPPORTED),
     (dict(d=96), _lib.MSA_ERR_UNSUPPORTED),
     (dict(d_idx=16), _lib.MSA_ERR_UNSUPPORTED),
-    (dict(topk=129), _lib.MSA_ERR_UNSUPPORTED),
+    (dict(topk=257), _lib.MSA_ERR_UNSUPPORTED),
+    (dict(N=(1 << 23) + 1), _lib.MSA_ERR_UNSUPPORTED),
     (dict(causal=0), _lib.MSA_ERR_UNSUPPORTED),
     (dict(scale=0.0), _lib.MSA_ERR_ARG),
     (dict(scale=float("nan")), _lib.MSA_ERR_ARG),

@@ -6,7 +6,7 @@ topk >= the number of blocks, so every visible block is selected, the main branc
 full causal attention, and the KL runs over every visible token.  The GPU path is run
 end to end through the C ABI (its own set, lse_idx, o and lse feed its backward);
 the oracle computes everything from the inputs.  The set is fixed by the rule and is
-compared exactly; the cases use more than 32 slots per row (up to 128).
+compared exactly; the cases use more than 32 slots per row (up to 256).
 """
 import numpy as np
 import pytest
@@ -77,3 +77,45 @@ def test_selection_above_32_below_nb_is_refused():
     _, d = device_inputs(cfg, names=("q_idx", "k_idx"))
     with pytest.raises(_lib.MSAError):
         ops.msa_index_topk(d["q_idx"], d["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d)
+
+
+def test_warmup_dense_32k_256_slots_sampled():
+    """256 slots (every block of a 32K-token sequence): the index LSE, o, lse and the
+    per-row gradients dq, dq_idx on sampled rows; dk and dv of the sampled rows alone
+    from a second backward with dO zero elsewhere and no KL (the oracle's row-subset
+    backward computes exactly that)."""
+    import torch
+    from gpu_inputs import rows_for
+    from parity import LSE_TOL
+    cfg = E.with_(name="warm-32k", B=1, N=32768, H_q=8, H_kv=2, topk=256, n_needle=2, seed=74)
+    assert cfg.topk >= cfg.nb
+    h, d = device_inputs(cfg)
+    rows, _ = rows_for(cfg, 192)
+    w = cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N)
+    bi, li = ops.msa_index_topk(d["q_idx"], d["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d)
+    o, lse = ops.msa_fwd(d["q"], d["k"], d["v"], bi, scale=cfg.scale, d_idx=cfg.d_idx)
+    g = ops.msa_bwd(d["q"], d["k"], d["v"], o, lse, d["dO"], d["q_idx"], d["k_idx"], bi, li, w,
+                    scale=cfg.scale)
+    assert ops.device_status() == 0
+    b, i = rows // cfg.N, rows % cfg.N
+    assert np.array_equal(bi.cpu().numpy(), _dense(cfg))
+    bi_ref, _, _ = oracle.select(cfg, h, rows=rows)
+    assert np.array_equal(bi.cpu().numpy()[b, :, i], bi_ref)
+    o_ref, lse_ref, li_ref = oracle.forward(cfg, h, bi_ref, rows=rows)
+    assert np.abs(li.cpu().numpy()[b, :, i] - li_ref).max() <= LSE_TOL
+    assert np.abs(f64(o)[b, i] - o_ref).max() <= O_TOL
+    assert np.abs(lse.cpu().numpy()[b, :, i] - lse_ref).max() <= LSE_TOL
+    ref = oracle.backward(cfg, h, bi_ref, w, rows=rows)
+    grad_close(f64(g["dq"])[b, i], ref["dq"], "dq")
+    grad_close(f64(g["dq_idx"])[b, i], ref["dq_idx"], "dq_idx")
+    del g
+    keep = torch.zeros(cfg.B * cfg.N, dtype=torch.bool, device="cuda")
+    keep[torch.from_numpy(rows).cuda()] = True
+    dO_m = d["dO"].clone().view(cfg.B * cfg.N, -1)
+    dO_m[~keep] = 0
+    g2 = ops.msa_bwd(d["q"], d["k"], d["v"], o, lse, dO_m.view_as(d["dO"]), d["q_idx"], d["k_idx"],
+                     bi, li, 0.0, scale=cfg.scale)
+    assert ops.device_status() == 0
+    ref0 = oracle.backward(cfg, h, bi_ref, 0.0, rows=rows)
+    grad_close(f64(g2["dk"]), ref0["dk"], "dk")
+    grad_close(f64(g2["dv"]), ref0["dv"], "dv")
