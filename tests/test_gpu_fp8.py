@@ -24,6 +24,9 @@ CASES = {
     "ragged": (T.with_(name="f8-ragged", B=2, N=2000, seed=92), [2000, 129]),
     "g16": (T.with_(name="f8-g16", H_q=32, H_kv=2, N=1024, B=2, seed=93), [1024, 700]),
     "8k": (synth.CONFIGS["8k"], [8192, 5001]),
+    # 24 groups (two group tiles of the pooling), G = 2, d = 64 with d_idx = 64, k = 20
+    "wide": (T.with_(name="f8-wide", H_q=48, H_kv=24, d_idx=64, topk=20, N=3000, B=2,
+                     seed=94), [3000, 2561]),
 }
 
 

@@ -17,6 +17,9 @@ pytestmark = pytest.mark.gpu
 
 CFG = synth.CONFIGS["tiny"].with_(name="varlen", seed=51)  # packed T = 2048 tokens
 CU = [0, 1024, 1024, 1796, 2048]                            # lengths 1024, 0, 772, 252
+# G = 8, d = 128, d_idx = 64, k = 16: packed T = 4096 tokens, lengths 2560, 4, 1532
+CFG8 = synth.CONFIGS["8k"].with_(name="varlen-g8", B=1, N=4096, H_q=16, H_kv=2, seed=52)
+CU8 = [0, 2560, 2564, 4096]
 
 
 def _seq(h, c0, c1):
@@ -24,8 +27,8 @@ def _seq(h, c0, c1):
     return {n: np.ascontiguousarray(h[n][:, c0:c1]) for n in h}
 
 
-def test_varlen_matches_oracle_per_sequence():
-    cfg = CFG
+@pytest.mark.parametrize("cfg,CU", [(CFG, CU), (CFG8, CU8)], ids=["tiny", "g8_d128"])
+def test_varlen_matches_oracle_per_sequence(cfg, CU):
     h = host_inputs(cfg)
     d = {n: to_dev(h[n])[0].contiguous() for n in ("q", "k", "v", "q_idx", "k_idx", "dO")}
     H_kv, k = cfg.H_kv, cfg.topk
