@@ -107,6 +107,22 @@ def test_decode_and_fp8_entry_points_reject_bad_arguments_on_the_host():
     assert _lib.msa_quantize_kv_fp8(_prob(H_kv=0, H_q=0), 16, 16, 16, None) == _lib.MSA_ERR_SHAPE
 
 
+def test_varlen_offsets_are_validated_on_the_host():
+    p = _prob()
+    for bad in ([4, 8, 16], [0, 8, 4], [0, 6, 16]):  # start != 0, decreasing, start % 4
+        assert _lib.msa_workspace_size_varlen(p, bad, _lib.MSA_WS_FWD) == 0
+        assert _lib.msa_index_topk_varlen(p, bad, 16, 16, 16, None, None, 0, None) == _lib.MSA_ERR_ARG
+        assert _lib.msa_fwd_varlen(p, bad, 16, 16, 16, 16, 16, 16, 256, 1 << 30, None) == \
+            _lib.MSA_ERR_ARG
+    # a valid batch needs the largest sequence's workspace (the calls reuse one)
+    cu = [0, 1024, 1024, 3072, 3100]
+    for which in (_lib.MSA_WS_INDEX, _lib.MSA_WS_FWD, _lib.MSA_WS_BWD):
+        need = _lib.msa_workspace_size_varlen(p, cu, which)
+        one = _lib.msa_workspace_size(_prob(N=2048), which)
+        assert need >= one > 0
+    assert _lib.msa_fwd_varlen(p, cu, 16, 16, 16, 16, 16, 16, 256, 16, None) == _lib.MSA_ERR_WORKSPACE
+
+
 def test_empty_problem_is_a_no_op():
     p = _prob(N=0)
     assert _lib.msa_index_topk(p, None, None, None, None, None, 0, None) == _lib.MSA_OK
