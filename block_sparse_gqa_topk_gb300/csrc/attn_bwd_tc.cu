@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* b_s = bar + 9;      // (1)(2) done
   uint64_t* b_p = bar + 10;     // E1 done (P^T, dS^T in smem)
   uint64_t* b_q = bar + 11;     // (3)(4)(5) done
-  uint64_t* b_e = bar + 12;     // E2 done (dQ^T columns and the staging read)
+  uint64_t* b_e = bar + 12;     // E2 has read dQ^T into registers
   uint64_t* b_key = bar + 13;   // block's MMAs done
   uint64_t* b_kfree = bar + 14; // block's accumulators read out
   uint64_t* mmadone = bar + 15;
@@ -424,7 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int hh = 0; hh < RW / RB; ++hh) {  // RB rows at a time
             uint32_t a[RB], d2[RB];
-            if constexpr (RB == 16) {
+            if constexpr (RB == 32) {
+              tmem_ld_32x32b_x32(tmem + lb + cST + RW * wg + RB * hh, a);
+              tmem_ld_32x32b_x32(tmem + lb + cDPT + RW * wg + RB * hh, d2);
+            } else if constexpr (RB == 16) {
               tmem_ld_32x32b_x16(tmem + lb + cST + RW * wg + RB * hh, a);
               tmem_ld_32x32b_x16(tmem + lb + cDPT + RW * wg + RB * hh, d2);
             } else {
@@ -554,6 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_32x32b_x8(tmem + lb + cDQT + RW * wg, a);
           }
           tmem_wait_ld();
+          // dQ^T is in registers: the z^T MMA of the next chunk may take its columns
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_e);
           // stage this warp's [RW rows][32 d] block so the global stores below write
           // 64-byte row segments; lanes (2m, 2m+1) swap one value so each stores a pair
           uint8_t* stg = sm + L::kStg + warp * (32 * 64);
@@ -578,11 +585,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (rp >= 0) *reinterpret_cast<uint4*>(p.dq_part + (int64_t)rp * D + 32 * q4 + cc * 8) = v;
           }
           __syncwarp();
+        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_e);
         }
-        tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(b_e);
           mbar_arrive(&sempty[u % 3]);
           if (ch == nch - 1) mbar_arrive(kvempty);
         }
