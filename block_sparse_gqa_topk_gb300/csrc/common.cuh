@@ -27,6 +27,17 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);  // first error wins
 }
 
+// Programmatic dependent launch (PTX griddepcontrol, sm_90 and later).  A kernel
+// launched with the programmatic-serialization attribute may be scheduled while the
+// previous kernel in its stream is still running; griddep_wait() returns once that
+// kernel has completed and its memory writes are visible (at once for a kernel launched
+// without the attribute).  griddep_launch_dependents() lets the next such kernel be
+// scheduled before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -71,6 +71,7 @@ __device__ __forceinline__ int seq_len(const DecodeParams& p, int b, int* status
 // the same order, so every product pairs matching d; the dot product is order-free.
 template <int DI, int NT>
 __global__ void __launch_bounds__(256) decode_pool_kernel(const DecodeParams p) {
+  griddep_launch_dependents();  // the selection may be scheduled while the pool drains
   const int b = blockIdx.y;
   const int L = seq_len(p, b, p.status);
   const int c_own = (L - 1) / 128;
@@ -147,6 +148,8 @@ template <int KM>
 __global__ void __launch_bounds__(256) decode_select_kernel(const DecodeParams p) {
   __shared__ uint64_t s_top[8 * KM];  // warp w's best M at [w M, w M + M)
   __shared__ int s_sel[KM];
+  griddep_wait();  // the pooled scores
+  griddep_launch_dependents();
   const int b = blockIdx.y, g = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = seq_len(p, b, p.status);
@@ -456,6 +459,7 @@ __global__ void __launch_bounds__(256) decode_attn_kernel(const DecodeParams p) 
   __shared__ float s_sv[F8 ? 128 : 1];  // FP8 V row scales
   __shared__ float s_w[32 * 16];  // [topk][G] merge weights
   __shared__ int s_last;
+  griddep_wait();  // the selection and its zeroed arrival counts
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int64_t part = (((int64_t)b * p.H_kv + g) * p.topk + s) * p.G;
   const int c = __ldg(&p.block_idx[((int64_t)b * p.H_kv + g) * p.topk + s]);
@@ -544,6 +548,25 @@ struct DecodeCache {
 
 // Shared driver of msa_decode and msa_decode_fp8: index pooling and selection
 // (bf16 index branch), then the split attention over the selected blocks.
+// Launches a kernel of this file with programmatic stream serialization: it may be
+// scheduled while the previous kernel in the stream drains, and waits for that kernel
+// (griddep_wait) before reading what it wrote.
+template <typename Kern>
+cudaError_t launch_after(Kern kern, dim3 grid, size_t smem, cudaStream_t stream,
+                         const DecodeParams& dp) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, dp);
+}
+
 int run_decode(const msa_problem_t* p, const void* q, const void* q_idx, const DecodeCache& kv,
                const void* k_idx, const int32_t* lens, int32_t* block_idx, void* o, float* lse,
                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -607,19 +630,20 @@ int run_decode(const msa_problem_t* p, const void* q, const void* q_idx, const D
 #undef MSA_POOL
   note_launch();
   const dim3 gsel((unsigned)s.H_kv, (unsigned)s.B);
-  if (s.topk - 1 <= 15) decode_select_kernel<15><<<gsel, 256, 0, stream>>>(dp);
-  else decode_select_kernel<31><<<gsel, 256, 0, stream>>>(dp);
+  cudaError_t e = s.topk - 1 <= 15 ? launch_after(decode_select_kernel<15>, gsel, 0, stream, dp)
+                                   : launch_after(decode_select_kernel<31>, gsel, 0, stream, dp);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
   note_launch();
   const int attn_nt = s.G <= 8 ? 1 : 2;
   const size_t attn_smem = (size_t)128 * (s.d + 8) * 2 + (size_t)8 * attn_nt * 128 * 4 +
                            (size_t)8 * attn_nt * (128 + 8) * 2;
   const dim3 gattn((unsigned)s.topk, (unsigned)s.H_kv, (unsigned)s.B);
-  cudaError_t e = cudaSuccess;
 #define MSA_ATTN(D, NT, F8)                                                                   \
   do {                                                                                        \
     e = cudaFuncSetAttribute(decode_attn_kernel<D, NT, F8>,                                   \
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem);    \
-    if (e == cudaSuccess) decode_attn_kernel<D, NT, F8><<<gattn, 256, attn_smem, stream>>>(dp); \
+    if (e == cudaSuccess)                                                                     \
+      e = launch_after(decode_attn_kernel<D, NT, F8>, gattn, attn_smem, stream, dp);          \
   } while (0)
   if (f8) {
     if (s.d == 128) {
