@@ -148,8 +148,7 @@ template <int KM>
 __global__ void __launch_bounds__(256) decode_select_kernel(const DecodeParams p) {
   __shared__ uint64_t s_top[8 * KM];  // warp w's best M at [w M, w M + M)
   __shared__ int s_sel[KM];
-  griddep_wait();  // the pooled scores
-  griddep_launch_dependents();
+  griddep_launch_dependents();  // the attention may be scheduled while this runs
   const int b = blockIdx.y, g = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = seq_len(p, b, p.status);
@@ -159,6 +158,7 @@ __global__ void __launch_bounds__(256) decode_select_kernel(const DecodeParams p
   uint64_t top[KM];
 #pragma unroll
   for (int s = 0; s < KM; ++s) top[s] = 0;  // below every real key
+  griddep_wait();  // the pooled scores (the length above is an input)
   for (int c0 = warp * 32 + lane; c0 < c_own; c0 += 4 * 256) {
     float v4[4];
 #pragma unroll
@@ -176,14 +176,13 @@ __global__ void __launch_bounds__(256) decode_select_kernel(const DecodeParams p
       }
     }
   }
-  // warp's best M
+  // warp's best M: each round takes the largest list head, as a warp max of the key's
+  // high word and then of the low word among the lanes holding that high word
   for (int r = 0; r < M; ++r) {
-    uint64_t best = top[0];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
+    const uint32_t hi = (uint32_t)(top[0] >> 32), lo = (uint32_t)top[0];
+    const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? lo : 0u);
+    const uint64_t best = ((uint64_t)mhi << 32) | mlo;
     if (lane == 0) s_top[warp * M + r] = best;  // 0 when the warp had fewer than M candidates
     if (best != 0 && top[0] == best) {
 #pragma unroll
@@ -234,7 +233,7 @@ __global__ void __launch_bounds__(256) decode_select_kernel(const DecodeParams p
 // folded into it), its row sum l stays fp32.
 template <int D, int NT, bool F8>
 __device__ __forceinline__ void block_partial(const DecodeParams& p, uint8_t* dsm, int64_t part,
-                                              int c, int b, int g, float* s_l, float* s_sv) {
+                                              int c, int b, int g, int L, float* s_l, float* s_sv) {
   constexpr int KS = D + 8;    // padded V row (bf16): conflict-free ldmatrix phases
   constexpr int PS = 128 + 8;  // padded P row (bf16)
   constexpr int NP = D / 32;   // 32-wide d chunks (two k steps each)
@@ -244,7 +243,6 @@ __device__ __forceinline__ void block_partial(const DecodeParams& p, uint8_t* ds
   const int G = p.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const int L = seq_len(p, b, p.status);
   const int jmax = min(L - 1, c * 128 + 127) - c * 128;  // last visible row of the block
   const int64_t row0 = ((int64_t)b * p.Lmax + c * 128) * p.H_kv + g;  // (b, c 128, g)
   // ---- V rows into shared memory ----
@@ -459,14 +457,15 @@ __global__ void __launch_bounds__(256) decode_attn_kernel(const DecodeParams p) 
   __shared__ float s_sv[F8 ? 128 : 1];  // FP8 V row scales
   __shared__ float s_w[32 * 16];  // [topk][G] merge weights
   __shared__ int s_last;
-  griddep_wait();  // the selection and its zeroed arrival counts
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int L = seq_len(p, b, p.status);  // an input: read while the selection finishes
+  griddep_wait();  // the selection and its zeroed arrival counts
   const int64_t part = (((int64_t)b * p.H_kv + g) * p.topk + s) * p.G;
   const int c = __ldg(&p.block_idx[((int64_t)b * p.H_kv + g) * p.topk + s]);
   if (c < 0) {
     for (int h = threadIdx.x; h < p.G; h += blockDim.x) p.lse_part[part + h] = -INFINITY;
   } else {
-    block_partial<D, NT, F8>(p, dsm, part, c, b, g, s_l, s_sv);
+    block_partial<D, NT, F8>(p, dsm, part, c, b, g, L, s_l, s_sv);
   }
   __threadfence();  // this CTA's partial is visible before its arrival
   __syncthreads();
