@@ -116,10 +116,10 @@ __global__ void plan_fill_kernel(const int32_t* __restrict__ block_idx, int64_t 
   entries[pos] = (i << kSlotBits) | slot;
 }
 
-// Shared-memory variants: one CTA takes kRowsPerCta consecutive rows of one
-// (b, g), histograms their block ids in shared memory and touches global memory
-// once per non-empty bin (count) or reserves one range per bin (fill), instead of
-// one global atomic per entry.  Used when the nb-bin histogram fits in smem.
+// Shared-memory count: one CTA takes kRowsPerCta consecutive rows of one (b, g),
+// histograms their block ids in shared memory and touches global memory once per
+// non-empty bin instead of once per entry.  Used, with the sorting fill above, when
+// the nb-bin histogram fits in smem.
 constexpr int kRowsPerCta = 1024;
 constexpr int kSmemBins = 16384;
 
@@ -134,49 +134,112 @@ __global__ void plan_count_smem_kernel(const int32_t* __restrict__ block_idx, in
   __syncthreads();
   const int32_t* src = block_idx + (bg * N + i0) * topk;
   const int n = (i1 - i0) * topk;
-  for (int e = threadIdx.x; e < n; e += blockDim.x) {
-    const int c = __ldg(&src[e]);
-    if (c < 0) continue;
-    if (c >= nb) {
-      set_status(status, MSA_ERR_ARG);
-      continue;
+  for (int e0 = threadIdx.x; e0 < n; e0 += 8 * blockDim.x) {
+    int cv[8];  // eight loads in flight before the histogram updates
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e0 + u * blockDim.x;
+      cv[u] = e < n ? __ldg(&src[e]) : -1;
     }
-    atomicAdd(&hist[c], 1);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = cv[u];
+      if (c < 0) continue;
+      if (c >= nb) {
+        set_status(status, MSA_ERR_ARG);
+        continue;
+      }
+      atomicAdd(&hist[c], 1);
+    }
   }
   __syncthreads();
   for (int c = threadIdx.x; c < nb; c += blockDim.x)
     if (hist[c]) atomicAdd(&cnt[bg * nb + c], hist[c]);
 }
 
-__global__ void plan_fill_smem_kernel(const int32_t* __restrict__ block_idx, int N, int topk,
-                                      int nb, const int* __restrict__ off,
-                                      int* __restrict__ cursor, int* __restrict__ entries) {
-  extern __shared__ int hist[];
-  const int chunks = (N + kRowsPerCta - 1) / kRowsPerCta;
+// Fill as a counting sort in shared memory: one CTA of kFillThreads takes `rows`
+// consecutive rows of one (b, g) (rows * topk <= kFillEntries entries), loads their
+// block ids into registers at once, histograms them, reserves one range of the global
+// list per non-empty bin, places each entry at its bin-ordered position in shared memory
+// (block id and entry index in one word), and writes the entries out in that order, so
+// consecutive threads write consecutive slots of a bin's range.
+constexpr int kFillThreads = 512;
+constexpr int kFillEntries = 16384;  // entry index < 2^16, block id < kSmemBins <= 2^16
+constexpr int kFillPer = kFillEntries / kFillThreads;
+
+__global__ void __launch_bounds__(kFillThreads)
+    plan_fill_sort_kernel(const int32_t* __restrict__ block_idx, int N, int topk, int nb, int rows,
+                          const int* __restrict__ off, int* __restrict__ cursor,
+                          int* __restrict__ entries) {
+  extern __shared__ int fill_smem[];
+  int* hist = fill_smem;        // [nb] counts, then the bin's next position in `stage`
+  int* delta = fill_smem + nb;  // [nb] global slot minus position in `stage`, per bin
+  uint32_t* stage = reinterpret_cast<uint32_t*>(fill_smem + 2 * nb);  // (c << 16 | e), bin order
+  __shared__ int s_warp[kFillThreads / 32];
+  const int chunks = (N + rows - 1) / rows;
   const int64_t bg = blockIdx.x / chunks;
-  const int i0 = (blockIdx.x % chunks) * kRowsPerCta;
-  const int i1 = min(N, i0 + kRowsPerCta);
-  for (int c = threadIdx.x; c < nb; c += blockDim.x) hist[c] = 0;
-  __syncthreads();
+  const int i0 = (blockIdx.x % chunks) * rows;
+  const int i1 = min(N, i0 + rows);
   const int32_t* src = block_idx + (bg * N + i0) * topk;
   const int n = (i1 - i0) * topk;
-  for (int e = threadIdx.x; e < n; e += blockDim.x) {
-    const int c = __ldg(&src[e]);
-    if (c >= 0 && c < nb) atomicAdd(&hist[c], 1);
+  int cv[kFillPer];  // block id of entry threadIdx.x + u kFillThreads, -1 if none
+#pragma unroll
+  for (int u = 0; u < kFillPer; ++u) {
+    const int e = threadIdx.x + u * kFillThreads;
+    const int c = e < n ? __ldg(&src[e]) : -1;
+    cv[u] = c < nb ? c : -1;
+  }
+  for (int c = threadIdx.x; c < nb; c += kFillThreads) hist[c] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < kFillPer; ++u)
+    if (cv[u] >= 0) atomicAdd(&hist[cv[u]], 1);
+  __syncthreads();
+  // exclusive scan of the counts: thread t owns bins [t per, t per + per)
+  const int per = (nb + kFillThreads - 1) / kFillThreads;
+  const int c0 = min(nb, (int)threadIdx.x * per), c1 = min(nb, c0 + per);
+  int tot = 0;
+  for (int c = c0; c < c1; ++c) tot += hist[c];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int nw = kFillThreads / 32;
+  int incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += x;
+    }
+    if (lane < nw) s_warp[lane] = w;  // inclusive over warps
   }
   __syncthreads();
-  // reserve one range per non-empty bin; the bin becomes this CTA's write cursor
-  for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+  const int total = s_warp[nw - 1];
+  int run = (warp ? s_warp[warp - 1] : 0) + incl - tot;
+  for (int c = c0; c < c1; ++c) {
     const int h = hist[c];
-    if (h) hist[c] = off[bg * nb + c] + atomicAdd(&cursor[bg * nb + c], h);
+    delta[c] = h ? off[bg * nb + c] + atomicAdd(&cursor[bg * nb + c], h) - run : 0;
+    hist[c] = run;
+    run += h;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < n; e += blockDim.x) {
-    const int c = __ldg(&src[e]);
-    if (c < 0 || c >= nb) continue;
-    const int q = e / topk;
-    const int pos = atomicAdd(&hist[c], 1);
-    entries[pos] = ((i0 + q) << kSlotBits) | (e - q * topk);
+#pragma unroll
+  for (int u = 0; u < kFillPer; ++u)
+    if (cv[u] >= 0)
+      stage[atomicAdd(&hist[cv[u]], 1)] =
+          ((uint32_t)cv[u] << 16) | (uint32_t)(threadIdx.x + u * kFillThreads);
+  __syncthreads();
+  for (int q = threadIdx.x; q < total; q += kFillThreads) {
+    const uint32_t w = stage[q];
+    const int c = (int)(w >> 16), e = (int)(w & 0xFFFFu);
+    const int r = e / topk;
+    entries[delta[c] + q] = ((i0 + r) << kSlotBits) | (e - r * topk);
   }
 }
 
@@ -213,13 +276,17 @@ cudaError_t launch_plan(const Shape& s, const int32_t* block_idx, int qpt, const
   const int64_t chunks = (s.N + kRowsPerCta - 1) / kRowsPerCta;
   const unsigned grid_s = (unsigned)((int64_t)s.B * s.H_kv * chunks);
   const size_t hist_bytes = (size_t)s.nb * sizeof(int);
+  const int fill_rows = s.topk >= kFillEntries ? 1 : kFillEntries / s.topk;
+  const unsigned grid_f =
+      (unsigned)((int64_t)s.B * s.H_kv * ((s.N + fill_rows - 1) / fill_rows));
+  const size_t fill_bytes = 2 * hist_bytes + (size_t)fill_rows * s.topk * sizeof(uint32_t);
   if (n > 0 && smem_bins) {
-    if (hist_bytes > 48 * 1024) {
+    if (hist_bytes > 48 * 1024)
       cudaFuncSetAttribute(plan_count_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)hist_bytes);
-      cudaFuncSetAttribute(plan_fill_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)hist_bytes);
-    }
+    if (fill_bytes > 48 * 1024)
+      cudaFuncSetAttribute(plan_fill_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)fill_bytes);
     plan_count_smem_kernel<<<grid_s, 512, hist_bytes, st>>>(block_idx, s.N, s.topk, s.nb,
                                                             pl.cnt, cx.status);
     note_launch();
@@ -234,8 +301,8 @@ cudaError_t launch_plan(const Shape& s, const int32_t* block_idx, int qpt, const
   note_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (n > 0 && smem_bins) {
-    plan_fill_smem_kernel<<<grid_s, 512, hist_bytes, st>>>(block_idx, s.N, s.topk, s.nb, pl.off,
-                                                           pl.cnt, pl.entries);
+    plan_fill_sort_kernel<<<grid_f, kFillThreads, fill_bytes, st>>>(block_idx, s.N, s.topk, s.nb, fill_rows,
+                                                           pl.off, pl.cnt, pl.entries);
     note_launch();
     e = cudaGetLastError();
   } else if (n > 0) {
