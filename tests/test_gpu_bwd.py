@@ -6,7 +6,9 @@ Full workloads (every gradient and the KL): small edge cases and the 8K workload
 Large workloads (32K, 128K, 1M): dq and dq_idx on seeded sampled rows (both are
 per-row quantities); dk and dv from a second backward whose dO is zero outside
 the sampled rows and whose KL weight is 0, which the oracle's row-subset backward
-computes exactly.
+computes exactly.  dk_idx of one whole key block at 32K and 128K: only rows at or after
+the block can select it, so the oracle's sets of those rows name every (query, group)
+that attends to it, and the row-subset backward over them gives its dk_idx exactly.
 """
 import numpy as np
 import pytest
@@ -111,3 +113,30 @@ def test_bwd_matches_oracle_sampled(name, n_rows):
     c3 = grad_close(f64(g2["dk"]), ref0["dk"], "dk")
     c4 = grad_close(f64(g2["dv"]), ref0["dv"], "dv")
     print(f"{name}: dq {c1}, dq_idx {c2}, dk {c3}, dv {c4}")
+
+
+@pytest.mark.parametrize("name", ["32k", "128k"])
+def test_bwd_dk_idx_of_a_key_block_full_size(name):
+    cfg = cfg_of(name)
+    assert cfg.B == 1
+    h, d = device_inputs(cfg)
+    nb = (cfg.N + cfg.Bk - 1) // cfg.Bk
+    c = nb - 8  # a late block: its possible readers are the 8 blocks of rows from c on
+    later = np.arange(c * cfg.Bk, cfg.N, dtype=np.int64)
+    bi_later, _, _ = oracle.select(cfg, h, rows=later)
+    _, _, li_later = oracle.forward(cfg, h, bi_later, rows=later, main=False)
+    # rows before block c keep a local window of sets, which never holds block c
+    block_idx = _dev_sel(cfg, bi_later, later)
+    lse_idx = _dev_lse_idx(cfg, li_later, later)
+    o, lse = ops.msa_fwd(d["q"], d["k"], d["v"], block_idx, scale=cfg.scale, d_idx=cfg.d_idx)
+    w = _w(cfg)
+    g = ops.msa_bwd(d["q"], d["k"], d["v"], o, lse, d["dO"], d["q_idx"], d["k_idx"], block_idx,
+                    lse_idx, w, scale=cfg.scale)
+    assert ops.device_status() == 0
+    hit = (bi_later == c).any(axis=(1, 2))  # rows with block c in some group's set
+    assert hit[:cfg.Bk].all()  # the block's own rows always hold it
+    rows = later[hit]
+    ref = oracle.backward(cfg, h, bi_later[hit], w, rows=rows)
+    keys = slice(c * cfg.Bk, min(cfg.N, (c + 1) * cfg.Bk))
+    cos, rel = grad_close(f64(g["dk_idx"])[0, keys], ref["dk_idx"][0, keys], "dk_idx")
+    print(f"{name}: block {c}, {len(rows)} reading rows: dk_idx cos {cos:.6f}, rel {rel:.2e}")
