@@ -97,7 +97,7 @@ def test_bwd_matches_oracle_sampled(name, n_rows):
     ref = oracle.backward(cfg, h, bi_ref, w, rows=rows)
     c1 = grad_close(f64(g["dq"])[b, i], ref["dq"], "dq")
     c2 = grad_close(f64(g["dq_idx"])[b, i], ref["dq_idx"], "dq_idx")
-    # (the KL total is not checked here: rows outside the sample carry a placeholder
+    # (the KL total is checked in 3): here rows outside the sample carry a placeholder
     # lse_idx, so their KL terms are not a divergence)
     del g
     # 2) key-side gradients of the sampled rows only: dO zero elsewhere, no KL
@@ -112,7 +112,18 @@ def test_bwd_matches_oracle_sampled(name, n_rows):
     ref0 = oracle.backward(cfg, h, bi_ref, 0.0, rows=rows)
     c3 = grad_close(f64(g2["dk"]), ref0["dk"], "dk")
     c4 = grad_close(f64(g2["dv"]), ref0["dv"], "dv")
-    print(f"{name}: dq {c1}, dq_idx {c2}, dk {c3}, dv {c4}")
+    del g2
+    # 3) the KL of the sampled rows: lse = +inf outside the sample makes those rows'
+    # main-branch probabilities, hence their teacher and their KL terms, exactly zero
+    other = torch.ones(cfg.B, cfg.N, dtype=torch.bool, device="cuda")
+    other.view(-1)[torch.from_numpy(rows).cuda()] = False
+    lse_m = lse.clone().masked_fill_(other[:, None, :], float("inf"))
+    g3 = ops.msa_bwd(d["q"], d["k"], d["v"], o, lse_m, d["dO"], d["q_idx"], d["k_idx"],
+                     block_idx, lse_idx, w, scale=cfg.scale)
+    assert ops.device_status() == 0
+    kl = float(g3["kl"].cpu())
+    assert abs(kl - ref["kl"]) <= KL_REL * abs(ref["kl"]) + 1e-6, (kl, ref["kl"])
+    print(f"{name}: dq {c1}, dq_idx {c2}, dk {c3}, dv {c4}, kl {kl:.6e} vs {ref['kl']:.6e}")
 
 
 @pytest.mark.parametrize("name", ["32k", "128k"])
