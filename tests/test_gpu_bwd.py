@@ -6,7 +6,7 @@ Full workloads (every gradient and the KL): small edge cases and the 8K workload
 Large workloads (32K, 128K, 1M): dq and dq_idx on seeded sampled rows (both are
 per-row quantities); dk and dv from a second backward whose dO is zero outside
 the sampled rows and whose KL weight is 0, which the oracle's row-subset backward
-computes exactly.  dk_idx of one whole key block at 32K and 128K: only rows at or after
+computes exactly.  dk_idx of one whole key block at 32K, 128K and 1M: only rows at or after
 the block can select it, so the oracle's sets of those rows name every (query, group)
 that attends to it, and the row-subset backward over them gives its dk_idx exactly.
 """
@@ -126,7 +126,7 @@ def test_bwd_matches_oracle_sampled(name, n_rows):
     print(f"{name}: dq {c1}, dq_idx {c2}, dk {c3}, dv {c4}, kl {kl:.6e} vs {ref['kl']:.6e}")
 
 
-@pytest.mark.parametrize("name", ["32k", "128k"])
+@pytest.mark.parametrize("name", ["32k", "128k", "1m"])
 def test_bwd_dk_idx_of_a_key_block_full_size(name):
     cfg = cfg_of(name)
     assert cfg.B == 1
