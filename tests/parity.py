@@ -78,6 +78,16 @@ def check_selection(cfg, inputs, bi_gpu_rows, rows, bi_ref, kth):
     return int(same.sum()), int(near.sum()), diff
 
 
+def validated_gpu_sets(cfg, inputs, bi_gpu_rows, rows):
+    """The GPU's block sets of the listed rows, after the near-tie rule has accepted
+    them: the oracle then reruns on exactly these sets, so a row where the GPU took
+    another valid set inside the band is compared against the oracle's output for
+    that set instead of being skipped.  Returns (sets [R,H_kv,k], n_differing)."""
+    bi_ref, kth, _ = oracle.select(cfg, inputs, rows=rows)
+    _, _, diff = check_selection(cfg, inputs, bi_gpu_rows, np.asarray(rows), bi_ref, kth)
+    return np.ascontiguousarray(bi_gpu_rows, dtype=np.int32), int(diff.sum())
+
+
 def grad_close(got: np.ndarray, ref: np.ndarray, name: str):
     g = got.ravel().astype(np.float64)
     r = ref.ravel().astype(np.float64)

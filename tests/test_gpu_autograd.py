@@ -10,7 +10,7 @@ import torch
 import oracle
 from block_sparse_gqa_topk_gb300 import ops, synth
 from gpu_inputs import host_inputs
-from parity import KL_REL, O_TOL, f64, grad_close, to_dev
+from parity import KL_REL, O_TOL, f64, gpu_sel_rows, grad_close, to_dev, validated_gpu_sets
 
 pytestmark = pytest.mark.gpu
 
@@ -20,17 +20,19 @@ def test_autograd_step_matches_oracle():
     h = host_inputs(cfg)
     leaf = {n: to_dev(h[n]).clone().requires_grad_(True) for n in ("q", "k", "v", "q_idx", "k_idx")}
     dO = to_dev(h["dO"])
-    o = ops.attention(leaf["q"], leaf["k"], leaf["v"], leaf["q_idx"], leaf["k_idx"],
-                      topk=cfg.topk, scale=cfg.scale, kl_coef=cfg.kl_coef)
+    o, block_idx = ops.MSAFunction.apply(leaf["q"], leaf["k"], leaf["v"], leaf["q_idx"],
+                                         leaf["k_idx"], cfg.topk, 128, cfg.scale, None,
+                                         cfg.kl_coef)
     o.backward(dO)
     assert ops.device_status() == 0
-    bi_ref, _, _ = oracle.select(cfg, h)
-    o_ref, _, _ = oracle.forward(cfg, h, bi_ref, index=False)
-    # the GPU's own selection drives this step; on this seeded workload it equals the
-    # oracle's (no near-ties), so the oracle's sets serve as the reference
+    # the GPU's own selection drives this step: validated against the oracle's with the
+    # near-tie rule, then the oracle reruns on exactly those sets
+    rows = np.arange(cfg.B * cfg.N, dtype=np.int64)
+    sets, _ = validated_gpu_sets(cfg, h, gpu_sel_rows(cfg, block_idx.cpu().numpy(), rows), rows)
+    o_ref, _, _ = oracle.forward(cfg, h, sets, index=False)
     assert np.abs(f64(o.detach()).reshape(o_ref.shape) - o_ref).max() <= O_TOL
     w = cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N)
-    ref = oracle.backward(cfg, h, bi_ref, w)
+    ref = oracle.backward(cfg, h, sets, w)
     for n, r in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("q_idx", "dq_idx"), ("k_idx", "dk_idx")):
         g = leaf[n].grad
         assert g is not None and g.dtype == torch.bfloat16, n

@@ -63,19 +63,17 @@ def test_decode_fp8_matches_oracle(name):
     k_deq, v_deq = fp8.dequantize_rows(kq, ks_ref), fp8.dequantize_rows(vq, vs_ref)
     q_bits = np.stack([h["q"][b, L - 1] for b, L in enumerate(lens)])
     sel = np.zeros_like(bi)
-    same = []
     for b, L in enumerate(lens):
         cb = cfg.with_(B=1, N=L)
         hb = {n: np.ascontiguousarray(h[n][b:b + 1, :L]) for n in h}
         rows = np.array([L - 1], dtype=np.int64)
         bi_ref, kth, _ = oracle.select(cb, hb, rows=rows)
-        _, _, diff = check_selection(cb, hb, bi[b][None], rows, bi_ref, kth)
-        sel[b] = bi_ref[0]
-        same.append(not diff.any())
+        check_selection(cb, hb, bi[b][None], rows, bi_ref, kth)
+        # the output follows the set the GPU took (the oracle's outside the near-tie
+        # band, a valid set inside it): the oracle's decode runs on that set
+        sel[b] = bi[b]
     o_ref, lse_ref = fp8.decode_attention(q_bits, k_deq, v_deq, sel, lens, cfg.scale)
     for b in range(cfg.B):
-        if not same[b]:  # a near-tie chose another valid set: the output follows that set
-            continue
         eo = np.abs(o[b] - o_ref[b]).max()
         el = np.abs(lse[b] - lse_ref[b]).max()
         assert eo <= O_TOL and el <= LSE_TOL, (name, b, eo, el)
