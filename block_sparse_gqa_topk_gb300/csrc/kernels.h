@@ -113,6 +113,15 @@ int device_ctx(Ctx* cx);
 // Launch bookkeeping (msa_api.cu): counts launches and records the profiling
 // events of msa_set_kernel_events around the named kernels.
 void note_launch(int n = 1);
+
+// The calling thread's current CUDA context (the driver's cuCtxGetCurrent, reached
+// through the runtime's entry-point query), or nullptr.
+void* current_context();
+// Device address of a module-scope __device__ variable on the current device.  The
+// address is cached per (device, context) and looked up again when the context
+// changes (after cudaDeviceReset the module is loaded anew and the old address is
+// stale).  A first lookup may load the module: do it before any stream capture.
+int device_symbol_address(const void* symbol, void** out);
 void kernel_event(int kernel, bool before, cudaStream_t st);
 
 }  // namespace msa

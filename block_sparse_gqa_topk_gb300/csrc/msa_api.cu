@@ -19,20 +19,13 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s per device-side wait
 uint64_t g_wait_ns = kDefaultWaitNs;
 int g_debug = 0;
 std::mutex g_mu;
+std::mutex g_sym_mu;
 
 int status_ptr(int** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MSA_ERR_CUDA;
-  static int* cache[64] = {nullptr};
-  if (dev < 0 || dev >= 64) return MSA_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!cache[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return MSA_ERR_CUDA;
-    cache[dev] = static_cast<int*>(p);
-  }
-  *out = cache[dev];
-  return MSA_OK;
+  void* p = nullptr;
+  const int rc = device_symbol_address(reinterpret_cast<const void*>(&g_status_word), &p);
+  if (rc == MSA_OK) *out = static_cast<int*>(p);
+  return rc;
 }
 
 int make_ctx(Ctx* cx) {
@@ -108,6 +101,54 @@ cudaEvent_t g_ev[4][2] = {};
 }  // namespace
 
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+void* current_context() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  static GetCurrent fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<GetCurrent>(ptr);
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+int device_symbol_address(const void* symbol, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MSA_ERR_CUDA;
+  struct Entry {
+    const void* symbol;
+    void* ctx;
+    void* addr;
+  };
+  static Entry cache[64][4] = {};
+  void* ctx = current_context();
+  std::lock_guard<std::mutex> lk(g_sym_mu);
+  Entry* slot = nullptr;
+  for (Entry& e : cache[dev]) {
+    if (e.symbol == symbol) {
+      slot = &e;
+      break;
+    }
+    if (!e.symbol && !slot) slot = &e;
+  }
+  if (!slot) return MSA_ERR_CUDA;  // more symbols than slots: a build error, not a user's
+  if (!ctx || slot->symbol != symbol || slot->ctx != ctx || !slot->addr) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, symbol) != cudaSuccess || !a) return MSA_ERR_CUDA;
+    slot->symbol = symbol;
+    slot->addr = a;
+    slot->ctx = current_context();  // the lookup makes the primary context current
+  }
+  *out = slot->addr;
+  return MSA_OK;
+}
 
 int validate_problem(const msa_problem_t* p, Shape* s) { return check_problem(p, s); }
 int device_ctx(Ctx* cx) { return make_ctx(cx); }

@@ -13,11 +13,15 @@
 // Every GPU that loads the library holds it until the process exits.  Host code
 // cannot use the array's name as a device address (on the host it names a shadow
 // variable), so the first call on each device, with that device current, looks the
-// address up with cudaGetSymbolAddress and caches it; make that first call before
-// any stream capture.  All calls on a device share the one array and it keeps the
-// last call's contents: the kernels clear what must start at zero themselves, and
-// calls whose executions overlap on the GPU (different streams, no ordering) race
-// on it and must not be issued.
+// address up with cudaGetSymbolAddress and caches it per (device, context); make
+// that first call before any stream capture.  A new context on the device (after
+// cudaDeviceReset, for instance) loads the module again, and the next call looks the
+// address up again.  All calls on a device share the one array and it keeps the last
+// call's contents: each call zeroes the counters it needs with a cudaMemsetAsync on
+// the caller's stream (a memset into the array, not an allocation), and calls whose
+// executions overlap on the GPU (different streams, no ordering) race on it and must
+// not be issued.  The stream must belong to the current device, as for every other
+// entry point.
 #include <mutex>
 
 #include "kernels.h"
@@ -29,19 +33,27 @@ constexpr size_t kScratchBytes = 64ull << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {nullptr};
+struct ScratchAddr {
+  void* ctx;
+  void* ptr;
+};
+ScratchAddr g_scratch_addr[64] = {};
 
-// Device address of the scratch array on the current device (looked up once).
+// Device address of the scratch array on the current device, looked up once per
+// (device, context).
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MSA_ERR_CUDA;
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchAddr& e = g_scratch_addr[dev];
+  if (!ctx || e.ctx != ctx || !e.ptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MSA_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    e.ptr = p;
+    e.ctx = current_context();  // the lookup makes the primary context current
   }
-  *out = g_scratch_ptr[dev];
+  *out = e.ptr;
   return MSA_OK;
 }
 

@@ -262,10 +262,13 @@ uint64_t msa_kernel_launch_count(void);
  * the library holds it until exit; msa_noalloc_scratch_bytes() returns the size).
  * Problems whose index workspace (msa_workspace_size(p, MSA_WS_INDEX)) exceeds it
  * return MSA_ERR_WORKSPACE before anything is enqueued; with lse_idx == NULL no
- * scratch is used.  The first call on a device looks up the array's device address
- * and must come before any stream capture.  All calls on a device share the array
- * and it keeps the previous call's contents (the kernels clear what they need):
- * calls that may overlap on the GPU race and must be ordered by the caller.
+ * scratch is used.  The first call on a device (and the first after the device's
+ * context changes, e.g. after cudaDeviceReset) looks up the array's device address,
+ * which may load the module: make it before any stream capture.  All calls on a
+ * device share the array and it keeps the previous call's contents: each call zeroes
+ * the counters it needs with a memset on `stream` (no allocation).  Calls that may
+ * overlap on the GPU race and must be ordered by the caller.  `stream` must belong
+ * to the current device, as for every entry point.
  */
 int msa_index_topk_noalloc(const msa_problem_t* p, const void* q_idx, const void* k_idx,
                            int32_t* block_idx, float* lse_idx, cudaStream_t stream);

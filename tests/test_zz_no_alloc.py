@@ -21,16 +21,20 @@ def test_oversized_problem_is_rejected_before_any_launch():
     assert rc == _lib.MSA_ERR_WORKSPACE
 
 
-@pytest.mark.gpu
-def test_noalloc_matches_workspace_entry_point_twice():
+def _problem(cfg):
+    return _lib.Problem(B=cfg.B, N=cfg.N, H_q=cfg.H_q, H_kv=cfg.H_kv, d=cfg.d, d_idx=cfg.d_idx,
+                        Bk=cfg.Bk, topk=cfg.topk, causal=1, scale=cfg.scale, scale_idx=0.0)
+
+
+def _compare_twice(cfg, with_lse=True):
+    """Runs the workspace entry point once and the no-alloc one twice in a row on the
+    same inputs; block sets must be identical and lse_idx within the LSE tolerance."""
     import torch
     from parity import to_dev
 
-    cfg = synth.CONFIGS["8k"]
     h = synth.make_inputs(cfg, names=("q_idx", "k_idx"))
     qi, ki = to_dev(h["q_idx"]), to_dev(h["k_idx"])
-    prob = _lib.Problem(B=cfg.B, N=cfg.N, H_q=cfg.H_q, H_kv=cfg.H_kv, d=cfg.d, d_idx=cfg.d_idx,
-                        Bk=cfg.Bk, topk=cfg.topk, causal=1, scale=cfg.scale, scale_idx=0.0)
+    prob = _problem(cfg)
     need = _lib.msa_workspace_size(prob, _lib.MSA_WS_INDEX)
     assert 0 < need <= _lib.msa_noalloc_scratch_bytes()
     stream = torch.cuda.current_stream().cuda_stream
@@ -49,8 +53,24 @@ def test_noalloc_matches_workspace_entry_point_twice():
     for call in range(2):
         bi, li = outputs()
         _lib.check(_lib.msa_index_topk_noalloc(prob, qi.data_ptr(), ki.data_ptr(), bi.data_ptr(),
-                                               li.data_ptr(), stream), "msa_index_topk_noalloc")
+                                               li.data_ptr() if with_lse else None, stream),
+                   "msa_index_topk_noalloc")
         assert _lib.msa_get_device_status(stream) == 0
-        np.testing.assert_array_equal(bi.cpu().numpy(), bi_ref.cpu().numpy(), err_msg=f"call {call}")
-        err = float((li - li_ref).abs().max())
-        assert err <= LSE_TOL, f"call {call}: lse_idx differs by {err}"
+        np.testing.assert_array_equal(bi.cpu().numpy(), bi_ref.cpu().numpy(),
+                                      err_msg=f"{cfg.name} call {call}")
+        if with_lse:
+            err = float((li - li_ref).abs().max())
+            assert err <= LSE_TOL, f"{cfg.name} call {call}: lse_idx differs by {err}"
+        else:  # no lse_idx asked for: the output buffer is left alone
+            assert torch.isnan(li).all()
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_workspace_entry_point_twice():
+    # a large problem first, then a ragged one (N not a multiple of 128, so the shared
+    # array holds the larger call's leftovers beyond the small call's lists), then the
+    # block-selection-only form (lse_idx NULL, no scratch used)
+    _compare_twice(synth.CONFIGS["8k"])
+    _compare_twice(synth.CONFIGS["tiny"].with_(name="ragged-noalloc", N=1000, B=3, seed=71))
+    _compare_twice(synth.CONFIGS["tiny"].with_(name="sel-only-noalloc", N=1500, seed=72),
+                   with_lse=False)
