@@ -12,10 +12,14 @@ Prints one JSON line.  `value` is device-timed tokens/s with inputs resident in
 HBM; `e2e` is the same metric through the public API with pinned host inputs
 copied in and the KL read back every step; `roofline` is the dominant kernel,
 timed live with CUDA events around its launches inside the timed steps;
-`cpu_baseline` is the float64 oracle on a bounded row sample on the host cores.
+`cpu_baseline` is the float64 oracle on a bounded row sample on the host cores;
+`workloads` times the same step on each of the five seeded workloads (tiny, 8K, 32K,
+128K, 1M): ms per step, per forward (index branch + sparse attention), per backward,
+the index scoring + top-k kernel alone, tokens/s and each kernel's fraction of peak.
 `--impl reference` times that oracle alone (the reference arm).
-Under torchrun (N > 1) every rank runs an independent replica (no data-path
-collective): weak scaling, value = tokens of all ranks / max rank time.
+Under torchrun (N > 1) the ranks shard one problem by GQA group (each rank owns a
+contiguous range of the groups; the step ends with the one exchange, an all-reduce
+of dk_idx and the KL): strong scaling, value = the problem's tokens / max rank time.
 """
 from __future__ import annotations
 
@@ -35,6 +39,9 @@ sys.path.insert(0, ROOT)
 from block_sparse_gqa_topk_gb300 import synth  # noqa: E402
 
 METRIC = "MSA fwd+bwd tokens/s @128K (Bk=128,k=16); % of bf16 tensor-pipe peak"
+# the five seeded workloads, each timed by the default run (the 128K one is the headline)
+WORKLOAD_ORDER = ("tiny", "8k", "32k", "128k", "1m")
+WORKLOAD_STEPS = {"tiny": 20, "8k": 20, "32k": 10, "128k": 10, "1m": 3}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -290,6 +297,110 @@ def run_reference(args, cfg, rank):
 
 
 # ----------------------------------------------------------------------------
+# one workload: warm-up steps, then K timed steps with live per-kernel events
+# ----------------------------------------------------------------------------
+def timed_workload(torch, ops, _lib, cfg, d, stream, steps, warmup, barrier=None,
+                   clock_gpu=False, kl_weight=None, after_bwd=None):
+    """Times `steps` whole steps (index scoring + top-k + index LSE, forward, fused
+    backward) of workload `cfg` on the device-resident inputs `d`, after `warmup`
+    untimed steps.  Returns the mean step time, live per-kernel times (CUDA events the
+    library records around its four tensor-core kernels), per-phase times, the
+    algorithmic FLOPs of one step, the launch count and the clock record.  In the
+    group-sharded mode `cfg` and `d` are this rank's groups, `kl_weight` uses the global
+    group count and `after_bwd` is the exchange (all-reduce of dk_idx and the KL)."""
+    w = kl_weight if kl_weight is not None else cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N)
+
+    def step(t, phase_ev=None):
+        if phase_ev:
+            phase_ev[0].record(stream)
+        bi, li = ops.msa_index_topk(t["q_idx"], t["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d)
+        if phase_ev:
+            phase_ev[1].record(stream)
+        o, lse = ops.msa_fwd(t["q"], t["k"], t["v"], bi, scale=cfg.scale, d_idx=cfg.d_idx)
+        if phase_ev:
+            phase_ev[2].record(stream)
+        g = ops.msa_bwd(t["q"], t["k"], t["v"], o, lse, t["dO"], t["q_idx"], t["k_idx"], bi, li, w,
+                        scale=cfg.scale)
+        if after_bwd is not None:
+            g = after_bwd(g)
+        if phase_ev:
+            phase_ev[3].record(stream)
+        return bi, g
+
+    for _ in range(warmup):
+        bi, g = step(d)
+    torch.cuda.synchronize()
+    st = ops.device_status()
+    if st != 0:
+        raise RuntimeError(f"{cfg.name}: device status after warm-up: {_lib.status_string(st)}")
+    sum_T = token_set_total(cfg, bi.cpu().numpy())
+    flops = algorithmic_flops(cfg, sum_T)
+    del bi, g
+
+    K = steps
+    kev = {kname: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(K)] for kname in ("index", "index_lse", "fwd", "bwd")}
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for lst in kev.values():  # materialise the events so their handles exist
+        for a, b in lst:
+            a.record(stream)
+            b.record(stream)
+    kid = {"index": _lib.MSA_KERNEL_INDEX, "index_lse": _lib.MSA_KERNEL_INDEX_LSE,
+           "fwd": _lib.MSA_KERNEL_FWD, "bwd": _lib.MSA_KERNEL_BWD}
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(clock_gpu) if clock_gpu is not False else None
+    if clocks is not None:
+        time.sleep(0.3)
+    launches0 = _lib.msa_kernel_launch_count()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for s in range(K):
+        for kname, lst in kev.items():
+            _lib.msa_set_kernel_events(kid[kname], lst[s][0].cuda_event, lst[s][1].cuda_event)
+        step(d, pev[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    launches = _lib.msa_kernel_launch_count() - launches0
+    clk = clocks.stop() if clocks is not None else None
+    for kname in kev:
+        _lib.msa_set_kernel_events(kid[kname], None, None)
+    st = ops.device_status()
+    if st != 0:
+        raise RuntimeError(f"{cfg.name}: device status after timed steps: {_lib.status_string(st)}")
+    kern_ms = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in kev.items()}
+    phase_ms = {
+        "index": statistics.mean(e[0].elapsed_time(e[1]) for e in pev),
+        "fwd": statistics.mean(e[1].elapsed_time(e[2]) for e in pev),
+        "bwd": statistics.mean(e[2].elapsed_time(e[3]) for e in pev),
+    }
+    return {"ms": t_start.elapsed_time(t_end) / K, "kernels_ms": kern_ms, "phases_ms": phase_ms,
+            "flops": flops, "sum_T": sum_T, "launches": launches, "clocks": clk, "steps": K}
+
+
+def workload_summary(cfg, r, peak_tf):
+    """Per-workload record: ms per step, per forward (index branch + sparse attention)
+    and per backward, the index scoring + top-k kernel alone, tokens/s, and each
+    tensor-core kernel's algorithmic TFLOP/s and fraction of the bf16 peak."""
+    ms, kern, ph, f = r["ms"], r["kernels_ms"], r["phases_ms"], r["flops"]
+    ktf = {k: f[k] / (kern[k] / 1000.0) / 1e12 for k in kern}
+    return {
+        "workload": workload_name(cfg), "steps": r["steps"], "ms_per_step": ms,
+        "tokens_per_s": cfg.B * cfg.N / (ms / 1000.0),
+        "ms_forward": ph["index"] + ph["fwd"], "ms_backward": ph["bwd"],
+        "ms_index_topk": kern["index"], "phases_ms": ph, "kernels_ms": kern,
+        "kernel_tflops": ktf, "kernel_frac_of_peak": {k: v / peak_tf for k, v in ktf.items()},
+        "algorithmic_tflop_per_step": sum(f.values()) / 1e12,
+        "pct_bf16_peak_step": sum(f.values()) / (ms / 1000.0) / 1e12 / peak_tf,
+    }
+
+
+# ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
 def run_ours(args, cfg, rank, world):
@@ -306,8 +417,20 @@ def run_ours(args, cfg, rank, world):
     def to_dev(x):
         return torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
 
+    full_cfg = cfg
+    after_bwd = None
+    if world > 1:
+        # group-sharded mode: this rank owns a contiguous range of the GQA groups and
+        # the step ends with the one exchange (all-reduce of dk_idx and the KL)
+        from block_sparse_gqa_topk_gb300 import shard
+        sh = shard.GroupShard(rank, world, cfg.H_kv)
+        host_t = {n: sh.take(n, torch.from_numpy(host[n].view(np.int16))) for n in names}
+        host = {n: host_t[n].numpy().view(np.uint16) for n in names}
+        del host_t
+        cfg = cfg.with_(H_q=sh.n_groups * cfg.G, H_kv=sh.n_groups)
+        after_bwd = shard.exchange
     d = {n: to_dev(host[n]) for n in names}
-    w = cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N)
+    w = full_cfg.kl_coef / (full_cfg.B * full_cfg.H_kv * full_cfg.N)
     stream = torch.cuda.current_stream(dev)
     if args.warmup_only:  # the indexer warm-up leg alone
         peaks, _ = load_peaks()
@@ -330,82 +453,22 @@ def run_ours(args, cfg, rank, world):
             print(json.dumps({"decode": dec}), flush=True)
         return
 
-    def step(t, phase_ev=None):
-        if phase_ev:
-            phase_ev[0].record(stream)
-        bi, li = ops.msa_index_topk(t["q_idx"], t["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d)
-        if phase_ev:
-            phase_ev[1].record(stream)
-        o, lse = ops.msa_fwd(t["q"], t["k"], t["v"], bi, scale=cfg.scale, d_idx=cfg.d_idx)
-        if phase_ev:
-            phase_ev[2].record(stream)
-        g = ops.msa_bwd(t["q"], t["k"], t["v"], o, lse, t["dO"], t["q_idx"], t["k_idx"], bi, li, w,
-                        scale=cfg.scale)
-        if phase_ev:
-            phase_ev[3].record(stream)
-        return bi, g
-
     def barrier():
         if world > 1:
             dist.barrier()
 
-    for _ in range(args.warmup):
-        bi, g = step(d)
-    torch.cuda.synchronize()
-    st = ops.device_status()
-    if st != 0:
-        raise RuntimeError(f"device status after warm-up: {_lib.status_string(st)}")
-    sum_T = token_set_total(cfg, bi.cpu().numpy())
-    flops = algorithmic_flops(cfg, sum_T)
-
-    # per-kernel events (hook) and per-phase events, one set per timed step
-    K = args.steps
-    kev = {kname: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(K)] for kname in ("index", "index_lse", "fwd", "bwd")}
-    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    for lst in kev.values():  # materialise the events so their handles exist
-        for a, b in lst:
-            a.record(stream)
-            b.record(stream)
-    kid = {"index": _lib.MSA_KERNEL_INDEX, "index_lse": _lib.MSA_KERNEL_INDEX_LSE,
-           "fwd": _lib.MSA_KERNEL_FWD, "bwd": _lib.MSA_KERNEL_BWD}
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         gpu_id = None
-    clocks = ClockSampler(gpu_id)
-    time.sleep(0.3)
-    launches0 = _lib.msa_kernel_launch_count()
-    barrier()
-    torch.cuda.synchronize()
-    t_start.record(stream)
-    for s in range(K):
-        for kname, lst in kev.items():
-            _lib.msa_set_kernel_events(kid[kname], lst[s][0].cuda_event, lst[s][1].cuda_event)
-        step(d, pev[s])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    launches = _lib.msa_kernel_launch_count() - launches0
-    clk = clocks.stop()
-    for kname in kev:
-        _lib.msa_set_kernel_events(kid[kname], None, None)
-    st = ops.device_status()
-    if st != 0:
-        raise RuntimeError(f"device status after timed steps: {_lib.status_string(st)}")
-
-    ms, value = job_rate(t_start.elapsed_time(t_end) / K, cfg.B * cfg.N, world, dev)
-
-    kern_ms = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in kev.items()}
-    phase_ms = {
-        "index": statistics.mean(e[0].elapsed_time(e[1]) for e in pev),
-        "fwd": statistics.mean(e[1].elapsed_time(e[2]) for e in pev),
-        "bwd": statistics.mean(e[2].elapsed_time(e[3]) for e in pev),
-    }
+    r = timed_workload(torch, ops, _lib, cfg, d, stream, args.steps, args.warmup,
+                       barrier=barrier, clock_gpu=gpu_id, kl_weight=w, after_bwd=after_bwd)
+    K = args.steps
+    # strong scaling: the ranks share one problem of B*N tokens
+    ms, value = job_rate(r["ms"], full_cfg.B * full_cfg.N / world, world, dev)
+    kern_ms, phase_ms, flops, launches, clk = (r["kernels_ms"], r["phases_ms"], r["flops"],
+                                               r["launches"], r["clocks"])
     peaks, peak_src = load_peaks()
     peak_tf = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     kflops = {k: flops[k] for k in kern_ms}
@@ -416,8 +479,8 @@ def run_ours(args, cfg, rank, world):
     if os.path.exists(tf_path):
         try:
             with open(tf_path) as f:
-                traffic = json.load(f).get(dom)
-        except (OSError, ValueError):
+                traffic = json.load(f).get(cfg.name, {}).get(dom)
+        except (OSError, ValueError, AttributeError):
             traffic = None
     total_flops = sum(flops.values())
 
@@ -457,8 +520,9 @@ def run_ours(args, cfg, rank, world):
             stream.wait_event(landed[i][n])
         o, lse = ops.msa_fwd(t["q"], t["k"], t["v"], bi, scale=cfg.scale, d_idx=cfg.d_idx)
         stream.wait_event(landed[i]["dO"])
-        return ops.msa_bwd(t["q"], t["k"], t["v"], o, lse, t["dO"], t["q_idx"], t["k_idx"], bi, li,
-                           w, scale=cfg.scale)
+        g = ops.msa_bwd(t["q"], t["k"], t["v"], o, lse, t["dO"], t["q_idx"], t["k_idx"], bi, li,
+                        w, scale=cfg.scale)
+        return after_bwd(g) if after_bwd is not None else g
 
     torch.cuda.synchronize()
     barrier()
@@ -473,18 +537,19 @@ def run_ours(args, cfg, rank, world):
         kl_host[si:si + 1].copy_(g["kl"], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms, e2e_val = job_rate(e0.elapsed_time(e1) / e2e_steps, cfg.B * cfg.N, world, dev)
+    e2e_ms, e2e_val = job_rate(e0.elapsed_time(e1) / e2e_steps, full_cfg.B * full_cfg.N / world,
+                               world, dev)
     del pinned, bufs
 
     # ---- decode (inference) leg ----
     dec = None
-    if not args.no_decode:
+    if not args.no_decode and world == 1:
         dec = decode_leg(torch, ops, d, cfg, dev, stream,
                          float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))
 
     # ---- indexer warm-up leg (dense set) ----
     wu = None
-    if not args.no_warmup_leg:
+    if not args.no_warmup_leg and world == 1:
         wu = warmup_leg(torch, ops, cfg, dev, stream, peak_tf)
         st = ops.device_status()
         if st != 0:
@@ -498,13 +563,34 @@ def run_ours(args, cfg, rank, world):
                "sample": (f"{n_rows} seeded query rows of the 128K workload, all {cfg.H_kv} groups: "
                           f"index top-k, forward, backward in float64 ({dt:.1f} s)")}
 
+    # ---- every other seeded workload: the same step timed on its own inputs ----
+    workloads = {cfg.name: workload_summary(cfg, r, peak_tf)}
+    others = [] if (args.no_workloads or world > 1) else [n for n in WORKLOAD_ORDER
+                                                          if n != cfg.name]
+    if others:
+        del d, host
+        for n in others:
+            torch.cuda.empty_cache()
+            wc = synth.CONFIGS[n]
+            hw = synth.make_inputs(wc)
+            dw = {x: to_dev(hw[x]) for x in names}
+            del hw
+            rw = timed_workload(torch, ops, _lib, wc, dw, stream, WORKLOAD_STEPS[n], args.warmup)
+            workloads[n] = workload_summary(wc, rw, peak_tf)
+            del dw
+        ops.release_workspace()
+        torch.cuda.empty_cache()
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_name(cfg), "global_batch": cfg.B * world,
-                       "seq_len": cfg.N, "parallelism": f"replicas x{world}",
+            "scaling": "strong", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_name(full_cfg), "global_batch": full_cfg.B,
+                       "seq_len": full_cfg.N,
+                       "parallelism": (f"group-sharded x{world} ({cfg.H_kv} of {full_cfg.H_kv} "
+                                       "GQA groups per rank, all-reduce of dk_idx and KL)")
+                       if world > 1 else "1 GPU",
                        "l2": "inputs larger than L2 (q and dO are 1.07 GB each)"},
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf,
                          "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
@@ -516,6 +602,7 @@ def run_ours(args, cfg, rank, world):
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": 4, "steps": e2e_steps},
             "cpu_baseline": cpu,
+            "workloads": {n: workloads[n] for n in WORKLOAD_ORDER if n in workloads},
             "decode": dec,
             "indexer_warmup": wu,
             "gpu_launches": launches,
@@ -535,6 +622,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=1400)
     ap.add_argument("--ref-rows", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time only the --config workload (skip the other four)")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode leg")
     ap.add_argument("--decode-only", action="store_true",
                     help="run only the decode leg and print its JSON object")

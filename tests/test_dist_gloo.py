@@ -2,13 +2,15 @@
 
 1. bench.job_rate: each rank gets the slowest rank's time and the whole-job rate
    (units of all ranks / max time), as the benchmark's torchrun mode reports it.
-2. Group sharding.  Every GQA group's selection, forward and main backward are
-   independent; the groups share only k_idx, whose gradient sums over groups
-   (MSA summary, 7minutos.es, "Cómo funcionan las dos ramas" ¶1: one shared
-   index-key head).  So a run split by group across ranks needs one exchange: an
-   all-reduce (sum) of dk_idx and of the KL.  Here rank r runs the oracle on group r
-   alone, the ranks all-reduce dk_idx and KL over gloo, and the result must equal
-   the unsharded oracle run; every other output must equal its group's slice.
+2. Group sharding (block_sparse_gqa_topk_gb300.shard).  Every GQA group's selection,
+   forward and main backward are independent; the groups share only k_idx, whose
+   gradient sums over groups (MSA summary, 7minutos.es, "Cómo funcionan las dos
+   ramas" ¶1: one shared index-key head).  So a run split by group across ranks needs
+   one exchange: an all-reduce (sum) of dk_idx and of the KL.  The product's
+   sharded_step slices each rank's groups and runs the exchange over gloo; the
+   per-rank step is injected (the oracle on CPU, where the library would run on a
+   GPU).  The result must equal the unsharded oracle run; every other output must
+   equal its group's slice.
 """
 import os
 import socket
@@ -78,58 +80,98 @@ def test_job_rate_takes_the_slowest_rank():
 
 
 # ---------------------------------------------------------------- group sharding
-def _group_slice(inputs, cfg, g):
-    G = cfg.H_q // cfg.H_kv
-    return {
-        "q": np.ascontiguousarray(inputs["q"][:, :, g * G:(g + 1) * G]),
-        "dO": np.ascontiguousarray(inputs["dO"][:, :, g * G:(g + 1) * G]),
-        "k": np.ascontiguousarray(inputs["k"][:, :, g:g + 1]),
-        "v": np.ascontiguousarray(inputs["v"][:, :, g:g + 1]),
-        "q_idx": np.ascontiguousarray(inputs["q_idx"][:, :, g:g + 1]),
-        "k_idx": inputs["k_idx"],
-    }
+SHARD3 = dict(SHARD, name="shard3", H_q=12, H_kv=3, seed=33, needle_seed=34)
+
+
+def _oracle_compute(cfg):
+    """The per-rank step of shard.sharded_step, computed by the oracle on the rank's
+    slice (bf16 bits carried in int16 tensors), in place of the library on a GPU."""
+    import torch
+    import oracle
+
+    def compute(x, topk, scale, w):
+        ng = x["k"].shape[2]
+        scfg = cfg.with_(H_q=ng * cfg.G, H_kv=ng)
+        h = {n: np.ascontiguousarray(x[n].numpy().view(np.uint16)) for n in x}
+        bi, _, _ = oracle.select(scfg, h)
+        g = oracle.backward(scfg, h, bi, w)
+        out = {n: g[n] for n in ("dq", "dk", "dv", "dq_idx")}
+        out["block_idx"] = bi
+        out["dk_idx"] = torch.from_numpy(np.ascontiguousarray(g["dk_idx"]))
+        out["kl"] = torch.tensor(g["kl"], dtype=torch.float64)
+        out["kl_local"] = g["kl"]
+        return out
+
+    return compute
+
+
+def _shard_job_for(spec):
+    def job(rank, world):
+        import torch
+        from block_sparse_gqa_topk_gb300 import shard, synth
+        cfg = synth.MSAConfig(**spec)
+        host = synth.make_inputs(cfg)
+        full = {n: torch.from_numpy(host[n].view(np.int16)) for n in host}
+        sh = shard.GroupShard(rank, world, cfg.H_kv)
+        out = shard.sharded_step(sh, full, cfg.topk, scale=cfg.scale, kl_coef=cfg.kl_coef,
+                                 compute=_oracle_compute(cfg))
+        out["groups"] = sh.groups
+        out["dk_idx"] = out["dk_idx"].numpy()
+        out["kl"] = float(out["kl"])
+        return out
+    return job
 
 
 def _shard_job(rank, world):
-    import torch
-    import torch.distributed as dist
-    import oracle
-    from block_sparse_gqa_topk_gb300 import synth
-    cfg = synth.MSAConfig(**SHARD)
-    w = cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N)
-    inputs = synth.make_inputs(cfg)
-    scfg = cfg.with_(H_q=cfg.G, H_kv=1)  # this rank's group alone
-    sl = _group_slice(inputs, cfg, rank)
-    bi, _, _ = oracle.select(scfg, sl)
-    g = oracle.backward(scfg, sl, bi, w)
-    dki = torch.from_numpy(np.ascontiguousarray(g["dk_idx"]))
-    kl = torch.tensor([g["kl"]], dtype=torch.float64)
-    dist.all_reduce(dki)  # the one exchange step
-    dist.all_reduce(kl)
-    return {"bi": bi, "dq": g["dq"], "dk": g["dk"], "dv": g["dv"], "dq_idx": g["dq_idx"],
-            "dk_idx": dki.numpy(), "kl": float(kl.item()), "kl_local": g["kl"]}
+    return _shard_job_for(SHARD)(rank, world)
 
 
-def test_group_sharded_oracle_with_dk_idx_allreduce_matches_unsharded():
+def _shard_job3(rank, world):
+    return _shard_job_for(SHARD3)(rank, world)
+
+
+@pytest.mark.parametrize("spec,job", [(SHARD, _shard_job), (SHARD3, _shard_job3)],
+                         ids=["2-groups", "3-groups-uneven"])
+def test_group_sharded_step_with_dk_idx_allreduce_matches_unsharded(spec, job):
+    """shard.sharded_step (the product's sharded mode) on two gloo ranks, with the
+    per-rank step computed by the oracle: every per-group output equals the unsharded
+    oracle's slice, and after the one all-reduce every rank holds the unsharded
+    dk_idx and KL."""
     import oracle
     from block_sparse_gqa_topk_gb300 import synth
     oracle.build()
-    cfg = synth.MSAConfig(**SHARD)
+    cfg = synth.MSAConfig(**spec)
     w = cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N)
     inputs = synth.make_inputs(cfg)
     bi, _, _ = oracle.select(cfg, inputs)
     full = oracle.backward(cfg, inputs, bi, w)
-    out = _run(_shard_job)
+    out = _run(job)
     G = cfg.G
-    for r in range(cfg.H_kv):
+    seen = []
+    for r in range(2):
         s = out[r]
-        np.testing.assert_array_equal(s["bi"][:, 0], bi[:, r])
-        np.testing.assert_allclose(s["dq"], full["dq"][:, r * G:(r + 1) * G], rtol=0, atol=1e-12)
-        np.testing.assert_allclose(s["dk"][:, :, 0], full["dk"][:, :, r], rtol=0, atol=1e-12)
-        np.testing.assert_allclose(s["dv"][:, :, 0], full["dv"][:, :, r], rtol=0, atol=1e-12)
-        np.testing.assert_allclose(s["dq_idx"][:, 0], full["dq_idx"][:, r], rtol=0, atol=1e-12)
-        # after the all-reduce every rank holds the unsharded dk_idx and KL
-        np.testing.assert_allclose(s["dk_idx"], full["dk_idx"], rtol=1e-12, atol=1e-15)
-        assert s["kl"] == pytest.approx(full["kl"], rel=1e-12)
-    # the exchange is needed: one group's share alone is not the answer
+        g0, g1 = s["groups"]
+        seen += list(range(g0, g1))
+        np.testing.assert_array_equal(s["block_idx"], bi[:, g0:g1])
+        np.testing.assert_allclose(s["dq"], full["dq"][:, g0 * G:g1 * G], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(s["dk"], full["dk"][:, :, g0:g1], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(s["dv"], full["dv"][:, :, g0:g1], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(s["dq_idx"], full["dq_idx"][:, g0:g1], rtol=0, atol=1e-12)
+        # the exchange sums in float32
+        scale = np.abs(full["dk_idx"]).max()
+        np.testing.assert_allclose(s["dk_idx"], full["dk_idx"], rtol=0, atol=1e-6 * scale)
+        assert s["kl"] == pytest.approx(full["kl"], rel=1e-6)
+    assert sorted(seen) == list(range(cfg.H_kv))  # every group owned exactly once
+    # the exchange is needed: one rank's share alone is not the answer
     assert abs(out[0]["kl_local"] - full["kl"]) > 1e-6 * abs(full["kl"])
+
+
+def test_group_ranges_cover_every_group_once():
+    from block_sparse_gqa_topk_gb300.shard import GroupShard
+    for H_kv in (1, 2, 3, 8, 13):
+        for world in (1, 2, 3, 4, 8):
+            rs = [GroupShard(r, world, H_kv).groups for r in range(world)]
+            assert rs[0][0] == 0 and rs[-1][1] == H_kv
+            assert all(a[1] == b[0] for a, b in zip(rs, rs[1:]))
+            sizes = [g1 - g0 for g0, g1 in rs]
+            assert max(sizes) - min(sizes) <= 1
