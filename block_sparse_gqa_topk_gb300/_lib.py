@@ -38,6 +38,8 @@ MSA_KERNEL_FWD = 1
 MSA_KERNEL_BWD = 2
 MSA_KERNEL_INDEX_LSE = 3
 
+MSA_DEBUG_WITHHOLD_LOAD = 1
+
 
 class Problem(ctypes.Structure):
     """msa_problem_t"""

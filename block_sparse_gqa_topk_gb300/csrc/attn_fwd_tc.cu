@@ -219,8 +219,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int qs = lane + 32 * m;
           my_ent[m] = qs < ne ? __ldg(&p.entries[e0 + qs]) : -1;
         }
-        for (int x = lt; x < 128 * CH; x += kLoadThreads) {
-          const int r = x / CH, ch = x % CH;
+        // Each thread copies one fixed 16-byte column (chf) of the rows r0, r0 + RS, ...:
+        // the per-copy work is a shuffle for the row's entry, one multiply-add for the
+        // source and the swizzled destination.
+        static_assert(kLoadThreads % CH == 0, "loader threads cover whole rows");
+        constexpr int RS = kLoadThreads / CH;  // rows per pass
+        const int chf = lt % CH;
+        const __nv_bfloat16* qg =
+            p.q + ((int64_t)b * p.N * p.H_kv * G + (int64_t)g * G) * D + chf * 8;
+        const int64_t qrow = (int64_t)p.H_kv * G * D;  // elements between consecutive queries
+        uint8_t* dcol = dq + (chf >> 3) * L::kHalf;
+#pragma unroll 4
+        for (int r = lt / CH; r < 128; r += RS) {
           const int qi = r / G, h = r % G;
           int ent = -1;
 #pragma unroll
@@ -230,8 +240,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           const bool ok = ent >= 0;
           const int i = ok ? (ent >> kSlotBits) : 0;
-          const int64_t src = (((int64_t)b * p.N + i) * p.H_kv * G + g * G + h) * D + ch * 8;
-          cp_async_16(dq + kmaj_off<D>(r, ch), p.q + src, ok);
+          cp_async_16(dcol + r * 128 + (((chf & 7) ^ (r & 7)) << 4), qg + i * qrow + h * D, ok);
         }
         cp_async_commit();
         if (u >= 1) {  // the previous tile's copies have landed: publish them

@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 8) {
     // ------------------------------ TMA producer ------------------------------
-    if (lane == 0 && !(p.debug & 1)) {
+    if (lane == 0 && !(p.debug & MSA_DEBUG_WITHHOLD_LOAD)) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       int kt = 0, qloads = 0;

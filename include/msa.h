@@ -231,9 +231,11 @@ int msa_get_device_status(cudaStream_t stream, int* status);
 const char* msa_status_string(int code);
 
 /* Test knob for the failure path, per process: the bounded device waits give up
- * after wait_limit_ns (0 restores the default of 2 s); flags bit 0 makes the next
- * index-top-k launches withhold their first TMA load, so the consumer's wait runs
- * out, the kernel records MSA_ERR_DEVICE_TIMEOUT and returns without hanging. */
+ * after wait_limit_ns (0 restores the default of 2 s); flags bit 0
+ * (MSA_DEBUG_WITHHOLD_LOAD) makes the next index-top-k launches withhold their first
+ * TMA load, so the consumer's wait runs out, the kernel records
+ * MSA_ERR_DEVICE_TIMEOUT and returns without hanging. */
+#define MSA_DEBUG_WITHHOLD_LOAD 1
 int msa_debug_set(uint64_t wait_limit_ns, int flags);
 
 /* Profiling hook.  Kernels: MSA_KERNEL_INDEX (the index scoring + top-k kernel of
