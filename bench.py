@@ -134,6 +134,53 @@ def decode_leg(torch, ops, d, cfg, dev, stream, hbm_peak, calls=20):
                     "achieved_gbs": gbs8, "frac": gbs8 / hbm_peak}}
 
 
+def fp8_forward_leg(torch, ops, _lib, d, cfg, stream, peak_tf, steps=5):
+    """FP8 (E4M3) training forward on the workload: the quantiser (q per row, k and v per
+    128-key block) and msa_fwd_fp8 over the step's block sets, each timed per call (CUDA
+    events, mean of `steps` after a warm-up call), with the tensor-core kernel alone timed
+    live, against msa_fwd (bf16) on the same sets.  The FP8 kernel's peak is the bf16
+    measured peak times the nominal 2x ratio of E4M3 to bf16 tensor throughput."""
+    bi, _ = ops.msa_index_topk(d["q_idx"], d["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d,
+                               with_lse=False)
+    torch.cuda.synchronize()
+    flops = algorithmic_flops(cfg, token_set_total(cfg, bi.cpu().numpy()))["fwd"]
+
+    def timed(fn, kernel_events):
+        fn()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        for e in ev:
+            for x in e:
+                x.record(stream)
+        torch.cuda.synchronize()
+        for e in ev:
+            if kernel_events:
+                _lib.msa_set_kernel_events(_lib.MSA_KERNEL_FWD, e[0].cuda_event, e[1].cuda_event)
+            e[2].record(stream)
+            fn()
+            e[3].record(stream)
+        torch.cuda.synchronize()
+        _lib.msa_set_kernel_events(_lib.MSA_KERNEL_FWD, None, None)
+        call = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+        kern = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) if kernel_events else None
+        return call, kern
+
+    bf_call, bf_kern = timed(lambda: ops.msa_fwd(d["q"], d["k"], d["v"], bi, scale=cfg.scale,
+                                                 d_idx=cfg.d_idx), True)
+    ops8 = ops.msa_quantize_fwd_fp8(d["q"], d["k"], d["v"])
+    q_call, _ = timed(lambda: ops.msa_quantize_fwd_fp8(d["q"], d["k"], d["v"]), False)
+    f8_call, f8_kern = timed(lambda: ops.msa_fwd_fp8(*ops8, bi, scale=cfg.scale,
+                                                     d_idx=cfg.d_idx), True)
+    del ops8, bi
+    tf8 = flops / (f8_kern / 1000.0) / 1e12
+    return {"recipe": "E4M3; q one scale per (token, head) row, k and v one per 128-key block; "
+                      "P rounded to E4M3 against the block's exact max",
+            "ms_quantize": q_call, "ms_forward_call": f8_call, "ms_forward_kernel": f8_kern,
+            "bf16_ms_forward_call": bf_call, "bf16_ms_forward_kernel": bf_kern,
+            "kernel_tflops": tf8, "peak_tflops": 2.0 * peak_tf,
+            "peak_source": "bf16_tflops_sustained x 2 (nominal E4M3 / bf16 ratio)",
+            "frac": tf8 / (2.0 * peak_tf), "steps": steps}
+
+
 def warmup_leg(torch, ops, cfg, dev, stream, peak_tf, steps=5, warm=3):
     """Indexer warm-up (dense set, topk >= nb): the workload's heads at N = 16384 with
     topk = 128 = nb, so both branches attend every visible token and the KL runs over
@@ -547,6 +594,14 @@ def run_ours(args, cfg, rank, world):
         dec = decode_leg(torch, ops, d, cfg, dev, stream,
                          float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))
 
+    # ---- FP8 (E4M3) training forward leg ----
+    f8 = None
+    if not args.no_fp8_leg and world == 1:
+        f8 = fp8_forward_leg(torch, ops, _lib, d, cfg, stream, peak_tf)
+        st = ops.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status after the FP8 leg: {_lib.status_string(st)}")
+
     # ---- indexer warm-up leg (dense set) ----
     wu = None
     if not args.no_warmup_leg and world == 1:
@@ -604,6 +659,7 @@ def run_ours(args, cfg, rank, world):
             "cpu_baseline": cpu,
             "workloads": {n: workloads[n] for n in WORKLOAD_ORDER if n in workloads},
             "decode": dec,
+            "fp8_forward": f8,
             "indexer_warmup": wu,
             "gpu_launches": launches,
             "clocks": clk,
@@ -627,6 +683,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode leg")
     ap.add_argument("--decode-only", action="store_true",
                     help="run only the decode leg and print its JSON object")
+    ap.add_argument("--no-fp8-leg", action="store_true",
+                    help="skip the FP8 (E4M3) forward leg")
     ap.add_argument("--no-warmup-leg", action="store_true",
                     help="skip the indexer warm-up (dense set) leg")
     ap.add_argument("--warmup-only", action="store_true",

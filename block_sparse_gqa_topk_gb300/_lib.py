@@ -31,7 +31,7 @@ EXPORTS = ("msa_workspace_size", "msa_index_topk", "msa_fwd", "msa_bwd",
            "msa_noalloc_scratch_bytes", "msa_version", "msa_workspace_size_varlen",
            "msa_index_topk_varlen", "msa_fwd_varlen", "msa_bwd_varlen",
            "msa_decode_workspace_size", "msa_decode", "msa_quantize_kv_fp8",
-           "msa_decode_fp8")
+           "msa_decode_fp8", "msa_quantize_fwd_fp8", "msa_fwd_fp8")
 
 MSA_KERNEL_INDEX = 0
 MSA_KERNEL_FWD = 1
@@ -110,6 +110,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_quantize_kv_fp8.restype = i32
     lib.msa_decode_fp8.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.msa_decode_fp8.restype = i32
+    lib.msa_quantize_fwd_fp8.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.msa_quantize_fwd_fp8.restype = i32
+    lib.msa_fwd_fp8.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.msa_fwd_fp8.restype = i32
     _lib = lib
     return lib
 
@@ -221,6 +225,17 @@ def msa_decode_fp8(prob, q, q_idx, k8, v8, k_scale, v_scale, k_idx, lens, block_
                    ws_bytes, stream) -> int:
     return load().msa_decode_fp8(ctypes.byref(prob), q, q_idx, k8, v8, k_scale, v_scale, k_idx,
                                  lens, block_idx, o, lse, ws, ws_bytes, stream)
+
+
+def msa_quantize_fwd_fp8(prob, q, k, v, q8, q_scale, k8, k_scale, v8t, v_scale, stream) -> int:
+    return load().msa_quantize_fwd_fp8(ctypes.byref(prob), q, k, v, q8, q_scale, k8, k_scale, v8t,
+                                       v_scale, stream)
+
+
+def msa_fwd_fp8(prob, q8, q_scale, k8, k_scale, v8t, v_scale, block_idx, o, lse, ws, ws_bytes,
+                stream) -> int:
+    return load().msa_fwd_fp8(ctypes.byref(prob), q8, q_scale, k8, k_scale, v8t, v_scale, block_idx,
+                              o, lse, ws, ws_bytes, stream)
 
 
 def msa_version() -> int:

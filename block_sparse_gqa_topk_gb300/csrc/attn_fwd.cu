@@ -195,6 +195,12 @@ cudaError_t launch_attn_fwd(const Shape& s, const void* q, const void* k, const 
                             cudaStream_t st) {
   cudaError_t e = launch_attn_fwd_tc(s, q, k, v, pl, o_part, lse_part, cx, st);
   if (e != cudaSuccess) return e;
+  return launch_attn_fwd_combine(s, block_idx, o_part, lse_part, o, lse, st);
+}
+
+cudaError_t launch_attn_fwd_combine(const Shape& s, const int32_t* block_idx,
+                                    const __nv_bfloat16* o_part, const float* lse_part, void* o,
+                                    float* lse, cudaStream_t st) {
   const unsigned grid = (unsigned)((s.rows_kv() + 7) / 8);
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
 #define MSA_COMBINE(DD, GG)                                                                   \

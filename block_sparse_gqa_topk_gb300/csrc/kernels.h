@@ -68,6 +68,20 @@ cudaError_t launch_attn_fwd(const Shape& s, const void* q, const void* k, const 
                             float* lse_part, void* o, float* lse, const Ctx& cx,
                             cudaStream_t st);
 
+// Per-row merge of the forward's slot partials into o and lse.
+cudaError_t launch_attn_fwd_combine(const Shape& s, const int32_t* block_idx,
+                                    const __nv_bfloat16* o_part, const float* lse_part, void* o,
+                                    float* lse, cudaStream_t st);
+
+// FP8 (E4M3) forward, d = 128: per-block quantiser of k (layout kept) or v (transposed
+// per block, v8t [B][H_kv][nb][d][128]) and the tcgen05 kind::f8f6f4 partials kernel.
+cudaError_t launch_quantize_blocks_fp8(const Shape& s, const void* x, uint8_t* x8, float* scale,
+                                       bool transpose, cudaStream_t st);
+cudaError_t launch_attn_fwd_fp8_tc(const Shape& s, const uint8_t* q8, const float* q_scale,
+                                   const uint8_t* k8, const float* k_scale, const uint8_t* v8t,
+                                   const float* v_scale, const Plan& pl, __nv_bfloat16* o_part,
+                                   float* lse_part, const Ctx& cx, cudaStream_t st);
+
 // tcgen05 gathered forward kernel (partials only; launch_attn_fwd adds the combine).
 cudaError_t launch_attn_fwd_tc(const Shape& s, const void* q, const void* k, const void* v,
                                const Plan& pl, __nv_bfloat16* o_part, float* lse_part,

@@ -354,3 +354,65 @@ def msa_decode_fp8(q, q_idx, k8, v8, k_scale, v_scale, k_idx, lens, topk: int = 
                              _ptr(lse), _ptr(ws), nws, _stream(dev))
     _lib.check(rc, "msa_decode_fp8")
     return block_idx, o, lse
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) main-branch forward for training (d = 128); see include/msa.h.
+# ---------------------------------------------------------------------------
+def msa_quantize_fwd_fp8(q, k, v, *, Bk: int = 128):
+    """bf16 q [B,N,H_q,d], k, v [B,N,H_kv,d] -> the FP8 forward's operands:
+    q8 [B,N,H_q,d] uint8 + q_scale [B,N,H_q] (one scale per row), k8 [B,N,H_kv,d] +
+    k_scale [B,H_kv,nb] and v8t [B,H_kv,nb,d,Bk] (v transposed per block) + v_scale
+    [B,H_kv,nb] (one scale per Bk-key block)."""
+    _need(q, "q", ndim=4)
+    _need(k, "k", ndim=4)
+    _need(v, "v", ndim=4)
+    B, N, H_q, d = q.shape
+    H_kv = k.shape[2]
+    if tuple(k.shape) != (B, N, H_kv, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k, v must be [B, N, H_kv, d] with q's B, N, d")
+    nb = (N + Bk - 1) // Bk
+    prob = make_problem(B, N, H_q, H_kv, d, 64, 1, Bk, True, None, None)
+    dev = q.device
+    q8 = torch.empty(q.shape, dtype=torch.uint8, device=dev)
+    q_scale = torch.empty((B, N, H_q), dtype=torch.float32, device=dev)
+    k8 = torch.empty(k.shape, dtype=torch.uint8, device=dev)
+    k_scale = torch.empty((B, H_kv, nb), dtype=torch.float32, device=dev)
+    v8t = torch.empty((B, H_kv, nb, d, Bk), dtype=torch.uint8, device=dev)
+    v_scale = torch.empty((B, H_kv, nb), dtype=torch.float32, device=dev)
+    rc = _lib.msa_quantize_fwd_fp8(prob, _ptr(q), _ptr(k), _ptr(v), _ptr(q8), _ptr(q_scale),
+                                   _ptr(k8), _ptr(k_scale), _ptr(v8t), _ptr(v_scale), _stream(dev))
+    _lib.check(rc, "msa_quantize_fwd_fp8")
+    return q8, q_scale, k8, k_scale, v8t, v_scale
+
+
+def msa_fwd_fp8(q8, q_scale, k8, k_scale, v8t, v_scale, block_idx, *, scale=None, Bk: int = 128,
+                d_idx: int = 64):
+    """FP8 forward over the operands of msa_quantize_fwd_fp8 and the block sets
+    block_idx [B,H_kv,N,topk]: returns (o [B,N,H_q,d] bf16, lse [B,H_q,N] f32)."""
+    _need(q8, "q8", torch.uint8, ndim=4)
+    _need(k8, "k8", torch.uint8, ndim=4)
+    _need(v8t, "v8t", torch.uint8, ndim=5)
+    _need(q_scale, "q_scale", torch.float32, ndim=3)
+    _need(k_scale, "k_scale", torch.float32, ndim=3)
+    _need(v_scale, "v_scale", torch.float32, ndim=3)
+    _need(block_idx, "block_idx", torch.int32, ndim=4)
+    B, N, H_q, d = q8.shape
+    H_kv = k8.shape[2]
+    topk = block_idx.shape[3]
+    nb = (N + Bk - 1) // Bk
+    if (tuple(k8.shape) != (B, N, H_kv, d) or tuple(v8t.shape) != (B, H_kv, nb, d, Bk)
+            or tuple(q_scale.shape) != (B, N, H_q) or tuple(k_scale.shape) != (B, H_kv, nb)
+            or tuple(v_scale.shape) != (B, H_kv, nb) or tuple(block_idx.shape[:3]) != (B, H_kv, N)):
+        raise ValueError("operand shapes must be those of msa_quantize_fwd_fp8")
+    prob = make_problem(B, N, H_q, H_kv, d, d_idx, topk, Bk, True, scale, None)
+    dev = q8.device
+    o = torch.empty((B, N, H_q, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H_q, N), dtype=torch.float32, device=dev)
+    nws = _lib.msa_workspace_size(prob, _lib.MSA_WS_FWD)
+    ws = _workspace(nws, dev)
+    rc = _lib.msa_fwd_fp8(prob, _ptr(q8), _ptr(q_scale), _ptr(k8), _ptr(k_scale), _ptr(v8t),
+                          _ptr(v_scale), _ptr(block_idx), _ptr(o), _ptr(lse), _ptr(ws), nws,
+                          _stream(dev))
+    _lib.check(rc, "msa_fwd_fp8")
+    return o, lse

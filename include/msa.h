@@ -223,6 +223,33 @@ int msa_decode_fp8(const msa_problem_t* p, const void* q, const void* q_idx, con
                    const int32_t* lens, int32_t* block_idx, void* o, float* lse, void* workspace,
                    size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * FP8 (E4M3) main-branch forward for training (d = 128): the same block-sparse
+ * attention as msa_fwd with E4M3 operands on the tensor cores.  The pages list FP8
+ * among the precisions of the MSA attention kernels ("El codiseño del kernel",
+ * fmha_sm100 paragraph) without a recipe; this build takes:
+ *   q8 [B][N][H_q][d] codes, q_scale [B][N][H_q]: one scale per (token, head) row;
+ *   k8 [B][N][H_kv][d] codes, k_scale [B][H_kv][nb]: one scale per 128-key block;
+ *   v8t [B][H_kv][nb][d][128] codes (v transposed within each block, keys past N
+ *       zero), v_scale [B][H_kv][nb]: one scale per block;
+ *   scale = amax / 448 over the row or block (1 if all zero), code = E4M3 nearest to
+ *   float32(x / scale), ties to even, saturating (the KV-cache quantiser's rule);
+ *   scores s_q s_k (q8 . k8) * scale, exact row max, P = exp(score - max) rounded to
+ *   E4M3 for the P V product, l = sum of the unrounded P,
+ *   o = s_v (P8 . v8) / l (bf16), lse = max + log l (float32).
+ * msa_quantize_fwd_fp8 writes q8, q_scale, k8, k_scale, v8t, v_scale from bf16 q, k, v
+ * (p->d must be 128); msa_fwd_fp8 takes them with the block sets and writes o, lse,
+ * using a workspace of msa_workspace_size(p, MSA_WS_FWD) bytes.  Pointers 16-byte
+ * aligned, outputs overwritten; errors as msa_fwd (MSA_ERR_UNSUPPORTED for d != 128).
+ */
+int msa_quantize_fwd_fp8(const msa_problem_t* p, const void* q, const void* k, const void* v,
+                         uint8_t* q8, float* q_scale, uint8_t* k8, float* k_scale, uint8_t* v8t,
+                         float* v_scale, cudaStream_t stream);
+int msa_fwd_fp8(const msa_problem_t* p, const uint8_t* q8, const float* q_scale, const uint8_t* k8,
+                const float* k_scale, const uint8_t* v8t, const float* v_scale,
+                const int32_t* block_idx, void* o, float* lse, void* workspace,
+                size_t workspace_bytes, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status word
  * (MSA_OK or the first MSA_ERR_* a kernel recorded since the last read). */
 int msa_get_device_status(cudaStream_t stream, int* status);

@@ -143,3 +143,22 @@ def test_product_code_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "liboracle" not in text and "msa_oracle" not in text, f
+
+
+def test_fp8_forward_entry_points_check_arguments_on_the_host():
+    """The FP8 training forward takes d = 128 only and rejects null or misaligned
+    pointers before anything is enqueued."""
+    lib = _lib.load()
+    p64 = _prob()  # d = 64
+    p128 = _prob(d=128, d_idx=64)
+    z = None
+    assert lib.msa_quantize_fwd_fp8(ctypes.byref(p64), 256, 256, 256, 256, 256, 256, 256, 256,
+                                    256, None) == _lib.MSA_ERR_UNSUPPORTED
+    assert lib.msa_quantize_fwd_fp8(ctypes.byref(p128), z, 256, 256, 256, 256, 256, 256, 256,
+                                    256, None) == _lib.MSA_ERR_ARG
+    assert lib.msa_fwd_fp8(ctypes.byref(p64), 256, 256, 256, 256, 256, 256, 256, 256, 256, 256,
+                           1 << 20, None) == _lib.MSA_ERR_UNSUPPORTED
+    assert lib.msa_fwd_fp8(ctypes.byref(p128), 256, 256, 264, 256, 256, 256, 256, 256, 256, 256,
+                           1 << 20, None) == _lib.MSA_ERR_ARG  # k8 not 16-byte aligned
+    assert lib.msa_fwd_fp8(ctypes.byref(p128), 256, 256, 256, 256, 256, 256, 256, 256, 256, 256,
+                           16, None) == _lib.MSA_ERR_WORKSPACE
