@@ -221,6 +221,64 @@ def warmup_leg(torch, ops, cfg, dev, stream, peak_tf, steps=5, warm=3):
             "frac": tf / peak_tf, "steps": steps}
 
 
+def varlen_leg(torch, ops, _lib, d, cfg, stream, peak_tf, steps=5, warm=3):
+    """Packed variable-length batch over the workload's token axis and heads: 32
+    sequences whose seeded lengths are log-uniform in 512 .. 16384 tokens, scaled to fill
+    the B*N tokens exactly (cu_seqlens on the device).  One step = index call (+ lse_idx),
+    forward, backward through the packed entry points; mean device time over `steps`
+    steps after `warm` untimed ones.  Algorithmic work = the sum of every sequence's own
+    work (each is its own causal problem)."""
+    T = cfg.B * cfg.N
+    cu = synth.varlen_offsets_total(32, T, 512, 16384, seed=55)
+    lens = [b - a for a, b in zip(cu, cu[1:])]
+    L = max(lens)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=d["q"].device)
+    t = {n: d[n].reshape((T,) + tuple(d[n].shape[2:])) for n in d}
+    w = cfg.kl_coef / (cfg.H_kv * T)
+    k = cfg.topk
+
+    def step():
+        bi, li = ops.msa_index_topk_varlen(t["q_idx"], t["k_idx"], cu_t, k, max_seqlen=L,
+                                           H_q=cfg.H_q, d=cfg.d)
+        o, lse = ops.msa_fwd_varlen(t["q"], t["k"], t["v"], bi, cu_t, k, max_seqlen=L,
+                                    scale=cfg.scale, d_idx=cfg.d_idx)
+        g = ops.msa_bwd_varlen(t["q"], t["k"], t["v"], o, lse, t["dO"], t["q_idx"], t["k_idx"], bi,
+                               li, w, cu_t, k, max_seqlen=L, scale=cfg.scale)
+        return bi, g
+
+    for _ in range(warm):
+        bi, _ = step()
+    torch.cuda.synchronize()
+    bi_h = bi.cpu().numpy()
+    flops = {"index": 0, "index_lse": 0, "fwd": 0, "bwd": 0}
+    for s, n in enumerate(lens):
+        if n == 0:
+            continue
+        cs = cfg.with_(B=1, N=n)
+        view = bi_h[cu[s] * cfg.H_kv * k:cu[s + 1] * cfg.H_kv * k].reshape(1, cfg.H_kv, n, k)
+        for key, v in algorithmic_flops(cs, token_set_total(cs, view)).items():
+            flops[key] += v
+    n0 = _lib.msa_kernel_launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = (_lib.msa_kernel_launch_count() - n0) // steps
+    ms = e0.elapsed_time(e1) / steps
+    total = sum(flops.values())
+    tf = total / (ms / 1000.0) / 1e12
+    return {"workload": (f"packed batch of {len(lens)} sequences ({min(lens)} .. {L} tokens, "
+                         f"log-uniform, seed 55) filling {T} tokens; H_q={cfg.H_q} "
+                         f"H_kv={cfg.H_kv} d={cfg.d} d_idx={cfg.d_idx} k={k}"),
+            "num_seqs": len(lens), "max_seqlen": L, "ms_per_step": ms,
+            "tokens_per_s": T / (ms / 1000.0), "launches_per_step": launches,
+            "algorithmic_tflop_per_step": total / 1e12, "tflops": tf, "peak_tflops": peak_tf,
+            "frac": tf / peak_tf, "steps": steps}
+
+
 # ----------------------------------------------------------------------------
 # algorithmic work (what the method must compute, not what a kernel happens to do)
 # ----------------------------------------------------------------------------
@@ -489,6 +547,16 @@ def run_ours(args, cfg, rank, world):
         if rank == 0:
             print(json.dumps({"indexer_warmup": wu}), flush=True)
         return
+    if args.varlen_only:  # the packed variable-length leg alone
+        peaks, _ = load_peaks()
+        vl = varlen_leg(torch, ops, _lib, d, cfg, stream, float(
+            peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])))
+        if ops.device_status() != 0:
+            raise RuntimeError("device status after the varlen leg: "
+                               + _lib.status_string(ops.device_status()))
+        if rank == 0:
+            print(json.dumps({"varlen": vl}), flush=True)
+        return
     if args.decode_only:  # the decode leg alone (e.g. for a profiler's launch list)
         peaks, _ = load_peaks()
         dec = decode_leg(torch, ops, d, cfg, dev, stream,
@@ -602,6 +670,14 @@ def run_ours(args, cfg, rank, world):
         if st != 0:
             raise RuntimeError(f"device status after the FP8 leg: {_lib.status_string(st)}")
 
+    # ---- packed variable-length batch leg ----
+    vl = None
+    if not args.no_varlen_leg and world == 1:
+        vl = varlen_leg(torch, ops, _lib, d, cfg, stream, peak_tf)
+        st = ops.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status after the varlen leg: {_lib.status_string(st)}")
+
     # ---- indexer warm-up leg (dense set) ----
     wu = None
     if not args.no_warmup_leg and world == 1:
@@ -660,6 +736,7 @@ def run_ours(args, cfg, rank, world):
             "workloads": {n: workloads[n] for n in WORKLOAD_ORDER if n in workloads},
             "decode": dec,
             "fp8_forward": f8,
+            "varlen": vl,
             "indexer_warmup": wu,
             "gpu_launches": launches,
             "clocks": clk,
@@ -687,6 +764,10 @@ def main():
                     help="skip the FP8 (E4M3) forward leg")
     ap.add_argument("--no-warmup-leg", action="store_true",
                     help="skip the indexer warm-up (dense set) leg")
+    ap.add_argument("--no-varlen-leg", action="store_true",
+                    help="skip the packed variable-length batch leg")
+    ap.add_argument("--varlen-only", action="store_true",
+                    help="run only the packed variable-length leg and print its JSON object")
     ap.add_argument("--warmup-only", action="store_true",
                     help="run only the indexer warm-up leg and print its JSON object")
     args = ap.parse_args()

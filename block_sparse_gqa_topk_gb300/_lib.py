@@ -92,15 +92,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_noalloc_scratch_bytes.restype = sz
     lib.msa_version.argtypes = []
     lib.msa_version.restype = i32
-    ip = ctypes.POINTER(ctypes.c_int32)
-    lib.msa_workspace_size_varlen.argtypes = [P, ip, i32, i32]
+    lib.msa_workspace_size_varlen.argtypes = [P, i32, i32, i32]
     lib.msa_workspace_size_varlen.restype = sz
-    lib.msa_index_topk_varlen.argtypes = [P, ip, i32, vp, vp, vp, vp, vp, sz, vp]
+    lib.msa_index_topk_varlen.argtypes = [P, vp, i32, i32, vp, vp, vp, vp, vp, sz, vp]
     lib.msa_index_topk_varlen.restype = i32
-    lib.msa_fwd_varlen.argtypes = [P, ip, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.msa_fwd_varlen.argtypes = [P, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.msa_fwd_varlen.restype = i32
-    lib.msa_bwd_varlen.argtypes = [P, ip, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp,
-                                   vp, vp, vp, vp, vp, sz, vp]
+    lib.msa_bwd_varlen.argtypes = [P, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, vp,
+                                   vp, vp, vp, vp, vp, vp, sz, vp]
     lib.msa_bwd_varlen.restype = i32
     lib.msa_decode_workspace_size.argtypes = [P]
     lib.msa_decode_workspace_size.restype = sz
@@ -176,36 +175,29 @@ def msa_kernel_launch_count() -> int:
     return int(load().msa_kernel_launch_count())
 
 
-def _cu(cu_seqlens):
-    """Host int32 array of the sequence offsets (kept alive by the caller's reference)."""
-    arr = (ctypes.c_int32 * len(cu_seqlens))(*[int(x) for x in cu_seqlens])
-    return arr, len(cu_seqlens) - 1
+def msa_workspace_size_varlen(prob: Problem, num_seqs: int, total_tokens: int, which: int) -> int:
+    return int(load().msa_workspace_size_varlen(ctypes.byref(prob), num_seqs, total_tokens, which))
 
 
-def msa_workspace_size_varlen(prob: Problem, cu_seqlens, which: int) -> int:
-    arr, n = _cu(cu_seqlens)
-    return int(load().msa_workspace_size_varlen(ctypes.byref(prob), arr, n, which))
+def msa_index_topk_varlen(prob, cu_seqlens, num_seqs, total_tokens, q_idx, k_idx, block_idx,
+                          lse_idx, ws, ws_bytes, stream) -> int:
+    """cu_seqlens: device pointer to num_seqs + 1 int32."""
+    return load().msa_index_topk_varlen(ctypes.byref(prob), cu_seqlens, num_seqs, total_tokens,
+                                        q_idx, k_idx, block_idx, lse_idx, ws, ws_bytes, stream)
 
 
-def msa_index_topk_varlen(prob, cu_seqlens, q_idx, k_idx, block_idx, lse_idx, ws, ws_bytes,
-                          stream) -> int:
-    arr, n = _cu(cu_seqlens)
-    return load().msa_index_topk_varlen(ctypes.byref(prob), arr, n, q_idx, k_idx, block_idx,
-                                        lse_idx, ws, ws_bytes, stream)
+def msa_fwd_varlen(prob, cu_seqlens, num_seqs, total_tokens, q, k, v, block_idx, o, lse, ws,
+                   ws_bytes, stream) -> int:
+    return load().msa_fwd_varlen(ctypes.byref(prob), cu_seqlens, num_seqs, total_tokens, q, k, v,
+                                 block_idx, o, lse, ws, ws_bytes, stream)
 
 
-def msa_fwd_varlen(prob, cu_seqlens, q, k, v, block_idx, o, lse, ws, ws_bytes, stream) -> int:
-    arr, n = _cu(cu_seqlens)
-    return load().msa_fwd_varlen(ctypes.byref(prob), arr, n, q, k, v, block_idx, o, lse, ws,
-                                 ws_bytes, stream)
-
-
-def msa_bwd_varlen(prob, cu_seqlens, q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx,
-                   kl_weight, dq, dk, dv, dq_idx, dk_idx, kl_out, ws, ws_bytes, stream) -> int:
-    arr, n = _cu(cu_seqlens)
-    return load().msa_bwd_varlen(ctypes.byref(prob), arr, n, q, k, v, o, lse, dO, q_idx, k_idx,
-                                 block_idx, lse_idx, float(kl_weight), dq, dk, dv, dq_idx, dk_idx,
-                                 kl_out, ws, ws_bytes, stream)
+def msa_bwd_varlen(prob, cu_seqlens, num_seqs, total_tokens, q, k, v, o, lse, dO, q_idx, k_idx,
+                   block_idx, lse_idx, kl_weight, dq, dk, dv, dq_idx, dk_idx, kl_out, ws, ws_bytes,
+                   stream) -> int:
+    return load().msa_bwd_varlen(ctypes.byref(prob), cu_seqlens, num_seqs, total_tokens, q, k, v, o,
+                                 lse, dO, q_idx, k_idx, block_idx, lse_idx, float(kl_weight), dq, dk,
+                                 dv, dq_idx, dk_idx, kl_out, ws, ws_bytes, stream)
 
 
 def msa_decode_workspace_size(prob: Problem) -> int:

@@ -26,28 +26,31 @@
 namespace msa {
 namespace {
 
-// D[b,h,i] = dO[b,i,h,:] . o[b,i,h,:].  One CTA per 64 consecutive queries i of one
-// (b, h): TPR = D / 8 threads per row (16-byte loads), every pass's loads issued before
-// the sums, and D written along i.
+// D[b,h,i] = dO[b,i,h,:] . o[b,i,h,:] (layout of lse: t0*H_q + h*len + i).  One CTA per
+// 64 consecutive queries i of one (b, h): TPR = D / 8 threads per row (16-byte loads),
+// every pass's loads issued before the sums, and D written along i.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO,
-                                                      float* __restrict__ Dv, int N, int H_q) {
+                                                      float* __restrict__ Dv,
+                                                      const int2* __restrict__ spans,
+                                                      const int* __restrict__ tab, int B, int N,
+                                                      int H_q) {
   constexpr int TPR = D / 8;      // threads per row
   constexpr int RPP = 256 / TPR;  // rows per pass
   constexpr int NP = 64 / RPP;    // passes
-  const int chunks = (N + 63) / 64;
-  const int64_t bh = blockIdx.x / chunks;  // b * H_q + h
-  const int i0 = (int)(blockIdx.x % chunks) * 64;
-  const int h = (int)(bh % H_q);
-  const int64_t b = bh / H_q;
+  const int h = blockIdx.x % H_q;
+  int b, chunk;
+  if (!chunk_item(tab, B, (N + 63) / 64, blockIdx.x / H_q, &b, &chunk)) return;
+  const SeqSpan sp = seq_span(spans, b, N);
+  const int i0 = chunk * 64;
   const int t = threadIdx.x % TPR, rr = threadIdx.x / TPR;
   uint4 xa[NP], xb[NP];
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
     const int i = i0 + q * RPP + rr;
-    if (i < N) {
-      const int64_t off = ((b * N + i) * H_q + h) * D + t * 8;
+    if (i < sp.len) {
+      const int64_t off = ((sp.t0 + i) * H_q + h) * D + t * 8;
       xa[q] = __ldg(reinterpret_cast<const uint4*>(o + off));
       xb[q] = __ldg(reinterpret_cast<const uint4*>(dO + off));
     } else {
@@ -66,7 +69,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     const int i = i0 + q * RPP + rr;
-    if (t == 0 && i < N) Dv[bh * N + i] = s;
+    if (t == 0 && i < sp.len) Dv[sp.t0 * H_q + (int64_t)h * sp.len + i] = s;
   }
 }
 
@@ -76,7 +79,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 template <int W, int G>
 __global__ void __launch_bounds__(256) slot_reduce_kernel(
     const __nv_bfloat16* __restrict__ part, const int32_t* __restrict__ block_idx,
-    __nv_bfloat16* __restrict__ out, int64_t rows_kv, int N, int H_kv, int topk, int nb) {
+    __nv_bfloat16* __restrict__ out, const int2* __restrict__ spans, int B, int64_t rows_kv,
+    int N, int H_kv, int topk, int nb) {
   constexpr int TC = G * W / 8;               // 16-byte chunks per row and slot
   constexpr int RPW = TC >= 32 ? 1 : 32 / TC; // rows per warp
   constexpr int CPL = TC >= 32 ? TC / 32 : 1; // chunks per lane
@@ -85,10 +89,10 @@ __global__ void __launch_bounds__(256) slot_reduce_kernel(
   const int64_t rkv = warp * RPW + (TC >= 32 ? 0 : lane / TC);
   const int l = TC >= 32 ? lane : lane % TC;
   if (rkv >= rows_kv) return;
-  const int i = (int)(rkv % N);
-  const int64_t bg = rkv / N;
-  const int g = (int)(bg % H_kv);
-  const int64_t b = bg / H_kv;
+  RowPos rp;
+  const bool valid = row_pos(spans, B, N, H_kv, rkv, &rp);  // tokens outside every sequence
+  if (!valid) return;
+  const int i = rp.i, g = rp.h;
   float acc[CPL][8];
 #pragma unroll
   for (int x = 0; x < CPL; ++x)
@@ -110,8 +114,8 @@ __global__ void __launch_bounds__(256) slot_reduce_kernel(
       }
     }
   }
-  // out row: dq [b][i][g*G .. g*G+G-1][W]  or  dq_idx [b][i][g][W]
-  uint4* dst = reinterpret_cast<uint4*>(out + ((b * N + i) * H_kv + g) * (int64_t)G * W);
+  // out row: dq [t0 + i][g*G .. g*G+G-1][W]  or  dq_idx [t0 + i][g][W]
+  uint4* dst = reinterpret_cast<uint4*>(out + ((rp.sp.t0 + i) * H_kv + g) * (int64_t)G * W);
 #pragma unroll
   for (int x = 0; x < CPL; ++x) {
     uint4 o;
@@ -122,15 +126,17 @@ __global__ void __launch_bounds__(256) slot_reduce_kernel(
   }
 }
 
-// dk_idx[b,j,:] = sum over groups of the per-group shares.
+// dk_idx[j,:] = sum over groups of the per-group shares (part [T][H_kv][DI], every token
+// of every sequence written by the tile kernel; tokens outside every sequence hold 0).
 __global__ void dki_reduce_kernel(const float* __restrict__ part, __nv_bfloat16* __restrict__ out,
-                                  int B, int N, int H_kv, int DI) {
+                                  const int2* __restrict__ spans, int B, int64_t T, int H_kv,
+                                  int DI) {
   const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  const int64_t per_b = (int64_t)N * DI;
-  if (t >= (int64_t)B * per_b) return;
-  const int64_t b = t / per_b, r = t - b * per_b;
+  if (t >= T * DI) return;
+  const int64_t j = t / DI, r = t - j * DI;
+  if (spans && j >= __ldg(&spans[B - 1].y)) return;  // past the last sequence
   float s = 0.f;
-  for (int g = 0; g < H_kv; ++g) s += part[(b * H_kv + g) * per_b + r];
+  for (int g = 0; g < H_kv; ++g) s += part[(j * H_kv + g) * DI + r];
   out[t] = __float2bfloat16(s);
 }
 
@@ -158,13 +164,13 @@ size_t carve(const Shape& s, void* ws, BwdWs* out) {
   w.kl_acc = reinterpret_cast<double*>(base + off + 128);
   off += 256;
   w.Dv = reinterpret_cast<float*>(base + off);
-  off += align256((size_t)s.B * s.H_q * s.N * 4);
+  off += align256((size_t)s.T * s.H_q * 4);
   w.dq_part = reinterpret_cast<__nv_bfloat16*>(base + off);
   off += align256(parts * s.G * s.d * 2);
   w.dqi_part = reinterpret_cast<__nv_bfloat16*>(base + off);
   off += align256(parts * s.d_idx * 2);
   w.dki_part = reinterpret_cast<float*>(base + off);
-  off += align256((size_t)s.B * s.H_kv * s.N * s.d_idx * 4);
+  off += align256((size_t)s.T * s.H_kv * s.d_idx * 4);
   if (out) *out = w;
   return off;
 }
@@ -184,17 +190,18 @@ cudaError_t run_bwd(const Shape& s, const void* q, const void* k, const void* v,
   if (e != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(w.counter, 0, 256, st)) != cudaSuccess) return e;  // counter + KL
   {
-    const int64_t blocks = (int64_t)s.B * s.H_q * ((s.N + 63) / 64);
+    const int64_t blocks = (int64_t)s.H_q * (s.packed() ? varlen_grid_items(s, kTabRows64)
+                                                        : (int64_t)s.B * ((s.N + 63) / 64));
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     const unsigned grid = (unsigned)blocks;
     if (s.d == 128)
       bwd_pre_kernel<128><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
-                                                static_cast<const __nv_bfloat16*>(dO), w.Dv, s.N,
-                                                s.H_q);
+                                                static_cast<const __nv_bfloat16*>(dO), w.Dv,
+                                                s.spans, s.tab(kTabRows64), s.B, s.N, s.H_q);
     else
       bwd_pre_kernel<64><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
-                                               static_cast<const __nv_bfloat16*>(dO), w.Dv, s.N,
-                                               s.H_q);
+                                               static_cast<const __nv_bfloat16*>(dO), w.Dv,
+                                               s.spans, s.tab(kTabRows64), s.B, s.N, s.H_q);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -211,8 +218,8 @@ cudaError_t run_bwd(const Shape& s, const void* q, const void* k, const void* v,
       return (unsigned)((warps + 7) / 8);
     };
 #define MSA_SLOT_REDUCE(W, GG)                                                                \
-  slot_reduce_kernel<W, GG><<<grid_for(GG * W / 8), 256, 0, st>>>(w.dq_part, block_idx, dqb, R, \
-                                                                  s.N, s.H_kv, s.topk, s.nb)
+  slot_reduce_kernel<W, GG><<<grid_for(GG * W / 8), 256, 0, st>>>(                             \
+      w.dq_part, block_idx, dqb, s.spans, s.B, R, s.N, s.H_kv, s.topk, s.nb)
     if (s.d == 128) {
       switch (s.G) {
         case 1: MSA_SLOT_REDUCE(128, 1); break;
@@ -234,16 +241,16 @@ cudaError_t run_bwd(const Shape& s, const void* q, const void* k, const void* v,
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (s.d_idx == 64)
-      slot_reduce_kernel<64, 1><<<grid_for(8), 256, 0, st>>>(w.dqi_part, block_idx, dqib, R, s.N,
-                                                            s.H_kv, s.topk, s.nb);
+      slot_reduce_kernel<64, 1><<<grid_for(8), 256, 0, st>>>(w.dqi_part, block_idx, dqib, s.spans,
+                                                            s.B, R, s.N, s.H_kv, s.topk, s.nb);
     else
-      slot_reduce_kernel<32, 1><<<grid_for(4), 256, 0, st>>>(w.dqi_part, block_idx, dqib, R, s.N,
-                                                            s.H_kv, s.topk, s.nb);
+      slot_reduce_kernel<32, 1><<<grid_for(4), 256, 0, st>>>(w.dqi_part, block_idx, dqib, s.spans,
+                                                            s.B, R, s.N, s.H_kv, s.topk, s.nb);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int64_t n = (int64_t)s.B * s.N * s.d_idx;
+    const int64_t n = s.T * s.d_idx;
     dki_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
-        w.dki_part, static_cast<__nv_bfloat16*>(dk_idx), s.B, s.N, s.H_kv, s.d_idx);
+        w.dki_part, static_cast<__nv_bfloat16*>(dk_idx), s.spans, s.B, s.T, s.H_kv, s.d_idx);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

@@ -51,6 +51,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 struct BwdTcParams {
   const __nv_bfloat16 *q, *dO, *q_idx, *k_idx;
+  const int2* spans;  // packed batches: (start, end) per sequence
   const float *lse, *Dv, *lse_idx;
   const int* off;
   const int* entries;
@@ -202,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t kk = blockIdx.x; kk < p.keys && !*abort_flag; kk += gridDim.x) {
       const int c = (int)(kk / BG), bg = (int)(kk % BG);
       const int b = bg / p.H_kv, g = bg - b * p.H_kv;
+      const SeqSpan sp = seq_span(p.spans, b, p.N);
       const int key = bg * p.nb + c;
       const int e_begin = __ldg(&p.off[key]), e_end = __ldg(&p.off[key + 1]);
       const int nch = (e_end - e_begin + QC - 1) / QC;
@@ -224,16 +226,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(kvfull, 2 * (D / 64) * L::kKH);
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
-              tma_load_4d(sm + L::kK + h * L::kKH, &tm_k, kvfull, h * 64, g, c * 128, b);
-              tma_load_4d(sm + L::kV + h * L::kKH, &tm_v, kvfull, h * 64, g, c * 128, b);
+              tma_load_4d(sm + L::kK + h * L::kKH, &tm_k, kvfull, h * 64, g, sp.tn + c * 128, sp.tb);
+              tma_load_4d(sm + L::kV + h * L::kKH, &tm_v, kvfull, h * 64, g, sp.tn + c * 128, sp.tb);
             }
             kv_issued = nkeys + 1;
           }
           for (int x = lt; x < 128 * 8; x += kLoadThreads) {  // k_idx rows, zero-padded
             const int r = x / 8, cc = x % 8;
             const int j = c * 128 + r;
-            const bool ok = j < p.N && cc * 8 < p.DI;
-            const int64_t src = ((int64_t)b * p.N + (ok ? j : 0)) * p.DI + (ok ? cc * 8 : 0);
+            const bool ok = j < sp.len && cc * 8 < p.DI;
+            const int64_t src = (sp.t0 + (ok ? j : 0)) * p.DI + (ok ? cc * 8 : 0);
             cp_async_16(sm + L::kKi + sw128(r, cc), p.k_idx + src, ok);
           }
         }
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ent = __shfl_sync(0xffffffffu, my_ent, qi);
           const bool ok = ent >= 0;
           const int i = ok ? (ent >> kSlotBits) : 0;
-          const int64_t src = (((int64_t)b * p.N + i) * p.H_kv * G + g * G + h) * D + cc * 8;
+          const int64_t src = ((sp.t0 + i) * p.H_kv * G + g * G + h) * D + cc * 8;
           const uint32_t o = (cc >> 3) * L::kQH + sw128(r, cc);
           cp_async_16(st + L::kSQ + o, p.q + src, ok);
           cp_async_16(st + L::kSdO + o, p.dO + src, ok);
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ent = __shfl_sync(0xffffffffu, my_ent, qi);
           const bool ok = ent >= 0 && cc * 8 < p.DI;
           const int i = ok ? (ent >> kSlotBits) : 0;
-          const int64_t src = (((int64_t)b * p.N + i) * p.H_kv + g) * p.DI + (ok ? cc * 8 : 0);
+          const int64_t src = ((sp.t0 + i) * p.H_kv + g) * p.DI + (ok ? cc * 8 : 0);
           cp_async_16(ss + L::kSQi + sw128(qi, cc), p.q_idx + src, ok);
         }
         {
@@ -279,19 +281,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ent = r < R ? ent0 : -1;  // rows past the chunk: padding
           const bool ok = ent >= 0;
           const int ri = ok ? (ent >> kSlotBits) : -1;
-          const int64_t x = ((int64_t)b * p.H_kv * G + g * G + h) * p.N + (ok ? ri : 0);
+          const int64_t x = sp.t0 * p.H_kv * G + (int64_t)(g * G + h) * sp.len + (ok ? ri : 0);
           cp_async_4(ss + L::kSLse + 4 * r, p.lse + x, ok);
           cp_async_4(ss + L::kSD + 4 * r, p.Dv + x, ok);
           reinterpret_cast<int*>(ss + L::kSRi)[r] = ri;
           reinterpret_cast<int*>(ss + L::kSRp)[r] =
-              ok ? (int)((((int64_t)bg * p.N + ri) * p.topk + (ent & kSlotMask)) * G + h) : -1;
+              ok ? (int)(((sp.t0 * p.H_kv + (int64_t)g * sp.len + ri) * p.topk + (ent & kSlotMask)) * G +
+                         h)
+                 : -1;
           if (lt < kQS) {
             const bool okq = my_ent >= 0;
             const int iq = okq ? (my_ent >> kSlotBits) : 0;
             reinterpret_cast<int*>(ss + L::kSQiq)[lt] = okq ? iq : -1;
             reinterpret_cast<int*>(ss + L::kSQp)[lt] =
-                okq ? (int)(((int64_t)bg * p.N + iq) * p.topk + (my_ent & kSlotMask)) : -1;
-            cp_async_4(ss + L::kSLi + 4 * lt, p.lse_idx + (int64_t)bg * p.N + iq, okq);
+                okq ? (int)((sp.t0 * p.H_kv + (int64_t)g * sp.len + iq) * p.topk + (my_ent & kSlotMask))
+                    : -1;
+            cp_async_4(ss + L::kSLi + 4 * lt, p.lse_idx + sp.t0 * p.H_kv + (int64_t)g * sp.len + iq,
+                       okq);
           }
         }
         cp_async_commit();
@@ -396,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t kk = blockIdx.x; kk < p.keys && ok; kk += gridDim.x) {
       const int c = (int)(kk / BG), bg = (int)(kk % BG);
       const int b = bg / p.H_kv, g = bg - b * p.H_kv;
+      const SeqSpan sp = seq_span(p.spans, b, p.N);
       const int key = bg * p.nb + c;
       const int e_begin = __ldg(&p.off[key]), e_end = __ldg(&p.off[key + 1]);
       const int nch = (e_end - e_begin + QC - 1) / QC;
@@ -598,9 +605,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- block end: dK (x scale), dV and the dk_idx share from TMEM ----
-      const bool in = j < p.N;
-      __nv_bfloat16* dk_row = p.dk + (((int64_t)b * p.N + j) * p.H_kv + g) * D;
-      __nv_bfloat16* dv_row = p.dv + (((int64_t)b * p.N + j) * p.H_kv + g) * D;
+      const bool in = j < sp.len;
+      __nv_bfloat16* dk_row = p.dk + ((sp.t0 + j) * p.H_kv + g) * D;
+      __nv_bfloat16* dv_row = p.dv + ((sp.t0 + j) * p.H_kv + g) * D;
       if (nch == 0) {
         if (in) {
           for (int x = wg * (D / 2); x < (wg + 1) * (D / 2); ++x) {
@@ -609,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (32 * wg < p.DI) {
             float4* dst = reinterpret_cast<float4*>(
-                p.dki_part + (((int64_t)b * p.H_kv + g) * p.N + j) * p.DI + 32 * wg);
+                p.dki_part + ((sp.t0 + j) * p.H_kv + g) * p.DI + 32 * wg);
 #pragma unroll
             for (int x = 0; x < 8; ++x) dst[x] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
@@ -649,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           if (in) {
             float4* dst = reinterpret_cast<float4*>(
-                p.dki_part + (((int64_t)b * p.H_kv + g) * p.N + j) * p.DI + 32 * wg);
+                p.dki_part + ((sp.t0 + j) * p.H_kv + g) * p.DI + 32 * wg);
 #pragma unroll
             for (int x = 0; x < 8; ++x)
               dst[x] = make_float4(__uint_as_float(a[4 * x]) * p.sidx, __uint_as_float(a[4 * x + 1]) * p.sidx,
@@ -700,9 +707,9 @@ cudaError_t launch_attn_bwd_tc(const Shape& s, const void* q, const void* k, con
                                __nv_bfloat16* dqi_part, float* dki_part, double* kl_acc, void* dk,
                                void* dv, const Ctx& cx, cudaStream_t st) {
   CUtensorMap tk, tv;
-  const uint64_t dims[4] = {(uint64_t)s.d, (uint64_t)s.H_kv, (uint64_t)s.N, (uint64_t)s.B};
+  const uint64_t dims[4] = {(uint64_t)s.d, (uint64_t)s.H_kv, s.tma_tokens(), s.tma_batches()};
   const uint64_t strides[3] = {(uint64_t)s.d * 2, (uint64_t)s.H_kv * s.d * 2,
-                               (uint64_t)s.N * s.H_kv * s.d * 2};
+                               s.tma_tokens() * s.H_kv * s.d * 2};
   const uint32_t box[4] = {64, 1, 128, 1};
   if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -714,6 +721,7 @@ cudaError_t launch_attn_bwd_tc(const Shape& s, const void* q, const void* k, con
   p.dO = static_cast<const __nv_bfloat16*>(dO);
   p.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
   p.k_idx = static_cast<const __nv_bfloat16*>(k_idx);
+  p.spans = s.spans;
   p.lse = lse;
   p.Dv = Dv;
   p.lse_idx = lse_idx;

@@ -23,17 +23,18 @@ template <int D, int G>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(
     const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
     const int32_t* __restrict__ block_idx, __nv_bfloat16* __restrict__ o,
-    float* __restrict__ lse, int64_t rows, int N, int H_kv, int topk, int nb) {
+    float* __restrict__ lse, const int2* __restrict__ spans, int B, int64_t rows, int N, int H_kv,
+    int topk, int nb) {
   constexpr int TC = G * D / 8;              // 16-byte chunks per slot
   constexpr int CPL = (TC + 31) / 32;        // chunks per lane
   __shared__ float wts[8][32 * G];
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t rkv = (int64_t)blockIdx.x * 8 + wib;  // (b*H_kv + g)*N + i
+  const int64_t rkv = (int64_t)blockIdx.x * 8 + wib;  // t0*H_kv + g*len + i
   if (rkv >= rows) return;
-  const int i = (int)(rkv % N);
-  const int64_t bg = rkv / N;
-  const int g = (int)(bg % H_kv);
-  const int64_t b = bg / H_kv;
+  RowPos rp;
+  if (!row_pos(spans, B, N, H_kv, rkv, &rp)) return;  // tokens outside every sequence
+  const int i = rp.i, g = rp.h;
+  const SeqSpan sp = rp.sp;
   const int32_t* sel = block_idx + rkv * topk;
   float* w = wts[wib];
   if (lane < G) {
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
     for (int s = 0; s < topk; ++s) w[s * G + h] *= inv;
-    lse[(b * H_kv * G + g * G + h) * N + i] = m + logf(l);
+    lse[sp.t0 * H_kv * G + (int64_t)(g * G + h) * sp.len + i] = m + logf(l);
   }
   __syncwarp();
   float acc[CPL][8];
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
       }
     }
   }
-  uint4* dst = reinterpret_cast<uint4*>(o + ((b * N + i) * H_kv * G + (int64_t)g * G) * D);
+  uint4* dst = reinterpret_cast<uint4*>(o + ((sp.t0 + i) * H_kv * G + (int64_t)g * G) * D);
 #pragma unroll
   for (int x = 0; x < CPL; ++x) {
     const int ch = lane + 32 * x;
@@ -102,17 +103,18 @@ template <int D, int G>
 __global__ void __launch_bounds__(256) fwd_combine_wide_kernel(
     const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
     const int32_t* __restrict__ block_idx, __nv_bfloat16* __restrict__ o,
-    float* __restrict__ lse, int64_t rows, int N, int H_kv, int topk, int nb) {
+    float* __restrict__ lse, const int2* __restrict__ spans, int B, int64_t rows, int N, int H_kv,
+    int topk, int nb) {
   constexpr int TC = G * D / 8;              // 16-byte chunks per slot
   constexpr int CPL = (TC + 31) / 32;        // chunks per lane
   __shared__ float wts[8][32 * G];
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t rkv = (int64_t)blockIdx.x * 8 + wib;  // (b*H_kv + g)*N + i
+  const int64_t rkv = (int64_t)blockIdx.x * 8 + wib;  // t0*H_kv + g*len + i
   if (rkv >= rows) return;
-  const int i = (int)(rkv % N);
-  const int64_t bg = rkv / N;
-  const int g = (int)(bg % H_kv);
-  const int64_t b = bg / H_kv;
+  RowPos rp;
+  if (!row_pos(spans, B, N, H_kv, rkv, &rp)) return;  // tokens outside every sequence
+  const int i = rp.i, g = rp.h;
+  const SeqSpan sp = rp.sp;
   const int32_t* sel = block_idx + rkv * topk;
   float* w = wts[wib];
   float m = -INFINITY, inv = 0.f;
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(256) fwd_combine_wide_kernel(
     }
     inv = l > 0.f ? 1.f / l : 0.f;
     for (int s = 0; s < min(32, topk); ++s) w[s * G + h] *= inv;
-    lse[(b * H_kv * G + g * G + h) * N + i] = m + logf(l);
+    lse[sp.t0 * H_kv * G + (int64_t)(g * G + h) * sp.len + i] = m + logf(l);
   }
   float acc[CPL][8];
 #pragma unroll
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(256) fwd_combine_wide_kernel(
       }
     }
   }
-  uint4* dst = reinterpret_cast<uint4*>(o + ((b * N + i) * H_kv * G + (int64_t)g * G) * D);
+  uint4* dst = reinterpret_cast<uint4*>(o + ((sp.t0 + i) * H_kv * G + (int64_t)g * G) * D);
 #pragma unroll
   for (int x = 0; x < CPL; ++x) {
     const int ch = lane + 32 * x;
@@ -207,11 +209,12 @@ cudaError_t launch_attn_fwd_combine(const Shape& s, const int32_t* block_idx,
   do {                                                                                         \
     if (s.topk <= 32)                                                                          \
       fwd_combine_kernel<DD, GG><<<grid, 256, 0, st>>>(o_part, lse_part, block_idx, ob, lse,   \
-                                                       s.rows_kv(), s.N, s.H_kv, s.topk, s.nb); \
+                                                       s.spans, s.B, s.rows_kv(), s.N, s.H_kv, \
+                                                       s.topk, s.nb);                          \
     else                                                                                       \
       fwd_combine_wide_kernel<DD, GG><<<grid, 256, 0, st>>>(o_part, lse_part, block_idx, ob,   \
-                                                            lse, s.rows_kv(), s.N, s.H_kv,     \
-                                                            s.topk, s.nb);                     \
+                                                            lse, s.spans, s.B, s.rows_kv(),    \
+                                                            s.N, s.H_kv, s.topk, s.nb);        \
   } while (0)
   if (s.d == 128) {
     switch (s.G) {

@@ -39,6 +39,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 struct FwdTcParams {
   const __nv_bfloat16* q;
+  const int2* spans;      // packed batches: (start, end) per sequence
   const int* off;
   const int* toff;
   const int* entries;
@@ -204,6 +205,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int key = kc.at(p.toff, p.keys, t);
         const int bg = key / p.nb, c = key - bg * p.nb;
         const int b = bg / p.H_kv, g = bg - b * p.H_kv;
+        const SeqSpan sp = seq_span(p.spans, b, p.N);
         const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * QPT;
         const int ne = min(QPT, __ldg(&p.off[key + 1]) - e0);
         if (!mbar_wait(&qempty[st], ((u / kQStages) & 1) ^ 1, p.wait_ns, abort_flag)) {
@@ -225,8 +227,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         static_assert(kLoadThreads % CH == 0, "loader threads cover whole rows");
         constexpr int RS = kLoadThreads / CH;  // rows per pass
         const int chf = lt % CH;
-        const __nv_bfloat16* qg =
-            p.q + ((int64_t)b * p.N * p.H_kv * G + (int64_t)g * G) * D + chf * 8;
+        const __nv_bfloat16* qg = p.q + (sp.t0 * p.H_kv * G + (int64_t)g * G) * D + chf * 8;
         const int64_t qrow = (int64_t)p.H_kv * G * D;  // elements between consecutive queries
         uint8_t* dcol = dq + (chf >> 3) * L::kHalf;
 #pragma unroll 4
@@ -257,8 +258,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               mbar_arrive_expect_tx(kvfull, 2 * L::kTile);
 #pragma unroll
               for (int h = 0; h < L::kHalves; ++h) {
-                tma_load_4d(sK + h * L::kHalf, &tm_k, kvfull, h * 64, g, c * 128, b);
-                tma_load_4d(sV + h * L::kHalf, &tm_v, kvfull, h * 64, g, c * 128, b);
+                tma_load_4d(sK + h * L::kHalf, &tm_k, kvfull, h * 64, g, sp.tn + c * 128, sp.tb);
+                tma_load_4d(sV + h * L::kHalf, &tm_v, kvfull, h * 64, g, sp.tn + c * 128, sp.tb);
               }
               kv_issued = kv_loads + 1;
             }
@@ -368,7 +369,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_after();
         // causal mask j <= i (and j < N), scaled to log2 units
-        const int jlim = ent >= 0 ? min(i, p.N - 1) - c * 128 : -1;  // last valid column
+        const int bb = bg / p.H_kv, gg = bg - bb * p.H_kv;
+        const SeqSpan sp = seq_span(p.spans, bb, p.N);
+        const int jlim = ent >= 0 ? min(i, sp.len - 1) - c * 128 : -1;  // last valid column
         // blocks wholly before every query of the warp need no mask (the usual case)
         const bool full = __all_sync(0xffffffffu, jlim >= 127);
         // P (bf16) into this group's K-major smem operand, once its previous PV is done
@@ -463,7 +466,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float inv = l > 0.f ? 1.f / l : 0.f;
         int prow = -1;
         if (ent >= 0) {
-          prow = (int)((((int64_t)bg * p.N + i) * p.topk + (ent & kSlotMask)) * G + row % G);
+          prow = (int)(((sp.t0 * p.H_kv + (int64_t)gg * sp.len + i) * p.topk + (ent & kSlotMask)) * G +
+                       row % G);
           p.lse_part[prow] = l > 0.f ? (ms + log2f(l)) * kLn2 : -INFINITY;
         }
         // Stage 64 columns at a time in this warp's own (now free) P rows, swizzled,
@@ -551,9 +555,9 @@ cudaError_t launch_attn_fwd_tc(const Shape& s, const void* q, const void* k, con
                                const Plan& pl, __nv_bfloat16* o_part, float* lse_part,
                                const Ctx& cx, cudaStream_t st) {
   CUtensorMap tk, tv;
-  const uint64_t dims[4] = {(uint64_t)s.d, (uint64_t)s.H_kv, (uint64_t)s.N, (uint64_t)s.B};
+  const uint64_t dims[4] = {(uint64_t)s.d, (uint64_t)s.H_kv, s.tma_tokens(), s.tma_batches()};
   const uint64_t strides[3] = {(uint64_t)s.d * 2, (uint64_t)s.H_kv * s.d * 2,
-                               (uint64_t)s.N * s.H_kv * s.d * 2};
+                               s.tma_tokens() * s.H_kv * s.d * 2};
   const uint32_t box[4] = {64, 1, 128, 1};
   if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -562,6 +566,7 @@ cudaError_t launch_attn_fwd_tc(const Shape& s, const void* q, const void* k, con
     return cudaErrorInvalidValue;
   FwdTcParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.spans = s.spans;
   prm.off = pl.off;
   prm.toff = pl.toff;
   prm.entries = pl.entries;

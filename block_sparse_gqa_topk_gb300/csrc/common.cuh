@@ -27,6 +27,91 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);  // first error wins
 }
 
+// ---------------------------------------------------------------------------
+// batches: B sequences of N tokens (spans == nullptr) or a packed variable-length
+// batch whose sequence b holds tokens spans[b].x .. spans[b].y - 1 (at most N of them).
+// Per-sequence head-major arrays ([H][len] per sequence, e.g. block_idx rows, lse) put
+// row (b, h, i) at t0*H + h*len + i, which is (b*H + h)*N + i in the fixed layout.
+// ---------------------------------------------------------------------------
+struct SeqSpan {
+  int64_t t0;  // first token of the sequence on the token axis
+  int len;     // its tokens
+  int tn, tb;  // TMA (token, batch) coordinates of its token 0
+};
+__device__ __forceinline__ SeqSpan seq_span(const int2* spans, int b, int N) {
+  SeqSpan s;
+  if (!spans) {
+    s.t0 = (int64_t)b * N;
+    s.len = N;
+    s.tn = 0;
+    s.tb = b;
+  } else {
+    const int2 v = __ldg(&spans[b]);
+    s.t0 = v.x;
+    s.len = v.y - v.x;
+    s.tn = v.x;
+    s.tb = 0;
+  }
+  return s;
+}
+
+// Last b in [0, n) with tab[b] <= x, for an ascending tab with tab[0] <= x.
+__device__ __forceinline__ int last_at_most(const int* __restrict__ tab, int n, int64_t x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(&tab[mid]) <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Work item w of a grid over row chunks: the sequence b and the chunk within it, from
+// the fixed layout (chunks per sequence `per`) or a row-chunk table.  False when w is
+// past the last chunk.
+__device__ __forceinline__ bool chunk_item(const int* tab, int B, int per, int64_t w, int* b,
+                                           int* chunk) {
+  if (!tab) {
+    if (w >= (int64_t)B * per) return false;
+    *b = (int)(w / per);
+    *chunk = (int)(w - (int64_t)*b * per);
+    return true;
+  }
+  if (w >= __ldg(&tab[B])) return false;
+  *b = last_at_most(tab, B, w);
+  *chunk = (int)(w - __ldg(&tab[*b]));
+  return true;
+}
+
+// Sequence, head and position of row r of a per-sequence head-major array with H heads.
+// False for rows past the batch's last token.
+struct RowPos {
+  SeqSpan sp;
+  int b, h, i;
+};
+__device__ __forceinline__ bool row_pos(const int2* spans, int B, int N, int H, int64_t r,
+                                        RowPos* o) {
+  if (!spans) {
+    const int64_t bh = r / N;
+    o->i = (int)(r - bh * N);
+    o->b = (int)(bh / H);
+    o->h = (int)(bh - (int64_t)o->b * H);
+    o->sp = seq_span(nullptr, o->b, N);
+    return o->b < B;
+  }
+  int lo = 0, hi = B - 1;  // last sequence whose rows start at or before r
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)__ldg(&spans[mid].x) * H <= r) lo = mid; else hi = mid - 1;
+  }
+  o->b = lo;
+  o->sp = seq_span(spans, lo, N);
+  const int64_t local = r - o->sp.t0 * H;
+  if (o->sp.len <= 0 || local < 0 || local >= (int64_t)o->sp.len * H) return false;
+  o->h = (int)(local / o->sp.len);
+  o->i = (int)(local - (int64_t)o->h * o->sp.len);
+  return true;
+}
+
 // Programmatic dependent launch (PTX griddepcontrol, sm_90 and later).  A kernel
 // launched with the programmatic-serialization attribute may be scheduled while the
 // previous kernel in its stream is still running; griddep_wait() returns once that

@@ -54,11 +54,12 @@ struct LseLayout {
 };
 
 struct LseParams {
-  const __nv_bfloat16* q_idx;  // [B][N][H_kv][DI]
+  const __nv_bfloat16* q_idx;  // [T][H_kv][DI]
+  const int2* spans;           // packed batches: (start, end) per sequence
   const int* off;
   const int* toff;
   const int* entries;
-  float* lse_part;             // [((b*H_kv + g)*N + i)*topk + slot]
+  float* lse_part;             // [(t0*H_kv + g*len + i)*topk + slot]
   int64_t keys;
   int N, H_kv, nb, topk;
   float scale_log2;            // scale_idx * log2(e)
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key = kc.at(p.toff, p.keys, t);
         const int bg = key / p.nb, c = key - bg * p.nb;
         const int b = bg / p.H_kv, g = bg - b * p.H_kv;
+        const SeqSpan sp = seq_span(p.spans, b, p.N);
         const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * 128;
         const int ne = min(128, __ldg(&p.off[key + 1]) - e0);
         if (key != prev_key) {
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               *abort_flag = 1;
             if (!*abort_flag) {
               mbar_arrive_expect_tx(&kfull[kb], L::kTile);
-              tma_load_3d(sK + kb * L::kTile, &tm_k, &kfull[kb], 0, c * 128, b);
+              tma_load_3d(sK + kb * L::kTile, &tm_k, &kfull[kb], 0, sp.tn + c * 128, sp.tb);
               k_issued = k_loads + 1;
             }
           }
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ent = r < ne ? __ldg(&p.entries[e0 + r]) : -1;
           const bool ok = ent >= 0;
           const int i = ok ? (ent >> kSlotBits) : 0;
-          const int64_t src = (((int64_t)b * p.N + i) * p.H_kv + g) * DI + ch * 8;
+          const int64_t src = ((sp.t0 + i) * p.H_kv + g) * DI + ch * 8;
           cp_async_16(dq + swz<RB>(r, ch), p.q_idx + src, ok);
         }
         cp_async_commit();
@@ -263,6 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sl = u % kSlots;
         const int key = kc.at(p.toff, p.keys, t);
         const int bg = key / p.nb, c = key - bg * p.nb;
+        const int b = bg / p.H_kv, g = bg - b * p.H_kv;
+        const SeqSpan sp = seq_span(p.spans, b, p.N);
         const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * 128;
         const int ne = min(128, __ldg(&p.off[key + 1]) - e0);
         const int ent = row < ne ? __ldg(&p.entries[e0 + row]) : -1;
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const int jlim = ent >= 0 ? min(i, p.N - 1) - c * 128 : -1;  // last valid column
+        const int jlim = ent >= 0 ? min(i, sp.len - 1) - c * 128 : -1;  // last valid column
         const bool full = __all_sync(0xffffffffu, jlim >= 127);
         float m = -INFINITY;  // running max of the raw scores
         float l0 = 0.f, l1 = 0.f;
@@ -331,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ent >= 0) {
           const float l = l0 + l1;
-          p.lse_part[((int64_t)bg * p.N + i) * p.topk + (ent & kSlotMask)] =
+          p.lse_part[(sp.t0 * p.H_kv + (int64_t)g * sp.len + i) * p.topk + (ent & kSlotMask)] =
               l > 0.f ? (m * sl2 + log2f(l)) * kLn2 : -INFINITY;
         }
       }
@@ -350,9 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // lse_idx[b,g,i] = log-sum-exp over the row's valid slots of the partial lse.
 __global__ void lse_combine_kernel(const float* __restrict__ lse_part,
                                    const int32_t* __restrict__ block_idx,
-                                   float* __restrict__ lse_idx, int64_t rows, int topk, int nb) {
+                                   float* __restrict__ lse_idx, const int2* __restrict__ spans,
+                                   int B, int N, int H_kv, int64_t rows, int topk, int nb) {
   const int64_t r = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (r >= rows) return;
+  RowPos rp;
+  if (spans && !row_pos(spans, B, N, H_kv, r, &rp)) return;  // tokens outside every sequence
   const int32_t* sel = block_idx + r * topk;
   float m = -INFINITY;
   for (int s = 0; s < topk; ++s)
@@ -384,14 +391,15 @@ cudaError_t launch_index_lse(const Shape& s, const void* q_idx, const void* k_id
                              float* lse_idx, const Ctx& cx, cudaStream_t st) {
   const int DI = s.d_idx;
   CUtensorMap tk;
-  const uint64_t dims[3] = {(uint64_t)DI, (uint64_t)s.N, (uint64_t)s.B};
-  const uint64_t strides[2] = {(uint64_t)DI * 2, (uint64_t)s.N * DI * 2};
+  const uint64_t dims[3] = {(uint64_t)DI, s.tma_tokens(), s.tma_batches()};
+  const uint64_t strides[2] = {(uint64_t)DI * 2, s.tma_tokens() * DI * 2};
   const uint32_t box[3] = {(uint32_t)DI, 128, 1};
   if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_idx, dims, strides, box,
                     DI == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   LseParams prm;
   prm.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
+  prm.spans = s.spans;
   prm.off = pl.off;
   prm.toff = pl.toff;
   prm.entries = pl.entries;
@@ -407,8 +415,8 @@ cudaError_t launch_index_lse(const Shape& s, const void* q_idx, const void* k_id
   cudaError_t e = DI == 64 ? launch_lse_tc<64>(tk, prm, cx, st) : launch_lse_tc<32>(tk, prm, cx, st);
   if (e != cudaSuccess) return e;
   const int64_t rows = s.rows_kv();
-  lse_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(lse_part, block_idx, lse_idx,
-                                                                     rows, s.topk, s.nb);
+  lse_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(
+      lse_part, block_idx, lse_idx, s.spans, s.B, s.N, s.H_kv, rows, s.topk, s.nb);
   note_launch();
   return cudaGetLastError();
 }

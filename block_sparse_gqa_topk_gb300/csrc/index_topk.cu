@@ -48,8 +48,10 @@ struct IdxLayout {
 
 struct IdxParams {
   int32_t* block_idx;
+  const int2* spans;  // packed batches: (start, end) per sequence; nullptr: fixed [B][N]
+  const int* units;   // packed batches: prefix counts of ceil(len / 256) per sequence
   int B, N, H_kv, nb, topk;
-  int n_units;  // ceil(nb / 2) query-block pairs
+  int n_units;  // fixed layout: ceil(nb / 2) query-block pairs per sequence
   int n_gp;     // ceil(H_kv / 2) group pairs
   uint64_t wait_ns;
   int debug;
@@ -117,13 +119,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // CTA -> (batch, group pair, query-block pair)
-  const int u = blockIdx.x % p.n_units;
-  const int gp = (blockIdx.x / p.n_units) % p.n_gp;
-  const int b = blockIdx.x / (p.n_units * p.n_gp);
+  // CTA -> (sequence, group pair, query-block pair); the pair (u, nbs-1-u) of a
+  // sequence of nbs blocks
+  int b, u, gp;
+  if (!p.units) {
+    u = blockIdx.x % p.n_units;
+    gp = (blockIdx.x / p.n_units) % p.n_gp;
+    b = blockIdx.x / (p.n_units * p.n_gp);
+  } else {
+    gp = blockIdx.x % p.n_gp;
+    if (!chunk_item(p.units, p.B, 0, blockIdx.x / p.n_gp, &b, &u)) return;  // whole CTA
+  }
+  const SeqSpan sp = seq_span(p.spans, b, p.N);
   const int g0 = 2 * gp;
   const int ng = min(2, p.H_kv - g0);
-  const int qa = p.nb - 1 - u;  // heavy block first
+  const int qa = (sp.len + 127) / 128 - 1 - u;  // heavy block first
   const int nq = (u < qa) ? 2 : 1;
   const int M = p.topk - 1;     // non-local slots
 
@@ -167,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(qfull, ng * L::kTile);
         for (int gi = 0; gi < ng; ++gi)
-          tma_load_4d(sQ + gi * L::kTile, &tm_q, qfull, 0, g0 + gi, qb * 128, b);
+          tma_load_4d(sQ + gi * L::kTile, &tm_q, qfull, 0, g0 + gi, sp.tn + qb * 128, sp.tb);
         ++qloads;
         for (int t = 0; t < nt; ++t, ++kt) {
           const int s = kt % kStages, use = kt / kStages;
@@ -176,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[s], L::kTile);
-          tma_load_3d(sK + s * L::kTile, &tm_k, &full[s], 0, t * 128, b);
+          tma_load_3d(sK + s * L::kTile, &tm_k, &full[s], 0, sp.tn + t * 128, sp.tb);
         }
       }
       // teardown: every load issued must have landed before the CTA exits
@@ -300,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;  // warp-uniform exit
         const int i = qb * 128 + row;
-        if (i < p.N) {
-          int32_t* dst = p.block_idx + (((int64_t)b * p.H_kv + g) * p.N + i) * p.topk;
+        if (i < sp.len) {
+          int32_t* dst = p.block_idx + (sp.t0 * p.H_kv + (int64_t)g * sp.len + i) * p.topk;
           store_row<KM>(dst, id, M, qb, p.topk);
         }
       }
@@ -321,13 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // topk >= nb: every visible block is selected (blocks 0..i/128 ascending, then -1) --
 // the dense set of the indexer warm-up, where both branches see the full causal
 // context ("Cómo se entrena MSA" ¶3: warm-up with full attention in both branches).
-__global__ void forced_set_kernel(int32_t* __restrict__ block_idx, int64_t rows, int N, int topk,
-                                  int all) {
+__global__ void forced_set_kernel(int32_t* __restrict__ block_idx, const int2* __restrict__ spans,
+                                  int B, int N, int H_kv, int64_t rows, int topk, int all) {
   const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (t >= rows * topk) return;
   const int64_t r = t / topk;
   const int s = (int)(t % topk);
-  const int c = (int)(r % N) / 128;
+  RowPos rp;
+  if (!row_pos(spans, B, N, H_kv, r, &rp)) return;  // tokens outside every sequence
+  const int c = rp.i / 128;
   block_idx[t] = all ? (s <= c ? s : -1) : (s == 0 ? c : -1);
 }
 
@@ -359,11 +371,11 @@ cudaError_t launch_di(const Shape& s, const CUtensorMap& tq, const CUtensorMap& 
 
 cudaError_t launch_index_topk(const Shape& s, const void* q_idx, const void* k_idx,
                               int32_t* block_idx, const Ctx& cx, cudaStream_t st) {
-  if (s.B == 0 || s.N == 0 || s.H_kv == 0) return cudaSuccess;
+  if (s.B == 0 || s.N == 0 || s.T == 0 || s.H_kv == 0) return cudaSuccess;
   if (s.topk == 1 || s.topk >= s.nb) {
     const int64_t n = s.rows_kv() * s.topk;
-    forced_set_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(block_idx, s.rows_kv(), s.N,
-                                                                   s.topk, s.topk >= s.nb);
+    forced_set_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
+        block_idx, s.spans, s.B, s.N, s.H_kv, s.rows_kv(), s.topk, s.topk >= s.nb);
     note_launch();
     return cudaGetLastError();
   }
@@ -372,22 +384,24 @@ cudaError_t launch_index_topk(const Shape& s, const void* q_idx, const void* k_i
   const CUtensorMapSwizzle swz = DI == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap tq, tk;
   {
-    const uint64_t dims[4] = {(uint64_t)DI, (uint64_t)s.H_kv, (uint64_t)s.N, (uint64_t)s.B};
+    const uint64_t dims[4] = {(uint64_t)DI, (uint64_t)s.H_kv, s.tma_tokens(), s.tma_batches()};
     const uint64_t strides[3] = {(uint64_t)DI * 2, (uint64_t)s.H_kv * DI * 2,
-                                 (uint64_t)s.N * s.H_kv * DI * 2};
+                                 s.tma_tokens() * s.H_kv * DI * 2};
     const uint32_t box[4] = {(uint32_t)DI, 1, 128, 1};
     if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, q_idx, dims, strides, box, swz))
       return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)DI, (uint64_t)s.N, (uint64_t)s.B};
-    const uint64_t strides[2] = {(uint64_t)DI * 2, (uint64_t)s.N * DI * 2};
+    const uint64_t dims[3] = {(uint64_t)DI, s.tma_tokens(), s.tma_batches()};
+    const uint64_t strides[2] = {(uint64_t)DI * 2, s.tma_tokens() * DI * 2};
     const uint32_t box[3] = {(uint32_t)DI, 128, 1};
     if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_idx, dims, strides, box, swz))
       return cudaErrorInvalidValue;
   }
   IdxParams p;
   p.block_idx = block_idx;
+  p.spans = s.spans;
+  p.units = s.tab(kTabIndexUnit);
   p.B = s.B;
   p.N = s.N;
   p.H_kv = s.H_kv;
@@ -398,7 +412,8 @@ cudaError_t launch_index_topk(const Shape& s, const void* q_idx, const void* k_i
   p.wait_ns = cx.wait_ns;
   p.debug = cx.debug;
   p.status = cx.status;
-  const int64_t grid = (int64_t)s.B * p.n_gp * p.n_units;
+  const int64_t grid = (int64_t)p.n_gp * (s.packed() ? varlen_grid_items(s, kTabIndexUnit)
+                                                      : (int64_t)s.B * p.n_units);
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   if (DI == 64) return launch_di<64>(s, tq, tk, p, (int)grid, st);
   return launch_di<32>(s, tq, tk, p, (int)grid, st);

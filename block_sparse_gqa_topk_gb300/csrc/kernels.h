@@ -19,16 +19,47 @@ constexpr int kSlotBits = 8;
 constexpr int kSlotMask = (1 << kSlotBits) - 1;
 constexpr int kMaxSlots = 1 << kSlotBits;
 constexpr int kMaxSelect = 32;
+// Blocks per sequence the plan histograms in shared memory (the only plan path for
+// packed variable-length batches).
+constexpr int kPlanSmemBins = 16384;
 
-// Validated problem, with derived sizes.
+// Row-chunk tables of a packed variable-length batch (written on the device by
+// varlen_prepare): tab[k][b] = sum over sequences b' < b of ceil(len_b' / kVarlenChunk[k]),
+// so work item w of a grid over chunks belongs to the last b with tab[k][b] <= w.
+enum VarlenTable {
+  kTabIndexUnit = 0,  // 256 queries: a pair of 128-query blocks of the index kernel
+  kTabPlanCount = 1,  // the plan's counting CTAs
+  kTabPlanFill = 2,   // the plan's fill CTAs (rows depend on topk)
+  kTabRows64 = 3,     // 64 rows: the backward preprocess
+  kNumVarlenTabs = 4
+};
+
+// Validated problem, with derived sizes.  A batch is either B sequences of N tokens
+// (spans == nullptr; sequence b starts at token b*N) or a packed variable-length batch of
+// B sequences of at most N tokens each, sequence b holding tokens spans[b].x .. spans[b].y-1
+// of T (device arrays checked and written by varlen_prepare).
 struct Shape {
   int B, N, H_q, H_kv, d, d_idx, Bk, topk, causal;
   float scale, scale_idx;
   int G;   // H_q / H_kv
-  int nb;  // ceil(N / Bk)
-  int64_t rows_kv() const { return (int64_t)B * H_kv * N; }  // (b, g, i) rows
-  int64_t keys() const { return (int64_t)B * H_kv * nb; }    // (b, g, block) lists
+  int nb;  // ceil(N / Bk): blocks of the longest sequence
+  int64_t T = 0;                // tokens on the token axis (B*N for the fixed layout)
+  const int2* spans = nullptr;  // [B] (start, end), packed batches only
+  const int* tabs = nullptr;    // [kNumVarlenTabs][B + 1] row-chunk tables, packed only
+  int64_t rows_kv() const { return T * H_kv; }            // (b, g, i) rows
+  int64_t keys() const { return (int64_t)B * H_kv * nb; } // (b, g, block) lists
+  bool packed() const { return spans != nullptr; }
+  // extents of the token and batch axes of the TMA tensor maps
+  uint64_t tma_tokens() const { return packed() ? (uint64_t)T : (uint64_t)N; }
+  uint64_t tma_batches() const { return packed() ? 1u : (uint64_t)B; }
+  const int* tab(VarlenTable k) const { return tabs ? tabs + (size_t)k * (B + 1) : nullptr; }
 };
+
+// Rows per chunk of each table (kTabPlanFill: the fill kernel's rows for this topk).
+int varlen_chunk_rows(VarlenTable k, int topk);
+// Work items of a grid over the chunks of table k: an upper bound the host can compute
+// without reading the spans (sum of ceil(len / R) <= ceil(T / R) + B).
+int64_t varlen_grid_items(const Shape& s, VarlenTable k);
 
 // Per-call device context.
 struct Ctx {
@@ -123,6 +154,29 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // current device (status word, wait limit, SM count; MSA_ERR_UNSUPPORTED off sm_103).
 int validate_problem(const msa_problem_t* p, Shape* s);
 int device_ctx(Ctx* cx);
+int finish(cudaError_t e);  // MSA_OK or MSA_ERR_CUDA
+
+// Argument checks and call sequences of the three training calls, shared by the fixed
+// and the packed variable-length entry points (msa_api.cu, attn_bwd.cu).  ws is the
+// call's workspace of ws_*_bytes(s) bytes, 256-byte aligned.
+size_t ws_index_bytes(const Shape& s);
+size_t ws_fwd_bytes(const Shape& s);
+size_t bwd_ws_bytes(const Shape& s);
+int check_index_args(const Shape& s, const void* q_idx, const void* k_idx,
+                     const int32_t* block_idx);
+int check_fwd_args(const void* q, const void* k, const void* v, const int32_t* block_idx,
+                   const void* o, const float* lse);
+int check_bwd_args(const void* const* ptrs, int n);
+cudaError_t run_index(const Shape& s, const void* q_idx, const void* k_idx, int32_t* block_idx,
+                      float* lse_idx, void* ws, const Ctx& cx, cudaStream_t st);
+cudaError_t run_fwd(const Shape& s, const void* q, const void* k, const void* v,
+                    const int32_t* block_idx, void* o, float* lse, void* ws, const Ctx& cx,
+                    cudaStream_t st);
+cudaError_t run_bwd(const Shape& s, const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const void* dO, const void* q_idx, const void* k_idx,
+                    const int32_t* block_idx, const float* lse_idx, float kl_weight, void* dq,
+                    void* dk, void* dv, void* dq_idx, void* dk_idx, float* kl_out, void* ws,
+                    const Ctx& cx, cudaStream_t st);
 
 // Launch bookkeeping (msa_api.cu): counts launches and records the profiling
 // events of msa_set_kernel_events around the named kernels.

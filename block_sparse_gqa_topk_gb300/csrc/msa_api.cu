@@ -80,6 +80,9 @@ int check_problem(const msa_problem_t* p, Shape* s) {
   s->scale_idx = p->scale_idx > 0.f ? p->scale_idx : 1.0f / sqrtf((float)p->d_idx);
   s->G = G;
   s->nb = (p->N + p->Bk - 1) / p->Bk;
+  s->T = (int64_t)p->B * p->N;
+  s->spans = nullptr;
+  s->tabs = nullptr;
   // int32 offsets index every (row, slot) entry and every partial row
   if (s->rows_kv() * s->topk * (int64_t)G >= (int64_t)1 << 31) return MSA_ERR_UNSUPPORTED;
   return MSA_OK;
@@ -93,7 +96,60 @@ size_t ws_fwd(const Shape& s) {
   return plan_bytes(s) + align256(parts * s.d * 2) + align256(parts * 4);
 }
 
+}  // namespace
+
 int finish(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
+size_t ws_index_bytes(const Shape& s) { return ws_index(s); }
+size_t ws_fwd_bytes(const Shape& s) { return ws_fwd(s); }
+
+int check_index_args(const Shape& s, const void* q_idx, const void* k_idx,
+                     const int32_t* block_idx) {
+  if (!q_idx || !k_idx || !block_idx) return MSA_ERR_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(block_idx)) return MSA_ERR_ARG;
+  // selection keeps at most kMaxSelect candidates; more slots only for the dense set
+  if (s.topk > kMaxSelect && s.topk < s.nb) return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+int check_fwd_args(const void* q, const void* k, const void* v, const int32_t* block_idx,
+                   const void* o, const float* lse) {
+  if (!q || !k || !v || !block_idx || !o || !lse) return MSA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(block_idx) || !aligned16(o) ||
+      !aligned16(lse))
+    return MSA_ERR_ARG;
+  return MSA_OK;
+}
+
+int check_bwd_args(const void* const* ptrs, int n) {
+  for (int i = 0; i < n; ++i)
+    if (!ptrs[i] || !aligned16(ptrs[i])) return MSA_ERR_ARG;
+  return MSA_OK;
+}
+
+cudaError_t run_index(const Shape& s, const void* q_idx, const void* k_idx, int32_t* block_idx,
+                      float* lse_idx, void* ws, const Ctx& cx, cudaStream_t st) {
+  cudaError_t e = launch_index_topk(s, q_idx, k_idx, block_idx, cx, st);
+  if (e != cudaSuccess || !lse_idx) return e;
+  Plan pl = plan_carve(s, ws);
+  float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + plan_bytes(s));
+  if ((e = launch_plan(s, block_idx, 128, pl, cx, st)) != cudaSuccess) return e;
+  return launch_index_lse(s, q_idx, k_idx, block_idx, pl, lse_part, lse_idx, cx, st);
+}
+
+cudaError_t run_fwd(const Shape& s, const void* q, const void* k, const void* v,
+                    const int32_t* block_idx, void* o, float* lse, void* ws, const Ctx& cx,
+                    cudaStream_t st) {
+  Plan pl = plan_carve(s, ws);
+  uint8_t* w = static_cast<uint8_t*>(ws) + plan_bytes(s);
+  const size_t parts = (size_t)s.rows_kv() * s.topk * s.G;
+  __nv_bfloat16* o_part = reinterpret_cast<__nv_bfloat16*>(w);
+  float* lse_part = reinterpret_cast<float*>(w + align256(parts * s.d * 2));
+  cudaError_t e = launch_plan(s, block_idx, 128 / s.G, pl, cx, st);
+  if (e != cudaSuccess) return e;
+  return launch_attn_fwd(s, q, k, v, block_idx, pl, o_part, lse_part, o, lse, cx, st);
+}
+
+namespace {
 
 std::atomic<uint64_t> g_launches{0};
 cudaEvent_t g_ev[4][2] = {};
@@ -163,12 +219,6 @@ void kernel_event(int kernel, bool before, cudaStream_t st) {
   if (ev) cudaEventRecord(ev, st);
 }
 
-size_t bwd_ws_bytes(const Shape& s);
-cudaError_t run_bwd(const Shape& s, const void* q, const void* k, const void* v, const void* o,
-                    const float* lse, const void* dO, const void* q_idx, const void* k_idx,
-                    const int32_t* block_idx, const float* lse_idx, float kl_weight, void* dq,
-                    void* dk, void* dv, void* dq_idx, void* dk_idx, float* kl_out, void* ws,
-                    const Ctx& cx, cudaStream_t st);
 
 }  // namespace msa
 
@@ -240,22 +290,14 @@ int msa_index_topk(const msa_problem_t* p, const void* q_idx, const void* k_idx,
   int rc = check_problem(p, &s);
   if (rc) return rc;
   if (s.B == 0 || s.N == 0) return MSA_OK;
-  if (!q_idx || !k_idx || !block_idx) return MSA_ERR_ARG;
-  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(block_idx)) return MSA_ERR_ARG;
-  // selection keeps at most kMaxSelect candidates; more slots only for the dense set
-  if (s.topk > kMaxSelect && s.topk < s.nb) return MSA_ERR_UNSUPPORTED;
+  if ((rc = check_index_args(s, q_idx, k_idx, block_idx))) return rc;
   if (lse_idx) {
     if (!workspace || workspace_bytes < ws_index(s)) return MSA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MSA_ERR_ARG;
   }
   Ctx cx;
   if ((rc = make_ctx(&cx))) return rc;
-  cudaError_t e = launch_index_topk(s, q_idx, k_idx, block_idx, cx, stream);
-  if (e != cudaSuccess || !lse_idx) return finish(e);
-  Plan pl = plan_carve(s, workspace);
-  float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan_bytes(s));
-  if ((e = launch_plan(s, block_idx, 128, pl, cx, stream)) != cudaSuccess) return finish(e);
-  return finish(launch_index_lse(s, q_idx, k_idx, block_idx, pl, lse_part, lse_idx, cx, stream));
+  return finish(run_index(s, q_idx, k_idx, block_idx, lse_idx, workspace, cx, stream));
 }
 
 int msa_fwd(const msa_problem_t* p, const void* q, const void* k, const void* v,
@@ -265,22 +307,12 @@ int msa_fwd(const msa_problem_t* p, const void* q, const void* k, const void* v,
   int rc = check_problem(p, &s);
   if (rc) return rc;
   if (s.B == 0 || s.N == 0) return MSA_OK;
-  if (!q || !k || !v || !block_idx || !o || !lse) return MSA_ERR_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(block_idx) || !aligned16(o) ||
-      !aligned16(lse))
-    return MSA_ERR_ARG;
+  if ((rc = check_fwd_args(q, k, v, block_idx, o, lse))) return rc;
   if (!workspace || workspace_bytes < ws_fwd(s)) return MSA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MSA_ERR_ARG;
   Ctx cx;
   if ((rc = make_ctx(&cx))) return rc;
-  Plan pl = plan_carve(s, workspace);
-  uint8_t* w = static_cast<uint8_t*>(workspace) + plan_bytes(s);
-  const size_t parts = (size_t)s.rows_kv() * s.topk * s.G;
-  __nv_bfloat16* o_part = reinterpret_cast<__nv_bfloat16*>(w);
-  float* lse_part = reinterpret_cast<float*>(w + align256(parts * s.d * 2));
-  cudaError_t e = launch_plan(s, block_idx, 128 / s.G, pl, cx, stream);
-  if (e != cudaSuccess) return finish(e);
-  return finish(launch_attn_fwd(s, q, k, v, block_idx, pl, o_part, lse_part, o, lse, cx, stream));
+  return finish(run_fwd(s, q, k, v, block_idx, o, lse, workspace, cx, stream));
 }
 
 int msa_bwd(const msa_problem_t* p, const void* q, const void* k, const void* v, const void* o,
@@ -298,8 +330,7 @@ int msa_bwd(const msa_problem_t* p, const void* q, const void* k, const void* v,
   }
   const void* ins[] = {q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx,
                        dq, dk, dv, dq_idx, dk_idx};
-  for (const void* x : ins)
-    if (!x || !aligned16(x)) return MSA_ERR_ARG;
+  if ((rc = check_bwd_args(ins, sizeof(ins) / sizeof(ins[0])))) return rc;
   if (!workspace || workspace_bytes < bwd_ws_bytes(s)) return MSA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MSA_ERR_ARG;
   Ctx cx;

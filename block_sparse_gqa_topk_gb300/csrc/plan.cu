@@ -121,18 +121,25 @@ __global__ void plan_fill_kernel(const int32_t* __restrict__ block_idx, int64_t 
 // non-empty bin instead of once per entry.  Used, with the sorting fill above, when
 // the nb-bin histogram fits in smem.
 constexpr int kRowsPerCta = 1024;
-constexpr int kSmemBins = 16384;
+constexpr int kSmemBins = kPlanSmemBins;
 
-__global__ void plan_count_smem_kernel(const int32_t* __restrict__ block_idx, int N, int topk,
-                                       int nb, int* __restrict__ cnt, int* status) {
+__global__ void plan_count_smem_kernel(const int32_t* __restrict__ block_idx,
+                                       const int2* __restrict__ spans, const int* __restrict__ tab,
+                                       int B, int N, int H_kv, int topk, int nb,
+                                       int* __restrict__ cnt, int* status) {
   extern __shared__ int hist[];
-  const int chunks = (N + kRowsPerCta - 1) / kRowsPerCta;
-  const int64_t bg = blockIdx.x / chunks;
-  const int i0 = (blockIdx.x % chunks) * kRowsPerCta;
-  const int i1 = min(N, i0 + kRowsPerCta);
+  // CTA -> (sequence b, group g, chunk of kRowsPerCta rows)
+  const int g = blockIdx.x % H_kv;
+  int b, chunk;
+  if (!chunk_item(tab, B, (N + kRowsPerCta - 1) / kRowsPerCta, blockIdx.x / H_kv, &b, &chunk))
+    return;
+  const SeqSpan sp = seq_span(spans, b, N);
+  const int64_t bg = (int64_t)b * H_kv + g;
+  const int i0 = chunk * kRowsPerCta;
+  const int i1 = min(sp.len, i0 + kRowsPerCta);
   for (int c = threadIdx.x; c < nb; c += blockDim.x) hist[c] = 0;
   __syncthreads();
-  const int32_t* src = block_idx + (bg * N + i0) * topk;
+  const int32_t* src = block_idx + (sp.t0 * H_kv + (int64_t)g * sp.len + i0) * topk;
   const int n = (i1 - i0) * topk;
   for (int e0 = threadIdx.x; e0 < n; e0 += 8 * blockDim.x) {
     int cv[8];  // eight loads in flight before the histogram updates
@@ -168,19 +175,23 @@ constexpr int kFillEntries = 16384;  // entry index < 2^16, block id < kSmemBins
 constexpr int kFillPer = kFillEntries / kFillThreads;
 
 __global__ void __launch_bounds__(kFillThreads)
-    plan_fill_sort_kernel(const int32_t* __restrict__ block_idx, int N, int topk, int nb, int rows,
-                          const int* __restrict__ off, int* __restrict__ cursor,
+    plan_fill_sort_kernel(const int32_t* __restrict__ block_idx, const int2* __restrict__ spans,
+                          const int* __restrict__ tab, int B, int N, int H_kv, int topk, int nb,
+                          int rows, const int* __restrict__ off, int* __restrict__ cursor,
                           int* __restrict__ entries) {
   extern __shared__ int fill_smem[];
   int* hist = fill_smem;        // [nb] counts, then the bin's next position in `stage`
   int* delta = fill_smem + nb;  // [nb] global slot minus position in `stage`, per bin
   uint32_t* stage = reinterpret_cast<uint32_t*>(fill_smem + 2 * nb);  // (c << 16 | e), bin order
   __shared__ int s_warp[kFillThreads / 32];
-  const int chunks = (N + rows - 1) / rows;
-  const int64_t bg = blockIdx.x / chunks;
-  const int i0 = (blockIdx.x % chunks) * rows;
-  const int i1 = min(N, i0 + rows);
-  const int32_t* src = block_idx + (bg * N + i0) * topk;
+  const int g = blockIdx.x % H_kv;
+  int b, chunk;
+  if (!chunk_item(tab, B, (N + rows - 1) / rows, blockIdx.x / H_kv, &b, &chunk)) return;
+  const SeqSpan sp = seq_span(spans, b, N);
+  const int64_t bg = (int64_t)b * H_kv + g;
+  const int i0 = chunk * rows;
+  const int i1 = min(sp.len, i0 + rows);
+  const int32_t* src = block_idx + (sp.t0 * H_kv + (int64_t)g * sp.len + i0) * topk;
   const int n = (i1 - i0) * topk;
   int cv[kFillPer];  // block id of entry threadIdx.x + u kFillThreads, -1 if none
 #pragma unroll
@@ -245,6 +256,20 @@ __global__ void __launch_bounds__(kFillThreads)
 
 }  // namespace
 
+int varlen_chunk_rows(VarlenTable k, int topk) {
+  switch (k) {
+    case kTabIndexUnit: return 256;  // a pair of 128-query blocks
+    case kTabPlanCount: return kRowsPerCta;
+    case kTabRows64: return 64;
+    default: return topk >= kFillEntries ? 1 : kFillEntries / topk;
+  }
+}
+
+int64_t varlen_grid_items(const Shape& s, VarlenTable k) {
+  const int64_t r = varlen_chunk_rows(k, s.topk);
+  return (s.T + r - 1) / r + s.B;
+}
+
 size_t plan_bytes(const Shape& s) {
   const size_t keys = (size_t)s.keys();
   return align256(keys * 4) + 2 * align256((keys + 1) * 4) +
@@ -273,12 +298,15 @@ cudaError_t launch_plan(const Shape& s, const int32_t* block_idx, int qpt, const
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((n + 255) / 256);
   const bool smem_bins = s.nb <= kSmemBins;
+  if (s.packed() && !smem_bins) return cudaErrorNotSupported;  // callers reject this first
   const int64_t chunks = (s.N + kRowsPerCta - 1) / kRowsPerCta;
-  const unsigned grid_s = (unsigned)((int64_t)s.B * s.H_kv * chunks);
+  const unsigned grid_s = (unsigned)(
+      s.H_kv * (s.packed() ? varlen_grid_items(s, kTabPlanCount) : (int64_t)s.B * chunks));
   const size_t hist_bytes = (size_t)s.nb * sizeof(int);
-  const int fill_rows = s.topk >= kFillEntries ? 1 : kFillEntries / s.topk;
-  const unsigned grid_f =
-      (unsigned)((int64_t)s.B * s.H_kv * ((s.N + fill_rows - 1) / fill_rows));
+  const int fill_rows = varlen_chunk_rows(kTabPlanFill, s.topk);
+  const unsigned grid_f = (unsigned)(
+      s.H_kv * (s.packed() ? varlen_grid_items(s, kTabPlanFill)
+                           : (int64_t)s.B * ((s.N + fill_rows - 1) / fill_rows)));
   const size_t fill_bytes = 2 * hist_bytes + (size_t)fill_rows * s.topk * sizeof(uint32_t);
   if (n > 0 && smem_bins) {
     if (hist_bytes > 48 * 1024)
@@ -287,8 +315,9 @@ cudaError_t launch_plan(const Shape& s, const int32_t* block_idx, int qpt, const
     if (fill_bytes > 48 * 1024)
       cudaFuncSetAttribute(plan_fill_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)fill_bytes);
-    plan_count_smem_kernel<<<grid_s, 512, hist_bytes, st>>>(block_idx, s.N, s.topk, s.nb,
-                                                            pl.cnt, cx.status);
+    plan_count_smem_kernel<<<grid_s, 512, hist_bytes, st>>>(
+        block_idx, s.spans, s.tab(kTabPlanCount), s.B, s.N, s.H_kv, s.topk, s.nb, pl.cnt,
+        cx.status);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else if (n > 0) {
@@ -301,8 +330,9 @@ cudaError_t launch_plan(const Shape& s, const int32_t* block_idx, int qpt, const
   note_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (n > 0 && smem_bins) {
-    plan_fill_sort_kernel<<<grid_f, kFillThreads, fill_bytes, st>>>(block_idx, s.N, s.topk, s.nb, fill_rows,
-                                                           pl.off, pl.cnt, pl.entries);
+    plan_fill_sort_kernel<<<grid_f, kFillThreads, fill_bytes, st>>>(
+        block_idx, s.spans, s.tab(kTabPlanFill), s.B, s.N, s.H_kv, s.topk, s.nb, fill_rows,
+        pl.off, pl.cnt, pl.entries);
     note_launch();
     e = cudaGetLastError();
   } else if (n > 0) {

@@ -181,97 +181,114 @@ def attention(q, k, v, q_idx, k_idx, topk: int = 16, Bk: int = 128, scale=None, 
 
 
 # ---------------------------------------------------------------------------
-# Packed variable-length batches (cu_seqlens): each sequence is its own causal
-# problem; token axes are packed, per-sequence outputs are stored one sequence
-# after another in the single-sequence layout (see include/msa.h).
+# Packed variable-length batches (cu_seqlens on the device): each sequence is its own
+# causal problem; token axes are packed, per-sequence outputs are stored one sequence
+# after another in the single-sequence layout (see include/msa.h).  Every call runs a
+# fixed number of kernels whatever the number of sequences; cu_seqlens is checked on
+# the device (a bad batch writes nothing and sets the device status).
 # ---------------------------------------------------------------------------
-def _cu_list(cu_seqlens):
-    cu = cu_seqlens.tolist() if isinstance(cu_seqlens, torch.Tensor) else [int(x) for x in cu_seqlens]
-    if not cu or cu[0] != 0 or any(b < a for a, b in zip(cu, cu[1:])):
-        raise ValueError("cu_seqlens must start at 0 and be non-decreasing")
-    return cu
+def _cu_dev(cu_seqlens, dev):
+    if not isinstance(cu_seqlens, torch.Tensor):
+        cu_seqlens = torch.tensor([int(x) for x in cu_seqlens], dtype=torch.int32)
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.ndim != 1 or cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 tensor of num_seqs + 1 offsets")
+    return cu_seqlens.to(dev).contiguous()
+
+
+def _max_len(cu, max_seqlen):
+    """max_seqlen as given, else read from cu_seqlens (one device-to-host copy)."""
+    if max_seqlen is not None:
+        return int(max_seqlen)
+    return int((cu[1:] - cu[:-1]).max()) if cu.numel() > 1 else 0
 
 
 def varlen_view(flat: torch.Tensor, cu_seqlens, s: int, heads: int, per_row: int = 1):
     """Sequence s of a packed per-sequence output: [heads, L_s, per_row] (block_idx:
     heads = H_kv, per_row = topk; lse_idx: H_kv, 1; lse: H_q, 1)."""
-    cu = _cu_list(cu_seqlens)
+    cu = cu_seqlens.tolist() if isinstance(cu_seqlens, torch.Tensor) else list(cu_seqlens)
     a, b = cu[s] * heads * per_row, cu[s + 1] * heads * per_row
     return flat[a:b].view(heads, cu[s + 1] - cu[s], per_row)
 
 
-def msa_index_topk_varlen(q_idx, k_idx, cu_seqlens, topk: int = 16, *, H_q=None, d=None,
-                          Bk: int = 128, causal: bool = True, scale_idx=None,
+def msa_index_topk_varlen(q_idx, k_idx, cu_seqlens, topk: int = 16, *, max_seqlen=None, H_q=None,
+                          d=None, Bk: int = 128, causal: bool = True, scale_idx=None,
                           with_lse: bool = True):
-    """q_idx [T,H_kv,d_idx], k_idx [T,d_idx] -> packed block_idx (int32, H_kv*T*topk) and
-    lse_idx (f32, H_kv*T) or None."""
+    """q_idx [T,H_kv,d_idx], k_idx [T,d_idx], cu_seqlens (int32, num_seqs + 1) -> packed
+    block_idx (int32, H_kv*T*topk) and lse_idx (f32, H_kv*T) or None."""
     _need(q_idx, "q_idx", ndim=3)
     _need(k_idx, "k_idx", ndim=2)
-    cu = _cu_list(cu_seqlens)
     T, H_kv, d_idx = q_idx.shape
-    if cu[-1] != T or tuple(k_idx.shape) != (T, d_idx):
-        raise ValueError("q_idx/k_idx token axes must equal cu_seqlens[-1]")
-    prob = make_problem(1, 0, H_q or H_kv, H_kv, d or 128, d_idx, topk, Bk, causal, None, scale_idx)
+    if tuple(k_idx.shape) != (T, d_idx):
+        raise ValueError("q_idx and k_idx must share the token axis")
     dev = q_idx.device
+    cu = _cu_dev(cu_seqlens, dev)
+    n = cu.numel() - 1
+    prob = make_problem(1, _max_len(cu, max_seqlen), H_q or H_kv, H_kv, d or 128, d_idx, topk, Bk,
+                        causal, None, scale_idx)
     block_idx = torch.empty(H_kv * T * topk, dtype=torch.int32, device=dev)
     lse_idx = torch.empty(H_kv * T, dtype=torch.float32, device=dev) if with_lse else None
-    nws = _lib.msa_workspace_size_varlen(prob, cu, _lib.MSA_WS_INDEX) if with_lse else 0
-    ws = _workspace(nws, dev) if with_lse else None
-    rc = _lib.msa_index_topk_varlen(prob, cu, _ptr(q_idx), _ptr(k_idx), _ptr(block_idx),
-                                    _ptr(lse_idx), _ptr(ws), nws, _stream(dev))
+    nws = _lib.msa_workspace_size_varlen(prob, n, T, _lib.MSA_WS_INDEX)
+    ws = _workspace(nws, dev)
+    rc = _lib.msa_index_topk_varlen(prob, _ptr(cu), n, T, _ptr(q_idx), _ptr(k_idx),
+                                    _ptr(block_idx), _ptr(lse_idx), _ptr(ws), nws, _stream(dev))
     _lib.check(rc, "msa_index_topk_varlen")
     return block_idx, lse_idx
 
 
-def msa_fwd_varlen(q, k, v, block_idx, cu_seqlens, topk: int, *, scale=None, Bk: int = 128,
-                   causal: bool = True, d_idx=64):
+def msa_fwd_varlen(q, k, v, block_idx, cu_seqlens, topk: int, *, max_seqlen=None, scale=None,
+                   Bk: int = 128, causal: bool = True, d_idx=64):
     """q [T,H_q,d], k, v [T,H_kv,d], packed block_idx -> o [T,H_q,d], packed lse (H_q*T)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, ndim=3)
     _need(block_idx, "block_idx", torch.int32, ndim=1)
-    cu = _cu_list(cu_seqlens)
     T, H_q, d = q.shape
     H_kv = k.shape[1]
-    if cu[-1] != T or block_idx.numel() != H_kv * T * topk:
-        raise ValueError("token axes must equal cu_seqlens[-1]; block_idx must be H_kv*T*topk")
-    prob = make_problem(1, 0, H_q, H_kv, d, d_idx, topk, Bk, causal, scale, None)
+    if block_idx.numel() != H_kv * T * topk:
+        raise ValueError("block_idx must hold H_kv*T*topk entries")
     dev = q.device
+    cu = _cu_dev(cu_seqlens, dev)
+    n = cu.numel() - 1
+    prob = make_problem(1, _max_len(cu, max_seqlen), H_q, H_kv, d, d_idx, topk, Bk, causal, scale,
+                        None)
     o = torch.empty_like(q)
     lse = torch.empty(H_q * T, dtype=torch.float32, device=dev)
-    nws = _lib.msa_workspace_size_varlen(prob, cu, _lib.MSA_WS_FWD)
+    nws = _lib.msa_workspace_size_varlen(prob, n, T, _lib.MSA_WS_FWD)
     ws = _workspace(nws, dev)
-    rc = _lib.msa_fwd_varlen(prob, cu, _ptr(q), _ptr(k), _ptr(v), _ptr(block_idx), _ptr(o),
-                             _ptr(lse), _ptr(ws), nws, _stream(dev))
+    rc = _lib.msa_fwd_varlen(prob, _ptr(cu), n, T, _ptr(q), _ptr(k), _ptr(v), _ptr(block_idx),
+                             _ptr(o), _ptr(lse), _ptr(ws), nws, _stream(dev))
     _lib.check(rc, "msa_fwd_varlen")
     return o, lse
 
 
 def msa_bwd_varlen(q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx, kl_weight: float,
-                   cu_seqlens, topk: int, *, scale=None, scale_idx=None, Bk: int = 128,
-                   causal: bool = True):
+                   cu_seqlens, topk: int, *, max_seqlen=None, scale=None, scale_idx=None,
+                   Bk: int = 128, causal: bool = True):
     """Fused backward over a packed batch: dict dq, dk, dv, dq_idx, dk_idx and kl (sum over
-    sequences)."""
+    every row of every sequence)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (q_idx, "q_idx")):
         _need(t, n, ndim=3)
     _need(k_idx, "k_idx", ndim=2)
     _need(lse, "lse", torch.float32, ndim=1)
     _need(lse_idx, "lse_idx", torch.float32, ndim=1)
     _need(block_idx, "block_idx", torch.int32, ndim=1)
-    cu = _cu_list(cu_seqlens)
     T, H_q, d = q.shape
     H_kv = k.shape[1]
     d_idx = q_idx.shape[2]
-    prob = make_problem(1, 0, H_q, H_kv, d, d_idx, topk, Bk, causal, scale, scale_idx)
     dev = q.device
+    cu = _cu_dev(cu_seqlens, dev)
+    n = cu.numel() - 1
+    prob = make_problem(1, _max_len(cu, max_seqlen), H_q, H_kv, d, d_idx, topk, Bk, causal, scale,
+                        scale_idx)
     out = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
            "dq_idx": torch.empty_like(q_idx), "dk_idx": torch.empty_like(k_idx),
            "kl": torch.empty(1, dtype=torch.float32, device=dev)}
-    nws = _lib.msa_workspace_size_varlen(prob, cu, _lib.MSA_WS_BWD)
+    nws = _lib.msa_workspace_size_varlen(prob, n, T, _lib.MSA_WS_BWD)
     ws = _workspace(nws, dev)
-    rc = _lib.msa_bwd_varlen(prob, cu, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
-                             _ptr(q_idx), _ptr(k_idx), _ptr(block_idx), _ptr(lse_idx), kl_weight,
-                             _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dq_idx"]),
-                             _ptr(out["dk_idx"]), _ptr(out["kl"]), _ptr(ws), nws, _stream(dev))
+    rc = _lib.msa_bwd_varlen(prob, _ptr(cu), n, T, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                             _ptr(dO), _ptr(q_idx), _ptr(k_idx), _ptr(block_idx), _ptr(lse_idx),
+                             kl_weight, _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                             _ptr(out["dq_idx"]), _ptr(out["dk_idx"]), _ptr(out["kl"]), _ptr(ws),
+                             nws, _stream(dev))
     _lib.check(rc, "msa_bwd_varlen")
     return out
 

@@ -182,3 +182,21 @@ def sample_rows(cfg: MSAConfig, n: int, seed: int) -> np.ndarray:
         picks.add(b * cfg.N)
         picks.add(b * cfg.N + cfg.N - 1)
     return np.array(sorted(picks), dtype=np.int64)
+
+
+def varlen_offsets(n: int, lo: int, hi: int, seed: int) -> list:
+    """cu_seqlens of a packed batch of n sequences whose lengths are drawn uniformly from
+    lo .. hi (inclusive, seeded): [0, L_0, L_0 + L_1, ...]."""
+    lens = np.random.default_rng(seed).integers(lo, hi + 1, size=n)
+    return [0] + np.cumsum(lens).astype(int).tolist()
+
+
+def varlen_offsets_total(n: int, total: int, lo: int, hi: int, seed: int) -> list:
+    """cu_seqlens of n sequences that fill exactly `total` tokens: seeded lengths drawn
+    log-uniformly from lo .. hi, scaled to the total and rounded, the rounding remainder
+    given to the last sequence."""
+    rng = np.random.default_rng(seed)
+    raw = np.exp(rng.uniform(np.log(lo), np.log(hi), size=n))
+    lens = np.maximum(1, np.floor(raw * total / raw.sum())).astype(np.int64)
+    lens[-1] += total - int(lens.sum())
+    return [0] + np.cumsum(lens).astype(int).tolist()

@@ -141,39 +141,50 @@ int msa_bwd(const msa_problem_t* p, const void* q, const void* k, const void* v,
 
 /*
  * Packed variable-length batches (the variable-length view of the sparse attention,
- * Flash-MSA article, tech.kuratif.com, ¶7).  num_seqs sequences share one token axis:
- * sequence s holds tokens cu_seqlens[s] .. cu_seqlens[s+1]-1 of every packed tensor,
- * whose layouts are the single-sequence ones with the batch axis dropped:
+ * Flash-MSA article, tech.kuratif.com, ¶7).  num_seqs sequences share one token axis of
+ * total_tokens tokens: sequence s holds tokens cu_seqlens[s] .. cu_seqlens[s+1]-1 of
+ * every packed tensor, whose layouts are the single-sequence ones with the batch axis
+ * dropped:
  *   q, o, dO, dq [T][H_q][d];  k, v, dk, dv [T][H_kv][d];  q_idx, dq_idx [T][H_kv][d_idx];
- *   k_idx, dk_idx [T][d_idx]   (T = cu_seqlens[num_seqs]).
+ *   k_idx, dk_idx [T][d_idx]   (T = total_tokens).
  * Each sequence is its own causal problem (its blocks start at its first token; its
- * last block may be ragged); p->B and p->N are ignored.  Per-sequence outputs are
- * packed sequence after sequence, each in the single-sequence layout:
+ * last block may be ragged).  Per-sequence outputs are packed sequence after sequence,
+ * each in the single-sequence layout:
  *   block_idx: [H_kv][L_s][topk] at element offset cu_seqlens[s] * H_kv * topk;
  *   lse_idx:   [H_kv][L_s]       at cu_seqlens[s] * H_kv;
  *   lse:       [H_q][L_s]        at cu_seqlens[s] * H_q.
- * cu_seqlens is a HOST array of num_seqs + 1 int32: cu_seqlens[0] = 0, non-decreasing,
- * and every sequence start a multiple of 4 (which keeps each per-sequence slice 16-byte
- * aligned); otherwise MSA_ERR_ARG before anything is enqueued.  Empty sequences are
- * allowed.  The workspace is sized by msa_workspace_size_varlen and reused by the
- * sequences in stream order; the backward's kl_out is the sum over sequences.  Errors
- * of a sequence's call are returned as they are (earlier sequences may have been
- * enqueued).
+ * cu_seqlens is a DEVICE array of num_seqs + 1 int32 (4-byte aligned), read by the
+ * kernels only: the host never waits for it.  p->N bounds every sequence's length (the
+ * batch's max_seqlen: it sizes the grids and the block space, ceil(N / 128) blocks per
+ * sequence and group, at most 16384); p->B is not read.  The rules, checked on the
+ * device: cu_seqlens[0] = 0, non-decreasing, cu_seqlens[num_seqs] <= total_tokens, every
+ * length <= p->N.  A batch that breaks one writes no output and sets the device status to
+ * MSA_ERR_ARG (msa_get_device_status).  Sequences may be empty and may start at any
+ * token.  Tokens from cu_seqlens[num_seqs] to total_tokens are outside every sequence:
+ * their output rows are not written (dk_idx included).
+ * Each call runs a fixed number of kernels whatever num_seqs is: one small kernel
+ * validates cu_seqlens and writes per-sequence spans and work tables into the head of
+ * the workspace, then the single-sequence kernels run over the whole batch.
+ * The workspace (256-byte aligned) is sized by msa_workspace_size_varlen for the call;
+ * msa_index_topk_varlen needs one even when lse_idx is NULL.  The backward's kl_out is
+ * the KL summed over every row of every sequence (weighted by kl_weight).
  */
-size_t msa_workspace_size_varlen(const msa_problem_t* p, const int32_t* cu_seqlens, int num_seqs,
+size_t msa_workspace_size_varlen(const msa_problem_t* p, int num_seqs, int total_tokens,
                                  int which);
 int msa_index_topk_varlen(const msa_problem_t* p, const int32_t* cu_seqlens, int num_seqs,
-                          const void* q_idx, const void* k_idx, int32_t* block_idx, float* lse_idx,
-                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
-int msa_fwd_varlen(const msa_problem_t* p, const int32_t* cu_seqlens, int num_seqs, const void* q,
-                   const void* k, const void* v, const int32_t* block_idx, void* o, float* lse,
-                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
-int msa_bwd_varlen(const msa_problem_t* p, const int32_t* cu_seqlens, int num_seqs, const void* q,
-                   const void* k, const void* v, const void* o, const float* lse, const void* dO,
-                   const void* q_idx, const void* k_idx, const int32_t* block_idx,
-                   const float* lse_idx, float kl_weight, void* dq, void* dk, void* dv,
-                   void* dq_idx, void* dk_idx, float* kl_out, void* workspace,
+                          int total_tokens, const void* q_idx, const void* k_idx,
+                          int32_t* block_idx, float* lse_idx, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+int msa_fwd_varlen(const msa_problem_t* p, const int32_t* cu_seqlens, int num_seqs,
+                   int total_tokens, const void* q, const void* k, const void* v,
+                   const int32_t* block_idx, void* o, float* lse, void* workspace,
                    size_t workspace_bytes, cudaStream_t stream);
+int msa_bwd_varlen(const msa_problem_t* p, const int32_t* cu_seqlens, int num_seqs,
+                   int total_tokens, const void* q, const void* k, const void* v, const void* o,
+                   const float* lse, const void* dO, const void* q_idx, const void* k_idx,
+                   const int32_t* block_idx, const float* lse_idx, float kl_weight, void* dq,
+                   void* dk, void* dv, void* dq_idx, void* dk_idx, float* kl_out,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Decode (inference): one new query token per sequence against its KV cache.

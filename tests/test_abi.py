@@ -107,20 +107,36 @@ def test_decode_and_fp8_entry_points_reject_bad_arguments_on_the_host():
     assert _lib.msa_quantize_kv_fp8(_prob(H_kv=0, H_q=0), 16, 16, 16, None) == _lib.MSA_ERR_SHAPE
 
 
-def test_varlen_offsets_are_validated_on_the_host():
-    p = _prob()
-    for bad in ([4, 8, 16], [0, 8, 4], [0, 6, 16]):  # start != 0, decreasing, start % 4
-        assert _lib.msa_workspace_size_varlen(p, bad, _lib.MSA_WS_FWD) == 0
-        assert _lib.msa_index_topk_varlen(p, bad, 16, 16, 16, None, None, 0, None) == _lib.MSA_ERR_ARG
-        assert _lib.msa_fwd_varlen(p, bad, 16, 16, 16, 16, 16, 16, 256, 1 << 30, None) == \
-            _lib.MSA_ERR_ARG
-    # a valid batch needs the largest sequence's workspace (the calls reuse one)
-    cu = [0, 1024, 1024, 3072, 3100]
+def test_varlen_arguments_are_checked_on_the_host():
+    # cu_seqlens lives on the device and is checked there; the host checks what it is
+    # given: sizes, pointers and the workspace.  p.N is the batch's max_seqlen.
+    p = _prob(N=4096)
+    assert _lib.msa_workspace_size_varlen(p, -1, 100, _lib.MSA_WS_FWD) == 0
+    assert _lib.msa_workspace_size_varlen(p, 2, -5, _lib.MSA_WS_FWD) == 0
+    assert _lib.msa_workspace_size_varlen(p, 2, 100, 7) == 0
+    assert _lib.msa_workspace_size_varlen(_prob(N=(1 << 21) + 128), 1, 100, _lib.MSA_WS_FWD) == 0
+    # the workspace grows with the packed tokens, not with num_seqs x max_seqlen
     for which in (_lib.MSA_WS_INDEX, _lib.MSA_WS_FWD, _lib.MSA_WS_BWD):
-        need = _lib.msa_workspace_size_varlen(p, cu, which)
-        one = _lib.msa_workspace_size(_prob(N=2048), which)
-        assert need >= one > 0
-    assert _lib.msa_fwd_varlen(p, cu, 16, 16, 16, 16, 16, 16, 256, 16, None) == _lib.MSA_ERR_WORKSPACE
+        packed = _lib.msa_workspace_size_varlen(p, 8, 8192, which)
+        fixed = _lib.msa_workspace_size(_prob(B=2, N=4096), which)
+        assert packed > 0 and packed < fixed + (1 << 20)
+        assert _lib.msa_workspace_size_varlen(p, 8, 16384, which) > packed
+    # empty batches are no-ops; a null or misaligned cu_seqlens is refused
+    assert _lib.msa_index_topk_varlen(p, None, 0, 100, None, None, None, None, None, 0, None) == \
+        _lib.MSA_OK
+    assert _lib.msa_fwd_varlen(p, None, 2, 0, None, None, None, None, None, None, None, 0,
+                               None) == _lib.MSA_OK
+    assert _lib.msa_index_topk_varlen(p, None, 2, 100, 16, 16, 16, None, 256, 1 << 20, None) == \
+        _lib.MSA_ERR_ARG
+    assert _lib.msa_index_topk_varlen(p, 18, 2, 100, 16, 16, 16, None, 256, 1 << 20, None) == \
+        _lib.MSA_ERR_ARG
+    # the index call needs the workspace head even without lse_idx
+    assert _lib.msa_index_topk_varlen(p, 16, 2, 100, 16, 16, 16, None, None, 0, None) == \
+        _lib.MSA_ERR_WORKSPACE
+    assert _lib.msa_fwd_varlen(p, 16, 2, 100, 16, 16, 16, 16, 16, 16, 256, 16, None) == \
+        _lib.MSA_ERR_WORKSPACE
+    assert _lib.msa_fwd_varlen(p, 16, 2, 100, 16, 16, 16, 16, 16, 16, 128, 1 << 30, None) == \
+        _lib.MSA_ERR_ARG  # workspace not 256-byte aligned
 
 
 def test_empty_problem_is_a_no_op():
