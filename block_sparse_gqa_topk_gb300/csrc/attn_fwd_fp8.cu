@@ -198,26 +198,34 @@ __global__ void __launch_bounds__(kThreads8, 1)
       const int chf = lt % CH;
       Cursor8 kc;
       int prev_key = -1, kv_loads = 0, kv_issued = 0;
-      for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
+      // a tile's key and entries (lane l holds query slots l + 32 m), fetched one tile
+      // ahead so the entry loads of tile u+1 overlap the copies of tile u
+      constexpr int NE = (QPT + 31) / 32;
+      int cur_key = 0, nxt_key = 0;
+      int my_ent[NE], nxt_ent[NE];
+      auto fetch = [&](int u, int& key, int (&ent)[NE]) {
         const int t = t_begin + u;
-        const int st = u % kStages8;
-        const int key = kc.at(p.toff, p.keys, t);
-        const int bg = key / p.nb, c = key - bg * p.nb;
-        const int b = bg / p.H_kv, g = bg - b * p.H_kv;
+        key = kc.at(p.toff, p.keys, t);
         const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * QPT;
         const int ne = min(QPT, __ldg(&p.off[key + 1]) - e0);
+#pragma unroll
+        for (int m = 0; m < NE; ++m) {
+          const int qs = lane + 32 * m;
+          ent[m] = qs < ne ? __ldg(&p.entries[e0 + qs]) : -1;
+        }
+      };
+      if (n_tiles > 0) fetch(0, cur_key, my_ent);
+      for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
+        const int st = u % kStages8;
+        const int key = cur_key;
+        if (u + 1 < n_tiles) fetch(u + 1, nxt_key, nxt_ent);
+        const int bg = key / p.nb, c = key - bg * p.nb;
+        const int b = bg / p.H_kv, g = bg - b * p.H_kv;
         if (!mbar_wait(&qempty[st], ((u / kStages8) & 1) ^ 1, p.wait_ns, abort_flag)) {
           *abort_flag = 1;
           break;
         }
         uint8_t* dq = sQ + st * L::kTile;
-        constexpr int NE = (QPT + 31) / 32;
-        int my_ent[NE];
-#pragma unroll
-        for (int m = 0; m < NE; ++m) {
-          const int qs = lane + 32 * m;
-          my_ent[m] = qs < ne ? __ldg(&p.entries[e0 + qs]) : -1;
-        }
         const uint8_t* qg = p.q8 + ((int64_t)b * p.N * p.H_kv * G + (int64_t)g * G) * kD8 + chf * 16;
         const int64_t qrow = (int64_t)p.H_kv * G * kD8;  // bytes between consecutive queries
 #pragma unroll 4
@@ -253,6 +261,9 @@ __global__ void __launch_bounds__(kThreads8, 1)
           ++kv_loads;
           prev_key = key;
         }
+        cur_key = nxt_key;
+#pragma unroll
+        for (int m = 0; m < NE; ++m) my_ent[m] = nxt_ent[m];
       }
       cp_async_wait<0>();
       fence_async();
@@ -328,15 +339,23 @@ __global__ void __launch_bounds__(kThreads8, 1)
       const int row = (warp & 3) * 32 + lane;  // TMEM lane
       uint8_t* sPw = sP + wg * L::kTile;
       Cursor8 kc;
-      for (int u = wg; u < n_tiles; u += 2) {
+      const int qi = row / G;
+      // the key and this row's entry of the warpgroup's next tile are fetched while the
+      // current tile is processed
+      auto fetch = [&](int u, int& key, int& ent) {
         const int t = t_begin + u;
-        const int b = wg;
-        const int key = kc.at(p.toff, p.keys, t);
-        const int bg = key / p.nb, c = key - bg * p.nb;
+        key = kc.at(p.toff, p.keys, t);
         const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * QPT;
         const int ne = min(QPT, __ldg(&p.off[key + 1]) - e0);
-        const int qi = row / G;
-        const int ent = qi < ne ? __ldg(&p.entries[e0 + qi]) : -1;
+        ent = qi < ne ? __ldg(&p.entries[e0 + qi]) : -1;
+      };
+      int nxt_key = 0, nxt_ent = -1;
+      if (wg < n_tiles) fetch(wg, nxt_key, nxt_ent);
+      for (int u = wg; u < n_tiles; u += 2) {
+        const int b = wg;
+        const int key = nxt_key, ent = nxt_ent;
+        if (u + 2 < n_tiles) fetch(u + 2, nxt_key, nxt_ent);
+        const int bg = key / p.nb, c = key - bg * p.nb;
         const int i = ent >> kSlotBits;
         const int bb = bg / p.H_kv, g = bg - bb * p.H_kv;
         // per-row score factor: log2(e) * scale * s_q(row) * s_k(block)

@@ -199,28 +199,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int lt = threadIdx.x - 256;  // 0 .. kLoadThreads-1
       KeyCursor kc;
       int prev_key = -1, kv_loads = 0, kv_issued = 0;
-      for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
+      // A tile's key and entries (once per warp: lane l holds query slots l + 32 m) are
+      // fetched one tile ahead, so the entry loads of tile u+1 are in flight while the
+      // rows of tile u are copied.
+      constexpr int NE = (QPT + 31) / 32;
+      int cur_key = 0, nxt_key = 0;
+      int my_ent[NE], nxt_ent[NE];
+      auto fetch = [&](int u, int& key, int (&ent)[NE]) {
         const int t = t_begin + u;
+        key = kc.at(p.toff, p.keys, t);
+        const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * QPT;
+        const int ne = min(QPT, __ldg(&p.off[key + 1]) - e0);
+#pragma unroll
+        for (int m = 0; m < NE; ++m) {
+          const int qs = lane + 32 * m;
+          ent[m] = qs < ne ? __ldg(&p.entries[e0 + qs]) : -1;
+        }
+      };
+      if (n_tiles > 0) fetch(0, cur_key, my_ent);
+      for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
         const int st = u % kQStages;
-        const int key = kc.at(p.toff, p.keys, t);
+        const int key = cur_key;
+        if (u + 1 < n_tiles) fetch(u + 1, nxt_key, nxt_ent);
         const int bg = key / p.nb, c = key - bg * p.nb;
         const int b = bg / p.H_kv, g = bg - b * p.H_kv;
         const SeqSpan sp = seq_span(p.spans, b, p.N);
-        const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * QPT;
-        const int ne = min(QPT, __ldg(&p.off[key + 1]) - e0);
         if (!mbar_wait(&qempty[st], ((u / kQStages) & 1) ^ 1, p.wait_ns, abort_flag)) {
           *abort_flag = 1;
           break;
         }
         uint8_t* dq = sQ + st * L::kTile;
-        // the tile's entries, loaded once per warp: lane l holds query slots l + 32 m
-        constexpr int NE = (QPT + 31) / 32;
-        int my_ent[NE];
-#pragma unroll
-        for (int m = 0; m < NE; ++m) {
-          const int qs = lane + 32 * m;
-          my_ent[m] = qs < ne ? __ldg(&p.entries[e0 + qs]) : -1;
-        }
         // Each thread copies one fixed 16-byte column (chf) of the rows r0, r0 + RS, ...:
         // the per-copy work is a shuffle for the row's entry, one multiply-add for the
         // source and the swizzled destination.
@@ -267,6 +275,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ++kv_loads;
           prev_key = key;
         }
+        cur_key = nxt_key;
+#pragma unroll
+        for (int m = 0; m < NE; ++m) my_ent[m] = nxt_ent[m];
       }
       cp_async_wait<0>();
       fence_proxy_async_smem();
@@ -351,15 +362,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int row = (warp & 3) * 32 + lane;  // TMEM lane
       uint8_t* sPw = sP + wg * 2 * L::kHalf;
       KeyCursor kc;
-      for (int u = wg; u < n_tiles; u += 2) {
+      const int qi = row / G;
+      // the key and this row's entry of the warpgroup's next tile are fetched while the
+      // current tile is processed
+      auto fetch = [&](int u, int& key, int& ent) {
         const int t = t_begin + u;
-        const int b = wg;
-        const int key = kc.at(p.toff, p.keys, t);
-        const int bg = key / p.nb, c = key - bg * p.nb;
+        key = kc.at(p.toff, p.keys, t);
         const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * QPT;
         const int ne = min(QPT, __ldg(&p.off[key + 1]) - e0);
-        const int qi = row / G;
-        const int ent = qi < ne ? __ldg(&p.entries[e0 + qi]) : -1;
+        ent = qi < ne ? __ldg(&p.entries[e0 + qi]) : -1;
+      };
+      int nxt_key = 0, nxt_ent = -1;
+      if (wg < n_tiles) fetch(wg, nxt_key, nxt_ent);
+      for (int u = wg; u < n_tiles; u += 2) {
+        const int b = wg;
+        const int key = nxt_key, ent = nxt_ent;
+        if (u + 2 < n_tiles) fetch(u + 2, nxt_key, nxt_ent);
+        const int bg = key / p.nb, c = key - bg * p.nb;
         const int i = ent >> kSlotBits;
         const int rowv = opaque(row), lanev = opaque(lane);
         bool ok = __all_sync(0xffffffffu, mbar_wait(&sfull[b], (u >> 1) & 1, p.wait_ns, abort_flag));

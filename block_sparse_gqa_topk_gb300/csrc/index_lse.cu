@@ -11,14 +11,15 @@
 // Work unit: a tile is one key block c of one (batch, group) and up to 128 of the
 // queries whose block set holds c (the inverted lists of plan.cu with 128 queries
 // per tile).  Per CTA (persistent, a contiguous range of tiles):
-//   warps 8-11  loaders: gather the tile's 128 q_idx rows with cp.async into a
+//   warps 12-15 loaders: gather the tile's 128 q_idx rows with cp.async into a
 //               4-stage ring in the swizzled K-major layout tcgen05 reads; one
 //               thread TMA-loads the block's k_idx tile into a 2-deep buffer;
-//   warp 12     TMEM owner + one MMA thread: S = Q_idx K_idx^T (128 x 128, K = d_idx)
+//   warp 16     TMEM owner + one MMA thread: S = Q_idx K_idx^T (128 x 128, K = d_idx)
 //               into a 4-slot TMEM ring;
-//   warps 0-7   two warpgroups taking alternate tiles (thread = row = TMEM lane):
+//   warps 0-11  three warpgroups taking every third tile (thread = row = TMEM lane):
 //               tcgen05.ld the row's 128 scores, causal mask, max, exp2 sum, and the
 //               partial lse of (row, slot).
+// Loaders and softmax warps fetch a tile's key and entries one tile ahead of its use.
 // A second kernel merges the k partials of every row.  The exp2 throughput of the
 // SM bounds the first kernel: 128 x 128 exponentials per tile.
 #include <cudaTypedefs.h>
@@ -30,7 +31,10 @@
 namespace msa {
 namespace {
 
-constexpr int kThreads = 416;  // warps 0-7 softmax, 8-11 loaders, 12 MMA + TMEM owner
+constexpr int kSoftWG = 3;      // softmax warpgroups, taking every third tile
+constexpr int kLoadWarp0 = 4 * kSoftWG;      // 4 loader warps
+constexpr int kMmaWarp = kLoadWarp0 + 4;     // MMA + TMEM owner
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr int kLoadThreads = 128;
 constexpr int kQStages = 4;
 constexpr int kSlots = 4;      // TMEM score slots of 128 fp32 columns
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 12) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
   }
@@ -149,24 +153,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
 
   if (n_tiles > 0) {
-    if (warp >= 8 && warp < 12) {
+    if (warp >= kLoadWarp0 && warp < kMmaWarp) {
       // ================================ loaders =================================
       // Per tile: (new block) TMA its k_idx tile -> gather q(u) -> publish q(u-1).
       // The k_idx wait is on the block two keys back: its last tile is at most u-2,
       // published in an earlier iteration, and the MMA thread releases the buffer
       // right after that tile's MMA.
-      const int lt = threadIdx.x - 256;
+      const int lt = threadIdx.x - 32 * kLoadWarp0;
       Cursor kc;
       int prev_key = -1, k_loads = 0, k_issued = 0;
-      for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
+      // Thread lt copies the 16-byte column chf of rows r0, r0 + RS, ...  A tile's key and
+      // the entries of these rows are fetched one tile ahead, so the entry loads of tile
+      // u+1 are in flight while the rows of tile u are copied.
+      constexpr int RS = kLoadThreads / CH;  // rows per pass
+      constexpr int NR = 128 / RS;           // rows per thread
+      const int r0 = lt / CH, chf = lt % CH;
+      int cur_key = 0, nxt_key = 0;
+      int cur_ent[NR], nxt_ent[NR];
+      auto fetch = [&](int u, int& key, int (&ent)[NR]) {
         const int t = t_begin + u;
+        key = kc.at(p.toff, p.keys, t);
+        const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * 128;
+        const int ne = min(128, __ldg(&p.off[key + 1]) - e0);
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+          const int r = r0 + RS * k;
+          ent[k] = r < ne ? __ldg(&p.entries[e0 + r]) : -1;
+        }
+      };
+      if (n_tiles > 0) fetch(0, cur_key, cur_ent);
+      for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
         const int st = u % kQStages;
-        const int key = kc.at(p.toff, p.keys, t);
+        const int key = cur_key;
+        if (u + 1 < n_tiles) fetch(u + 1, nxt_key, nxt_ent);
         const int bg = key / p.nb, c = key - bg * p.nb;
         const int b = bg / p.H_kv, g = bg - b * p.H_kv;
         const SeqSpan sp = seq_span(p.spans, b, p.N);
-        const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * 128;
-        const int ne = min(128, __ldg(&p.off[key + 1]) - e0);
         if (key != prev_key) {
           if (lt == 0) {
             const int kb = k_loads & 1;
@@ -187,14 +209,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         uint8_t* dq = sQ + st * L::kTile;
-#pragma unroll 4
-        for (int x = lt; x < 128 * CH; x += kLoadThreads) {
-          const int r = x / CH, ch = x % CH;
-          const int ent = r < ne ? __ldg(&p.entries[e0 + r]) : -1;
-          const bool ok = ent >= 0;
-          const int i = ok ? (ent >> kSlotBits) : 0;
-          const int64_t src = ((sp.t0 + i) * p.H_kv + g) * DI + ch * 8;
-          cp_async_16(dq + swz<RB>(r, ch), p.q_idx + src, ok);
+        const __nv_bfloat16* qg = p.q_idx + (sp.t0 * p.H_kv + g) * DI + chf * 8;
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+          const int r = r0 + RS * k;
+          const bool ok = cur_ent[k] >= 0;
+          const int i = ok ? (cur_ent[k] >> kSlotBits) : 0;
+          cp_async_16(dq + swz<RB>(r, chf), qg + (int64_t)i * p.H_kv * DI, ok);
         }
         cp_async_commit();
         if (u >= 1) {
@@ -202,6 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           mbar_arrive(&qfull[(u - 1) % kQStages]);
         }
+        cur_key = nxt_key;
+#pragma unroll
+        for (int k = 0; k < NR; ++k) cur_ent[k] = nxt_ent[k];
       }
       cp_async_wait<0>();
       fence_proxy_async_smem();
@@ -210,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lt == 0)
         for (int n = max(0, k_issued - 2); n < k_issued; ++n)
           mbar_wait(&kfull[n & 1], (n >> 1) & 1, 1000000000ull);
-    } else if (warp == 12) {
+    } else if (warp == kMmaWarp) {
       // ============================== MMA issuer ================================
       if (lane == 0) {
         constexpr uint32_t idesc = umma_idesc_bf16_f32(128, 128);
@@ -254,22 +278,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      // ====================== row log-sum-exp: warps 0-7 ========================
+      // ====================== row log-sum-exp: warps 0-11 =======================
       const int wg = warp >> 2;
       const int row = (warp & 3) * 32 + lane;  // TMEM lane
       const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
       const float sl2 = p.scale_log2;
       Cursor kc;
-      for (int u = wg; u < n_tiles; u += 2) {
+      // the key and this row's entry of the warpgroup's next tile are fetched while the
+      // current tile is processed
+      auto fetch = [&](int u, int& key, int& ent) {
         const int t = t_begin + u;
+        key = kc.at(p.toff, p.keys, t);
+        const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * 128;
+        const int ne = min(128, __ldg(&p.off[key + 1]) - e0);
+        ent = row < ne ? __ldg(&p.entries[e0 + row]) : -1;
+      };
+      int nxt_key = 0, nxt_ent = -1;
+      if (wg < n_tiles) fetch(wg, nxt_key, nxt_ent);
+      for (int u = wg; u < n_tiles; u += kSoftWG) {
         const int sl = u % kSlots;
-        const int key = kc.at(p.toff, p.keys, t);
+        const int key = nxt_key, ent = nxt_ent;
+        if (u + kSoftWG < n_tiles) fetch(u + kSoftWG, nxt_key, nxt_ent);
         const int bg = key / p.nb, c = key - bg * p.nb;
         const int b = bg / p.H_kv, g = bg - b * p.H_kv;
         const SeqSpan sp = seq_span(p.spans, b, p.N);
-        const int e0 = __ldg(&p.off[key]) + (t - __ldg(&p.toff[key])) * 128;
-        const int ne = min(128, __ldg(&p.off[key + 1]) - e0);
-        const int ent = row < ne ? __ldg(&p.entries[e0 + row]) : -1;
         const int i = ent >> kSlotBits;
         const bool ok =
             __all_sync(0xffffffffu, mbar_wait(&sfull[sl], (u / kSlots) & 1, p.wait_ns, abort_flag));
@@ -345,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) set_status(p.status, MSA_ERR_DEVICE_TIMEOUT);
-  if (warp == 12) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
