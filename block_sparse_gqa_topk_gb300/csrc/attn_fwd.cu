@@ -16,9 +16,11 @@ namespace msa {
 namespace {
 
 // o[b,i,h] and lse[b,h,i] from the k partials of each (b, g, i) row.  One warp per
-// row: the partials of one slot are G*D contiguous bf16 (all heads of the group), read
-// as 16-byte chunks; the per-(slot, head) weights exp(lse_s - lse) come from shared
-// memory, computed by G lanes.  Up to 32 slots (every selected set).
+// row.  The (slot, head) lse partials of the row are contiguous: lane l reads pairs
+// l, l + 32, ... at once (head l % G, since G divides 32), and shuffles across the lanes
+// of one head give its max and sum; the weights exp(lse_s - lse) go to shared memory.
+// The partials of one slot are G*D contiguous bf16 (all heads of the group), read as
+// 16-byte chunks, eight loads a lane in flight at a time.  Up to 32 slots.
 template <int D, int G>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(
     const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
@@ -27,6 +29,8 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
     int topk, int nb) {
   constexpr int TC = G * D / 8;              // 16-byte chunks per slot
   constexpr int CPL = (TC + 31) / 32;        // chunks per lane
+  constexpr int NP = (32 * G + 31) / 32;     // (slot, head) pairs per lane, 32 slots at most
+  constexpr int SB = CPL >= 8 ? 1 : 8 / CPL;  // slots in flight: 8 loads per lane
   __shared__ float wts[8][32 * G];
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t rkv = (int64_t)blockIdx.x * 8 + wib;  // t0*H_kv + g*len + i
@@ -37,46 +41,71 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
   const SeqSpan sp = rp.sp;
   const int32_t* sel = block_idx + rkv * topk;
   float* w = wts[wib];
-  if (lane < G) {
-    const int h = lane;
-    float m = -INFINITY;
-    for (int s = 0; s < topk; ++s) {
-      const int c = __ldg(&sel[s]);
-      if (c >= 0 && c < nb) m = fmaxf(m, __ldg(&lse_part[(rkv * topk + s) * G + h]));
+  const int npair = topk * G;
+  float ls[NP];
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < NP; ++j) {
+    const int pr = lane + 32 * j;
+    ls[j] = -INFINITY;
+    if (pr < npair) {
+      const int c = __ldg(&sel[pr / G]);
+      if (c >= 0 && c < nb) ls[j] = __ldg(&lse_part[rkv * npair + pr]);
     }
-    float l = 0.f;
-    for (int s = 0; s < topk; ++s) {
-      const int c = __ldg(&sel[s]);
-      const float ls = (c >= 0 && c < nb) ? __ldg(&lse_part[(rkv * topk + s) * G + h]) : -INFINITY;
-      const float e = ls == -INFINITY ? 0.f : __expf(ls - m);
-      w[s * G + h] = e;
-      l += e;
-    }
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    for (int s = 0; s < topk; ++s) w[s * G + h] *= inv;
-    lse[sp.t0 * H_kv * G + (int64_t)(g * G + h) * sp.len + i] = m + logf(l);
+    m = fmaxf(m, ls[j]);
   }
+#pragma unroll
+  for (int o = G; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float l = 0.f;
+#pragma unroll
+  for (int j = 0; j < NP; ++j) {
+    ls[j] = ls[j] == -INFINITY ? 0.f : __expf(ls[j] - m);
+    l += ls[j];
+  }
+#pragma unroll
+  for (int o = G; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+  for (int j = 0; j < NP; ++j) {
+    const int pr = lane + 32 * j;
+    if (pr < npair) w[pr] = ls[j] * inv;
+  }
+  if (lane < G) lse[sp.t0 * H_kv * G + (int64_t)(g * G + lane) * sp.len + i] = m + logf(l);
   __syncwarp();
   float acc[CPL][8];
 #pragma unroll
   for (int x = 0; x < CPL; ++x)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[x][e] = 0.f;
-  for (int s = 0; s < topk; ++s) {
-    const int c = __ldg(&sel[s]);
-    if (c < 0 || c >= nb) continue;  // same for every lane
-    const uint4* src = reinterpret_cast<const uint4*>(o_part + (rkv * topk + s) * G * D);
+  const uint4* src = reinterpret_cast<const uint4*>(o_part + rkv * topk * G * D);
+  for (int s0 = 0; s0 < topk; s0 += SB) {
+    uint4 raw[SB][CPL];
 #pragma unroll
-    for (int x = 0; x < CPL; ++x) {
-      const int ch = lane + 32 * x;
-      if (ch < TC) {
-        const float wt = w[s * G + (ch * 8) / D];
-        const uint4 raw = __ldg(&src[ch]);
-        const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    for (int j = 0; j < SB; ++j) {
+      const int s = s0 + j;
+      const int c = s < topk ? __ldg(&sel[s]) : -1;
+      const bool valid = c >= 0 && c < nb;  // partials of unused slots were never written
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[x][2 * e] += wt * __low2float(pr[e]);
-          acc[x][2 * e + 1] += wt * __high2float(pr[e]);
+      for (int x = 0; x < CPL; ++x) {
+        const int ch = lane + 32 * x;
+        raw[j][x] = (valid && ch < TC) ? __ldg(&src[s * TC + ch]) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < SB; ++j) {
+      const int s = s0 + j;
+      if (s >= topk) break;
+#pragma unroll
+      for (int x = 0; x < CPL; ++x) {
+        const int ch = lane + 32 * x;
+        if (ch < TC) {
+          const float wt = w[s * G + (ch * 8) / D];
+          const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw[j][x]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[x][2 * e] += wt * __low2float(pr[e]);
+            acc[x][2 * e + 1] += wt * __high2float(pr[e]);
+          }
         }
       }
     }

@@ -509,12 +509,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t (&r)[32] = r2[hh];
 #pragma unroll
             for (int x = 0; x < 32; x += 8) {
-              uint4 w;
-              w.x = pack_bf16(__uint_as_float(r[x + 0]) * inv, __uint_as_float(r[x + 1]) * inv);
-              w.y = pack_bf16(__uint_as_float(r[x + 2]) * inv, __uint_as_float(r[x + 3]) * inv);
-              w.z = pack_bf16(__uint_as_float(r[x + 4]) * inv, __uint_as_float(r[x + 5]) * inv);
-              w.w = pack_bf16(__uint_as_float(r[x + 6]) * inv, __uint_as_float(r[x + 7]) * inv);
-              *reinterpret_cast<uint4*>(stg + sw128_row(lanev, 4 * hh + x / 8)) = w;
+              const float2 iv = make_float2(inv, inv);
+              uint32_t wv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 y = fmul2(
+                    make_float2(__uint_as_float(r[x + 2 * e]), __uint_as_float(r[x + 2 * e + 1])), iv);
+                wv[e] = pack_bf16(y.x, y.y);
+              }
+              *reinterpret_cast<uint4*>(stg + sw128_row(lanev, 4 * hh + x / 8)) =
+                  make_uint4(wv[0], wv[1], wv[2], wv[3]);
             }
           }
           __syncwarp();

@@ -312,63 +312,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int jlim = ent >= 0 ? min(i, sp.len - 1) - c * 128 : -1;  // last valid column
         const bool full = __all_sync(0xffffffffu, jlim >= 127);
-        float m = -INFINITY;  // running max of the raw scores
-        float l0 = 0.f, l1 = 0.f;
+        // One pass over the row: the exp2 offset is the max of its first 32 columns
+        // (column 0, the block's first key, is visible to every real row).  The lse is
+        // exact for any offset; only overflow matters, so a row sum above 2^64 (a later
+        // score far above the offset) takes the exact row max and a second pass.  The
+        // TMEM slot is handed back after that check.
+        const uint32_t srow = tmem + lane_base + 128 * sl;
+        auto exp_sum = [&](const uint32_t (&r)[64], int c0, float ms, float2& acc) {
+          if (full) {  // packed pairs: one FFMA2 and one FADD2 per two scores
+            const float2 scl = make_float2(sl2, sl2), off = make_float2(-ms, -ms);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t ra[32], rb[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + 128 * sl + 64 * hh, ra);
-          tmem_ld_32x32b_x32(tmem + lane_base + 128 * sl + 64 * hh + 32, rb);
-          tmem_wait_ld();
-          uint32_t r[64];
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            r[x] = ra[x];
-            r[32 + x] = rb[x];
-          }
-          if (hh == 1) {  // the slot is in registers: hand it back to the MMA
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tfree[sl]);
-          }
-          float cm = -INFINITY;
-          if (full) {
-#pragma unroll
-            for (int x = 0; x < 64; x += 2)
-              cm = fmax3(cm, __uint_as_float(r[x]), __uint_as_float(r[x + 1]));
+            for (int x = 0; x < 64; x += 2) {
+              const float2 a =
+                  ffma2(make_float2(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), scl, off);
+              acc = fadd2(acc, make_float2(ex2_fast(a.x), ex2_fast(a.y)));
+            }
           } else {
 #pragma unroll
-            for (int x = 0; x < 64; x += 2)
-              cm = fmax3(cm, 64 * hh + x <= jlim ? __uint_as_float(r[x]) : -INFINITY,
-                         64 * hh + x + 1 <= jlim ? __uint_as_float(r[x + 1]) : -INFINITY);
-          }
-          const float nm = fmaxf(m, cm);
-          if (nm != -INFINITY) {
-            const float ms = nm * sl2;
-            const float rescale = ex2_fast(m * sl2 - ms);  // 0 while m = -inf
-            l0 *= rescale;
-            l1 *= rescale;
-            if (full) {
-#pragma unroll
-              for (int x = 0; x < 64; x += 2) {
-                l0 += ex2_fast(__uint_as_float(r[x]) * sl2 - ms);
-                l1 += ex2_fast(__uint_as_float(r[x + 1]) * sl2 - ms);
-              }
-            } else {
-#pragma unroll
-              for (int x = 0; x < 64; x += 2) {
-                l0 += 64 * hh + x <= jlim ? ex2_fast(__uint_as_float(r[x]) * sl2 - ms) : 0.f;
-                l1 += 64 * hh + x + 1 <= jlim ? ex2_fast(__uint_as_float(r[x + 1]) * sl2 - ms)
-                                              : 0.f;
-              }
+            for (int x = 0; x < 64; x += 2) {
+              acc.x += c0 + x <= jlim ? ex2_fast(__uint_as_float(r[x]) * sl2 - ms) : 0.f;
+              acc.y += c0 + x + 1 <= jlim ? ex2_fast(__uint_as_float(r[x + 1]) * sl2 - ms) : 0.f;
             }
-            m = nm;
           }
+        };
+        auto load64 = [&](uint32_t (&r)[64], int c0) {
+          tmem_ld_32x32b_x32(srow + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld_32x32b_x32(srow + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+          tmem_wait_ld();
+        };
+        float ms;
+        float2 acc = make_float2(0.f, 0.f);
+        {
+          uint32_t r[64];
+          load64(r, 0);
+          float m0 = -INFINITY;
+#pragma unroll
+          for (int x = 0; x < 32; x += 2)
+            m0 = fmax3(m0, full || x <= jlim ? __uint_as_float(r[x]) : -INFINITY,
+                       full || x + 1 <= jlim ? __uint_as_float(r[x + 1]) : -INFINITY);
+          ms = m0 == -INFINITY ? 0.f : m0 * sl2;
+          exp_sum(r, 0, ms, acc);
+          load64(r, 64);
+          exp_sum(r, 64, ms, acc);
         }
+        float l = acc.x + acc.y;
+        if (__any_sync(0xffffffffu, l > 0x1p64f)) {  // rare: exact max, second pass
+          float m = -INFINITY;
+#pragma unroll 1
+          for (int h = 0; h < 4; ++h) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(srow + 32 * h, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+              m = fmaxf(m, 32 * h + x <= jlim ? __uint_as_float(r[x]) : -INFINITY);
+          }
+          ms = m == -INFINITY ? 0.f : m * sl2;
+          acc = make_float2(0.f, 0.f);
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 64) {
+            uint32_t r[64];
+            load64(r, c0);
+            exp_sum(r, c0, ms, acc);
+          }
+          l = acc.x + acc.y;
+        }
+        // the scores are in registers: hand the slot back to the MMA
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tfree[sl]);
         if (ent >= 0) {
-          const float l = l0 + l1;
           p.lse_part[(sp.t0 * p.H_kv + (int64_t)g * sp.len + i) * p.topk + (ent & kSlotMask)] =
-              l > 0.f ? (m * sl2 + log2f(l)) * kLn2 : -INFINITY;
+              l > 0.f ? (ms + log2f(l)) * kLn2 : -INFINITY;
         }
       }
     }
@@ -383,23 +398,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// lse_idx[b,g,i] = log-sum-exp over the row's valid slots of the partial lse.
+// lse_idx[b,g,i] = log-sum-exp over the row's valid slots of the partial lse.  A row's
+// slots are read by W consecutive lanes (W = topk rounded up to a power of two, at most
+// 32; 32 / W rows per warp), each lane keeping a running (max, sum) over its slots; the
+// pairs are merged across the row's lanes by shuffles.
+__device__ __forceinline__ void lse_merge(float& m, float& l, float m2, float l2) {
+  const float mm = fmaxf(m, m2);
+  l = mm == -INFINITY ? 0.f : l * __expf(m - mm) + l2 * __expf(m2 - mm);
+  m = mm;
+}
+
 __global__ void lse_combine_kernel(const float* __restrict__ lse_part,
                                    const int32_t* __restrict__ block_idx,
                                    float* __restrict__ lse_idx, const int2* __restrict__ spans,
-                                   int B, int N, int H_kv, int64_t rows, int topk, int nb) {
-  const int64_t r = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (r >= rows) return;
-  RowPos rp;
-  if (spans && !row_pos(spans, B, N, H_kv, r, &rp)) return;  // tokens outside every sequence
-  const int32_t* sel = block_idx + r * topk;
-  float m = -INFINITY;
-  for (int s = 0; s < topk; ++s)
-    if (sel[s] >= 0 && sel[s] < nb) m = fmaxf(m, lse_part[r * topk + s]);
-  float l = 0.f;
-  for (int s = 0; s < topk; ++s)
-    if (sel[s] >= 0 && sel[s] < nb) l += __expf(lse_part[r * topk + s] - m);
-  lse_idx[r] = m + logf(l);
+                                   int B, int N, int H_kv, int64_t rows, int topk, int nb, int W) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t r = warp * (32 / W) + lane / W;
+  const int sl = lane % W;
+  bool live = r < rows;
+  if (live && spans) {
+    RowPos rp;
+    live = row_pos(spans, B, N, H_kv, r, &rp);  // tokens outside every sequence
+  }
+  float m = -INFINITY, l = 0.f;
+  if (live) {
+    for (int s = sl; s < topk; s += W) {
+      const int c = __ldg(&block_idx[r * topk + s]);
+      if (c < 0 || c >= nb) continue;
+      lse_merge(m, l, __ldg(&lse_part[r * topk + s]), 1.f);
+    }
+  }
+  for (int o = W / 2; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+    lse_merge(m, l, m2, l2);
+  }
+  if (live && sl == 0) lse_idx[r] = m + logf(l);
 }
 
 template <int DI>
@@ -447,8 +482,11 @@ cudaError_t launch_index_lse(const Shape& s, const void* q_idx, const void* k_id
   cudaError_t e = DI == 64 ? launch_lse_tc<64>(tk, prm, cx, st) : launch_lse_tc<32>(tk, prm, cx, st);
   if (e != cudaSuccess) return e;
   const int64_t rows = s.rows_kv();
-  lse_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(
-      lse_part, block_idx, lse_idx, s.spans, s.B, s.N, s.H_kv, rows, s.topk, s.nb);
+  int W = 1;
+  while (W < s.topk && W < 32) W <<= 1;
+  const int64_t warps = (rows + (32 / W) - 1) / (32 / W);
+  lse_combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+      lse_part, block_idx, lse_idx, s.spans, s.B, s.N, s.H_kv, rows, s.topk, s.nb, W);
   note_launch();
   return cudaGetLastError();
 }
