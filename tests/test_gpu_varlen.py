@@ -6,7 +6,8 @@ The whole GPU chain runs over the packed batch: selection, index LSE, forward an
 fused backward with the KL summed over sequences.  Each sequence's GPU block sets are
 checked by the near-tie rule, and the oracle then runs on exactly those sets, so every
 row of every sequence is compared.  Batches: a mix of a long, an empty, a ragged and a
-short sequence at odd token offsets; G = 8 with d = 128; and 64 short ragged sequences.
+short sequence at odd token offsets; G = 16, 8 and 2 with d = 128, G = 1 with d = 64; and
+64 short ragged sequences.
 The number of kernel launches of a call does not depend on the number of sequences.
 """
 import numpy as np
@@ -28,6 +29,14 @@ CU8 = [0, 2561, 2564, 4095, 4096]
 # 64 short ragged sequences (lengths 1 .. 700, seeded; two of them emptied), k = 4 so the
 # selection is sparse in the longer ones; the packed axis ends with tokens outside every
 # sequence
+# G = 16, 2 and 1 (the backward's 16 G-row chunks), d = 128 and 64
+CFG16 = synth.CONFIGS["8k"].with_(name="varlen-g16", B=1, N=3000, H_q=32, H_kv=2, topk=8, seed=55)
+CU16 = [0, 1200, 1201, 2333, 3000]
+CFG2 = synth.CONFIGS["8k"].with_(name="varlen-g2", B=1, N=2600, H_q=8, H_kv=4, topk=6, n_needle=1,
+                                  seed=56)
+CU2 = [0, 129, 1300, 2600]
+CFG1 = synth.CONFIGS["tiny"].with_(name="varlen-g1", N=2200, H_q=4, H_kv=4, topk=3, seed=57)
+CU1 = [0, 700, 700, 1957, 2150]
 CFG64 = synth.CONFIGS["tiny"].with_(name="varlen-64", N=20480, seed=53)
 _LENS = np.diff(synth.varlen_offsets(64, 1, 700, seed=54))
 _LENS[[5, 40]] = 0
@@ -52,8 +61,9 @@ def _chain(cfg, cu, d, w, max_seqlen=None):
     return bi, li, o, lse, g
 
 
-@pytest.mark.parametrize("cfg,cu", [(CFG, CU), (CFG8, CU8), (CFG64, CU64)],
-                         ids=["tiny_mix", "g8_d128", "64_ragged"])
+@pytest.mark.parametrize("cfg,cu", [(CFG, CU), (CFG8, CU8), (CFG16, CU16), (CFG2, CU2), (CFG1, CU1),
+                                    (CFG64, CU64)],
+                         ids=["tiny_mix", "g8_d128", "g16_d128", "g2_d128", "g1_d64", "64_ragged"])
 def test_varlen_chain_matches_oracle_per_sequence(cfg, cu):
     h = host_inputs(cfg)
     T = cu[-1]
