@@ -458,12 +458,17 @@ __global__ void __launch_bounds__(kThreads8, 1)
           for (int h = 0; h < 2; ++h) {
 #pragma unroll
             for (int x = 0; x < 32; x += 8) {
-              uint4 w;
-              w.x = pack_bf16(__uint_as_float(r2[h][x + 0]) * inv, __uint_as_float(r2[h][x + 1]) * inv);
-              w.y = pack_bf16(__uint_as_float(r2[h][x + 2]) * inv, __uint_as_float(r2[h][x + 3]) * inv);
-              w.z = pack_bf16(__uint_as_float(r2[h][x + 4]) * inv, __uint_as_float(r2[h][x + 5]) * inv);
-              w.w = pack_bf16(__uint_as_float(r2[h][x + 6]) * inv, __uint_as_float(r2[h][x + 7]) * inv);
-              *reinterpret_cast<uint4*>(stg + sw_row(lane, 4 * h + x / 8)) = w;
+              const float2 iv = make_float2(inv, inv);
+              uint32_t wv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {  // packed pairs: one FMUL2 per two values
+                const float2 y = fmul2(
+                    make_float2(__uint_as_float(r2[h][x + 2 * e]), __uint_as_float(r2[h][x + 2 * e + 1])),
+                    iv);
+                wv[e] = pack_bf16(y.x, y.y);
+              }
+              *reinterpret_cast<uint4*>(stg + sw_row(lane, 4 * h + x / 8)) =
+                  make_uint4(wv[0], wv[1], wv[2], wv[3]);
             }
           }
           __syncwarp();
