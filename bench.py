@@ -488,6 +488,45 @@ def timed_workload(torch, ops, _lib, cfg, d, stream, steps, warmup, barrier=None
             "flops": flops, "sum_T": sum_T, "launches": launches, "clocks": clk, "steps": K}
 
 
+def graph_step(torch, ops, cfg, d, kl_weight=None, replays=10):
+    """One whole step (index scoring + top-k + index LSE, forward, fused backward) on the
+    device-resident inputs `d`, captured once in a CUDA graph and replayed: the step
+    without per-launch host overhead, which bounds the small workloads.  The library
+    allocates nothing and queues only memsets and kernels on the caller's stream, so the
+    captured calls are the eager ones.  Returns ms per replayed step."""
+    w = kl_weight if kl_weight is not None else cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N)
+
+    def step():
+        bi, li = ops.msa_index_topk(d["q_idx"], d["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d)
+        o, lse = ops.msa_fwd(d["q"], d["k"], d["v"], bi, scale=cfg.scale, d_idx=cfg.d_idx)
+        return ops.msa_bwd(d["q"], d["k"], d["v"], o, lse, d["dO"], d["q_idx"], d["k_idx"], bi, li,
+                           w, scale=cfg.scale)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):  # the workspace is sized before the capture
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(replays):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / replays
+    del graph
+    return ms
+
+
 def workload_summary(cfg, r, peak_tf):
     """Per-workload record: ms per step, per forward (index branch + sparse attention)
     and per backward, the index scoring + top-k kernel alone, tokens/s, and each
@@ -708,6 +747,13 @@ def run_ours(args, cfg, rank, world):
 
     # ---- every other seeded workload: the same step timed on its own inputs ----
     workloads = {cfg.name: workload_summary(cfg, r, peak_tf)}
+    if world == 1 and not args.no_graph:
+        gms = graph_step(torch, ops, cfg, d, kl_weight=w, replays=5)
+        workloads[cfg.name]["graph"] = {"ms_per_step": gms,
+                                        "tokens_per_s": cfg.B * cfg.N / (gms / 1000.0)}
+        st = ops.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status after the graph replay: {_lib.status_string(st)}")
     others = [] if (args.no_workloads or world > 1) else [n for n in WORKLOAD_ORDER
                                                           if n != cfg.name]
     if others:
@@ -720,6 +766,14 @@ def run_ours(args, cfg, rank, world):
             del hw
             rw = timed_workload(torch, ops, _lib, wc, dw, stream, WORKLOAD_STEPS[n], args.warmup)
             workloads[n] = workload_summary(wc, rw, peak_tf)
+            if not args.no_graph:
+                gms = graph_step(torch, ops, wc, dw, replays=max(3, WORKLOAD_STEPS[n]))
+                workloads[n]["graph"] = {"ms_per_step": gms,
+                                         "tokens_per_s": wc.B * wc.N / (gms / 1000.0)}
+                st = ops.device_status()
+                if st != 0:
+                    raise RuntimeError(f"{n}: device status after the graph replay: "
+                                       f"{_lib.status_string(st)}")
             del dw
         ops.release_workspace()
         torch.cuda.empty_cache()
@@ -776,6 +830,8 @@ def main():
                     help="skip the FP8 (E4M3) forward leg")
     ap.add_argument("--no-warmup-leg", action="store_true",
                     help="skip the indexer warm-up (dense set) leg")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay timing of each workload")
     ap.add_argument("--no-varlen-leg", action="store_true",
                     help="skip the packed variable-length batch leg")
     ap.add_argument("--varlen-only", action="store_true",
