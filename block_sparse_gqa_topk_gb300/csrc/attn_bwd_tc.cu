@@ -28,7 +28,8 @@
 //     E2  dQ^T from TMEM (thread = d) -> bf16 per-slot partials
 // Chunk u+1's (1)(2) overlap chunk u's E2.  After the block's last chunk dK, dV and
 // dk_idx (TMEM) are written once: no atomics on dk/dv/dk_idx.
-// Warps 8-9: loaders (cp.async gathers of q, dO, q_idx rows and k_idx; TMA for K, V).
+// Warp 8: loader (TMA boxes for q, G head rows per query, q_idx rows, K, V and k_idx;
+// cp.async for the per-row scalars).  Warp 9: cp.async gather of the chunk's dO rows.
 // Warp 10: TMEM owner and MMA issuer.
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -41,7 +42,7 @@ namespace {
 
 constexpr int kThreads = 352;  // 11 warps
 constexpr int kEpiWarps = 8;
-constexpr int kLoadThreads = 64;
+constexpr int kLoadArrivals = 96;  // per chunk: warp 8 (plain stores + cp.async), warp 9 (cp.async)
 // rows per chunk: 64 (64/G queries) for G >= 4; 16 G (16 queries) for G = 1, 2, so a
 // chunk never holds more than the 16 query slots of the z and dk_idx MMAs
 __host__ __device__ constexpr int rows_per_chunk(int G) { return G >= 4 ? 64 : 16 * G; }
@@ -59,7 +60,7 @@ struct BwdTcParams {
   float* dki_part;
   double* kl_acc;
   int64_t keys;
-  int B, N, H_kv, nb, topk, DI;
+  int B, N, T, H_kv, nb, topk, DI;
   float scale, scale_log2, sidx, sidx_log2, w;
   uint64_t wait_ns;
   int* status;
@@ -132,6 +133,8 @@ constexpr uint32_t cDK = 0, cDV = 128, cST = 256, cDPT = 320, cDQT = 384, cDKI =
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_qi, const __grid_constant__ CUtensorMap tm_ki,
                   const BwdTcParams p) {
   constexpr int R = rows_per_chunk(G);  // rows per chunk
   constexpr int RW = R / 2;             // rows per warpgroup
@@ -167,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(kvfull, 1);
     mbar_init(kvempty, 1 + kEpiWarps);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&qfull[s], kLoadThreads);
+      mbar_init(&qfull[s], kLoadArrivals);
       mbar_init(&bempty[s], 1);
     }
     for (int s = 0; s < 3; ++s) mbar_init(&sempty[s], 1 + kEpiWarps);
@@ -195,56 +198,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 8 || warp == 9) {
-    // ================================= loaders ==================================
-    const int lt = threadIdx.x - 256;  // 0..63
+  if (warp == 8) {
+    // ================================== loader ==================================
+    // One warp, lane q = query slot q of the chunk.  The rows of a query are its G
+    // heads, consecutive in q and dO, so each is one TMA box per 64-column half,
+    // written straight into the swizzled K-major operand layout (the 128-byte swizzle
+    // follows the shared-memory address, so a box of G rows may start at any row).
+    // Padding slots read past the token axis and land as zeros.  The per-row scalars
+    // are 4-byte cp.async copies; the stage is published when the TMA bytes, every
+    // lane's copies (cp.async arrive) and every lane's plain stores (arrive) are in.
     int u = 0, nkeys = 0, kv_issued = 0;  // nkeys: blocks with at least one chunk
     int next_ent = -1;
-    for (int64_t kk = blockIdx.x; kk < p.keys && !*abort_flag; kk += gridDim.x) {
+    bool ok = true;
+    for (int64_t kk = blockIdx.x; kk < p.keys && ok && !*abort_flag; kk += gridDim.x) {
       const int c = (int)(kk / BG), bg = (int)(kk % BG);
       const int b = bg / p.H_kv, g = bg - b * p.H_kv;
       const SeqSpan sp = seq_span(p.spans, b, p.N);
       const int key = bg * p.nb + c;
       const int e_begin = __ldg(&p.off[key]), e_end = __ldg(&p.off[key + 1]);
       const int nch = (e_end - e_begin + QC - 1) / QC;
-      for (int ch = 0; ch < nch && !*abort_flag; ++ch, ++u) {
-        const int s = u & 1;
-        // publish the previous chunk first: it is needed as soon as the chunk before
-        // it finishes, which may be before this chunk's stage is free
-        if (u >= 1) {
-          cp_async_wait<0>();
-          fence_async_smem();
-          mbar_arrive(&qfull[(u - 1) & 1]);
-        }
+      for (int ch = 0; ch < nch; ++ch, ++u) {
+        const int s = u & 1, s3 = u % 3;
         if (ch == 0) {
-          // new block: wait until the previous block is done with K, V and k_idx
-          if (nkeys > 0 && !mbar_wait(kvempty, (nkeys - 1) & 1, p.wait_ns, abort_flag)) {
-            *abort_flag = 1;
-            break;
-          }
-          if (lt == 0) {
-            mbar_arrive_expect_tx(kvfull, 2 * (D / 64) * L::kKH);
+          // new block: once the previous block is done with K, V and k_idx, load them
+          bool okk = true;
+          if (lane == 0) {
+            okk = nkeys == 0 || mbar_wait(kvempty, (nkeys - 1) & 1, p.wait_ns, abort_flag);
+            if (okk) {
+              mbar_arrive_expect_tx(kvfull, 2 * (D / 64) * L::kKH + L::kKH);
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-              tma_load_4d(sm + L::kK + h * L::kKH, &tm_k, kvfull, h * 64, g, sp.tn + c * 128, sp.tb);
-              tma_load_4d(sm + L::kV + h * L::kKH, &tm_v, kvfull, h * 64, g, sp.tn + c * 128, sp.tb);
+              for (int h = 0; h < D / 64; ++h) {
+                tma_load_4d(sm + L::kK + h * L::kKH, &tm_k, kvfull, h * 64, g, sp.tn + c * 128, sp.tb);
+                tma_load_4d(sm + L::kV + h * L::kKH, &tm_v, kvfull, h * 64, g, sp.tn + c * 128, sp.tb);
+              }
+              tma_load_3d(sm + L::kKi, &tm_ki, kvfull, 0, sp.tn + c * 128, sp.tb);
+              kv_issued = nkeys + 1;
             }
-            kv_issued = nkeys + 1;
           }
-          for (int x = lt; x < 128 * 8; x += kLoadThreads) {  // k_idx rows, zero-padded
-            const int r = x / 8, cc = x % 8;
-            const int j = c * 128 + r;
-            const bool ok = j < sp.len && cc * 8 < p.DI;
-            const int64_t src = (sp.t0 + (ok ? j : 0)) * p.DI + (ok ? cc * 8 : 0);
-            cp_async_16(sm + L::kKi + sw128(r, cc), p.k_idx + src, ok);
-          }
+          if (!(ok = __shfl_sync(0xffffffffu, okk, 0))) break;
         }
-        const int s3 = u % 3;
-        if (!mbar_wait(&bempty[s], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag) ||
-            !mbar_wait(&sempty[s3], ((u / 3) & 1) ^ 1, p.wait_ns, abort_flag)) {
-          *abort_flag = 1;
-          break;
-        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&bempty[s], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag) &&
+                                         mbar_wait(&sempty[s3], ((u / 3) & 1) ^ 1, p.wait_ns, abort_flag));
+        if (!ok) break;
         uint8_t* st = sm + L::kBig0 + s * L::kBig;       // q, dO
         uint8_t* ss = sm + L::kSmall0 + s3 * L::kSmall;  // q_idx, scalars
         const int q0 = e_begin + ch * QC;
@@ -256,58 +251,98 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nq1 = min(QC, e_end - q1);
           next_ent = (ch + 1 < nch && lane < nq1) ? __ldg(&p.entries[q1 + lane]) : -1;
         }
-        for (int x = lt; x < R * (D / 8); x += kLoadThreads) {
-          const int r = x / (D / 8), cc = x % (D / 8);
-          const int qi = r / G, h = r % G;
-          const int ent = __shfl_sync(0xffffffffu, my_ent, qi);
-          const bool ok = ent >= 0;
-          const int i = ok ? (ent >> kSlotBits) : 0;
-          const int64_t src = ((sp.t0 + i) * p.H_kv * G + g * G + h) * D + cc * 8;
-          const uint32_t o = (cc >> 3) * L::kQH + sw128(r, cc);
-          cp_async_16(st + L::kSQ + o, p.q + src, ok);
-          cp_async_16(st + L::kSdO + o, p.dO + src, ok);
-        }
-        for (int x = lt; x < kQS * 8; x += kLoadThreads) {
-          const int qi = x / 8, cc = x % 8;
-          const int ent = __shfl_sync(0xffffffffu, my_ent, qi);
-          const bool ok = ent >= 0 && cc * 8 < p.DI;
-          const int i = ok ? (ent >> kSlotBits) : 0;
-          const int64_t src = ((sp.t0 + i) * p.H_kv + g) * p.DI + (ok ? cc * 8 : 0);
-          cp_async_16(ss + L::kSQi + sw128(qi, cc), p.q_idx + src, ok);
-        }
-        {
-          const int r = lt, qi = (r / G) & 31, h = r % G;  // one row per loader thread
-          const int ent0 = __shfl_sync(0xffffffffu, my_ent, qi);
-          const int ent = r < R ? ent0 : -1;  // rows past the chunk: padding
-          const bool ok = ent >= 0;
-          const int ri = ok ? (ent >> kSlotBits) : -1;
-          const int64_t x = sp.t0 * p.H_kv * G + (int64_t)(g * G + h) * sp.len + (ok ? ri : 0);
-          cp_async_4(ss + L::kSLse + 4 * r, p.lse + x, ok);
-          cp_async_4(ss + L::kSD + 4 * r, p.Dv + x, ok);
-          reinterpret_cast<int*>(ss + L::kSRi)[r] = ri;
-          reinterpret_cast<int*>(ss + L::kSRp)[r] =
-              ok ? (int)(((sp.t0 * p.H_kv + (int64_t)g * sp.len + ri) * p.topk + (ent & kSlotMask)) * G +
-                         h)
-                 : -1;
-          if (lt < kQS) {
-            const bool okq = my_ent >= 0;
-            const int iq = okq ? (my_ent >> kSlotBits) : 0;
-            reinterpret_cast<int*>(ss + L::kSQiq)[lt] = okq ? iq : -1;
-            reinterpret_cast<int*>(ss + L::kSQp)[lt] =
-                okq ? (int)((sp.t0 * p.H_kv + (int64_t)g * sp.len + iq) * p.topk + (my_ent & kSlotMask))
-                    : -1;
-            cp_async_4(ss + L::kSLi + 4 * lt, p.lse_idx + sp.t0 * p.H_kv + (int64_t)g * sp.len + iq,
-                       okq);
+        if (lane == 0) mbar_expect_tx(&qfull[s], R * D * 2 + kQS * 128);
+        __syncwarp();
+        const bool okq = my_ent >= 0;
+        const int iq = okq ? (my_ent >> kSlotBits) : 0;
+        const int zq = okq ? (int)(sp.t0 + iq) : p.T;  // past the token axis: zeros
+        if (lane < QC) {
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            const uint32_t o = h * L::kQH + lane * G * 128;
+            tma_load_3d(st + L::kSQ + o, &tm_q, &qfull[s], h * 64, g * G, zq);
           }
         }
-        cp_async_commit();
+        if (lane < kQS) tma_load_3d(ss + L::kSQi + lane * 128, &tm_qi, &qfull[s], 0, g, zq);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {  // rows lane, lane + 32 of the 64-row scalar arrays
+          const int r = lane + 32 * k, qi = (r / G) & 31, h = r % G;
+          const int ent0 = __shfl_sync(0xffffffffu, my_ent, qi);
+          const int ent = r < R ? ent0 : -1;  // rows past the chunk: padding
+          const bool okr = ent >= 0;
+          const int ri = okr ? (ent >> kSlotBits) : -1;
+          const int64_t x = sp.t0 * p.H_kv * G + (int64_t)(g * G + h) * sp.len + (okr ? ri : 0);
+          cp_async_4(ss + L::kSLse + 4 * r, p.lse + x, okr);
+          cp_async_4(ss + L::kSD + 4 * r, p.Dv + x, okr);
+          reinterpret_cast<int*>(ss + L::kSRi)[r] = ri;
+          reinterpret_cast<int*>(ss + L::kSRp)[r] =
+              okr ? (int)(((sp.t0 * p.H_kv + (int64_t)g * sp.len + ri) * p.topk + (ent & kSlotMask)) * G + h)
+                  : -1;
+        }
+        if (lane < kQS) {
+          reinterpret_cast<int*>(ss + L::kSQiq)[lane] = okq ? iq : -1;
+          reinterpret_cast<int*>(ss + L::kSQp)[lane] =
+              okq ? (int)((sp.t0 * p.H_kv + (int64_t)g * sp.len + iq) * p.topk + (my_ent & kSlotMask)) : -1;
+          cp_async_4(ss + L::kSLi + 4 * lane, p.lse_idx + sp.t0 * p.H_kv + (int64_t)g * sp.len + iq, okq);
+        }
+        mbar_arrive(&qfull[s]);           // this lane's plain stores
+        cp_async_mbar_arrive(&qfull[s]);  // this lane's cp.async copies, once landed
       }
       if (nch > 0) ++nkeys;
     }
+    if (!ok) *abort_flag = 1;
+    // nothing may still be landing in shared memory when the CTA exits
     cp_async_wait<0>();
-    fence_async_smem();
-    if (u > 0 && !*abort_flag) mbar_arrive(&qfull[(u - 1) & 1]);
-    if (lt == 0 && kv_issued > 0) mbar_wait(kvfull, (kv_issued - 1) & 1, 1000000000ull);
+    if (lane == 0) {
+      for (int v = max(0, u - 2); v < u; ++v) mbar_wait(&qfull[v & 1], (v >> 1) & 1, 1000000000ull);
+      if (kv_issued > 0) mbar_wait(kvfull, (kv_issued - 1) & 1, 1000000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ================================ dO gather =================================
+    // The chunk's dO rows (G heads of each gathered query) by cp.async into the same
+    // swizzled layout, in parallel with warp 8's TMA boxes for q: the copy engines
+    // and the load/store path share the chunk's bytes.
+    int u = 0;
+    int next_ent = -1;
+    bool ok = true;
+    for (int64_t kk = blockIdx.x; kk < p.keys && ok && !*abort_flag; kk += gridDim.x) {
+      const int c = (int)(kk / BG), bg = (int)(kk % BG);
+      const int b = bg / p.H_kv, g = bg - b * p.H_kv;
+      const SeqSpan sp = seq_span(p.spans, b, p.N);
+      const int key = bg * p.nb + c;
+      const int e_begin = __ldg(&p.off[key]), e_end = __ldg(&p.off[key + 1]);
+      const int nch = (e_end - e_begin + QC - 1) / QC;
+      for (int ch = 0; ch < nch; ++ch, ++u) {
+        const int s = u & 1;
+        if (!(ok = __all_sync(0xffffffffu,
+                              mbar_wait(&bempty[s], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag))))
+          break;
+        const int q0 = e_begin + ch * QC;
+        const int nq = min(QC, e_end - q0);
+        const int my_ent = ch == 0 ? (lane < nq ? __ldg(&p.entries[q0 + lane]) : -1) : next_ent;
+        {
+          const int q1 = q0 + QC;
+          const int nq1 = min(QC, e_end - q1);
+          next_ent = (ch + 1 < nch && lane < nq1) ? __ldg(&p.entries[q1 + lane]) : -1;
+        }
+        uint8_t* st = sm + L::kBig0 + s * L::kBig + L::kSdO;
+        static_assert((R * (D / 8)) % 32 == 0, "whole passes of the warp");
+#pragma unroll 4
+        for (int x = lane; x < R * (D / 8); x += 32) {
+          const int r = x / (D / 8), cc = x % (D / 8);
+          const int qi = r / G, h = r % G;
+          const int ent = __shfl_sync(0xffffffffu, my_ent, qi);
+          const bool okr = ent >= 0;
+          const int i = okr ? (ent >> kSlotBits) : 0;
+          const int64_t src = ((sp.t0 + i) * p.H_kv * G + g * G + h) * D + cc * 8;
+          cp_async_16(st + (cc >> 3) * L::kQH + sw128(r, cc), p.dO + src, okr);
+        }
+        cp_async_mbar_arrive(&qfull[s]);
+      }
+    }
+    if (!ok) *abort_flag = 1;
+    cp_async_wait<0>();
   } else if (warp == 10) {
     // ================================ MMA issuer =================================
     if (lane == 0) {
@@ -353,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (u > 0 && !(ok = mbar_wait(b_e, (u - 1) & 1, p.wait_ns, abort_flag))) break;
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tc_mma_bf16(tmem + cZ, desc_k(aKi + k * 32), desc_k(aQi + k * 32), iz, k > 0);
+          for (int k = 0; k < 4; ++k)  // K = d_idx (the columns past it are zeros)
+            if (16 * k < p.DI) tc_mma_bf16(tmem + cZ, desc_k(aKi + k * 32), desc_k(aQi + k * 32), iz, k > 0);
           tc_commit(b_z);
           if (!(ok = mbar_wait(b_p, u & 1, p.wait_ns, abort_flag))) break;
           tc_fence_after();
@@ -388,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(mmadone, 0, 1000000000ull);
       }
     }
-  } else {
+  } else if (warp < 8) {
     // ============================= epilogue warps 0-7 =============================
     const int wg = warp >> 2;              // which 32 of the 64 row columns
     const int tl = (warp & 3) * 32 + lane; // TMEM lane: key (E1, block end), d (E2)
@@ -419,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* s_li = reinterpret_cast<const float*>(ss + L::kSLi);
         const uint8_t* sQi = ss + L::kSQi;
         ok = __all_sync(0xffffffffu, mbar_wait(&qfull[s], (u >> 1) & 1, p.wait_ns, abort_flag) &&
+                                         (ch > 0 || mbar_wait(kvfull, nkeys & 1, p.wait_ns, abort_flag)) &&
                                          mbar_wait(b_s, u & 1, p.wait_ns, abort_flag) &&
                                          mbar_wait(b_z, u & 1, p.wait_ns, abort_flag));
         if (!ok) break;
@@ -684,15 +720,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+struct BwdMaps {
+  CUtensorMap k, v, q, dO, qi, ki;
+};
+
 template <int D, int G>
-cudaError_t launch_dg(const BwdTcParams& prm, const CUtensorMap& tk, const CUtensorMap& tv,
-                      const Ctx& cx, cudaStream_t st) {
+cudaError_t launch_dg(const BwdTcParams& prm, const BwdMaps& m, const Ctx& cx, cudaStream_t st) {
   using L = BL<D, rows_per_chunk(G)>;
   auto kern = bwd_tc_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   kernel_event(MSA_KERNEL_BWD, true, st);
-  kern<<<cx.num_sms, kThreads, L::kAlloc, st>>>(tk, tv, prm);
+  kern<<<cx.num_sms, kThreads, L::kAlloc, st>>>(m.k, m.v, m.q, m.dO, m.qi, m.ki, prm);
   kernel_event(MSA_KERNEL_BWD, false, st);
   note_launch();
   return cudaGetLastError();
@@ -706,15 +745,33 @@ cudaError_t launch_attn_bwd_tc(const Shape& s, const void* q, const void* k, con
                                float kl_weight, const Plan& pl, __nv_bfloat16* dq_part,
                                __nv_bfloat16* dqi_part, float* dki_part, double* kl_acc, void* dk,
                                void* dv, const Ctx& cx, cudaStream_t st) {
-  CUtensorMap tk, tv;
-  const uint64_t dims[4] = {(uint64_t)s.d, (uint64_t)s.H_kv, s.tma_tokens(), s.tma_batches()};
-  const uint64_t strides[3] = {(uint64_t)s.d * 2, (uint64_t)s.H_kv * s.d * 2,
-                               s.tma_tokens() * s.H_kv * s.d * 2};
-  const uint32_t box[4] = {64, 1, 128, 1};
-  if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dims, strides, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dims, strides, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B))
+  // K, V: [tokens][H_kv][d] per batch, one (64-column, 128-key) box per half.
+  // q, dO: [T][H_q][d], one (64-column, G-head) box per query and half.
+  // q_idx: [T][H_kv][d_idx], one row box per query slot; k_idx: [tokens][d_idx] per
+  // batch, one 128-key box.  All 128-byte swizzled; the q_idx and k_idx boxes are 64
+  // columns wide whatever d_idx is, so with d_idx = 32 the upper half lands as zeros.
+  if (s.T >= 0x7fffffff) return cudaErrorInvalidValue;  // token coordinates are int32
+  BwdMaps m;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const uint64_t H_q = (uint64_t)s.H_kv * s.G, T = (uint64_t)s.T, DI = (uint64_t)s.d_idx;
+  const uint64_t dkv[4] = {(uint64_t)s.d, (uint64_t)s.H_kv, s.tma_tokens(), s.tma_batches()};
+  const uint64_t skv[3] = {(uint64_t)s.d * 2, (uint64_t)s.H_kv * s.d * 2,
+                           s.tma_tokens() * s.H_kv * s.d * 2};
+  const uint32_t bkv[4] = {64, 1, 128, 1};
+  const uint64_t dq[3] = {(uint64_t)s.d, H_q, T};
+  const uint64_t sq[2] = {(uint64_t)s.d * 2, H_q * s.d * 2};
+  const uint32_t bq[3] = {64, (uint32_t)s.G, 1};
+  const uint64_t dqi[3] = {DI, (uint64_t)s.H_kv, T};
+  const uint64_t sqi[2] = {DI * 2, (uint64_t)s.H_kv * DI * 2};
+  const uint32_t bqi[3] = {64, 1, 1};
+  const uint64_t dki[3] = {DI, s.tma_tokens(), s.tma_batches()};
+  const uint64_t ski[2] = {DI * 2, s.tma_tokens() * DI * 2};
+  const uint32_t bki[3] = {64, 128, 1};
+  if (!encode_tiled(&m.k, bf, 4, k, dkv, skv, bkv, sw) || !encode_tiled(&m.v, bf, 4, v, dkv, skv, bkv, sw) ||
+      !encode_tiled(&m.q, bf, 3, q, dq, sq, bq, sw) || !encode_tiled(&m.dO, bf, 3, dO, dq, sq, bq, sw) ||
+      !encode_tiled(&m.qi, bf, 3, q_idx, dqi, sqi, bqi, sw) ||
+      !encode_tiled(&m.ki, bf, 3, k_idx, dki, ski, bki, sw))
     return cudaErrorInvalidValue;
   BwdTcParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -736,6 +793,7 @@ cudaError_t launch_attn_bwd_tc(const Shape& s, const void* q, const void* k, con
   p.keys = s.keys();
   p.B = s.B;
   p.N = s.N;
+  p.T = (int)s.T;
   p.H_kv = s.H_kv;
   p.nb = s.nb;
   p.topk = s.topk;
@@ -749,11 +807,11 @@ cudaError_t launch_attn_bwd_tc(const Shape& s, const void* q, const void* k, con
   p.status = cx.status;
 #define MSA_BWD_G(DD)                                                  \
   switch (s.G) {                                                       \
-    case 1: return launch_dg<DD, 1>(p, tk, tv, cx, st);                \
-    case 2: return launch_dg<DD, 2>(p, tk, tv, cx, st);                \
-    case 4: return launch_dg<DD, 4>(p, tk, tv, cx, st);                \
-    case 8: return launch_dg<DD, 8>(p, tk, tv, cx, st);                \
-    default: return launch_dg<DD, 16>(p, tk, tv, cx, st);              \
+    case 1: return launch_dg<DD, 1>(p, m, cx, st);                \
+    case 2: return launch_dg<DD, 2>(p, m, cx, st);                \
+    case 4: return launch_dg<DD, 4>(p, m, cx, st);                \
+    case 8: return launch_dg<DD, 8>(p, m, cx, st);                \
+    default: return launch_dg<DD, 16>(p, m, cx, st);              \
   }
   if (s.d == 128) MSA_BWD_G(128)
   MSA_BWD_G(64)
