@@ -192,11 +192,14 @@ def warmup_leg(torch, ops, cfg, dev, stream, peak_tf, steps=5, warm=3):
          for n in ("q", "k", "v", "q_idx", "k_idx", "dO")}
     w = wc.kl_coef / (wc.B * wc.H_kv * wc.N)
 
+    plan = ops.new_plan(wc.B, wc.N, wc.H_q, wc.H_kv, wc.topk, d=wc.d, d_idx=wc.d_idx, device=dev)
+
     def step():
-        bi, li = ops.msa_index_topk(t["q_idx"], t["k_idx"], wc.topk, H_q=wc.H_q, d=wc.d)
-        o, lse = ops.msa_fwd(t["q"], t["k"], t["v"], bi, scale=wc.scale, d_idx=wc.d_idx)
+        bi, li = ops.msa_index_topk(t["q_idx"], t["k_idx"], wc.topk, H_q=wc.H_q, d=wc.d,
+                                    plan=plan)
+        o, lse = ops.msa_fwd(t["q"], t["k"], t["v"], bi, scale=wc.scale, d_idx=wc.d_idx, plan=plan)
         g = ops.msa_bwd(t["q"], t["k"], t["v"], o, lse, t["dO"], t["q_idx"], t["k_idx"], bi, li,
-                        w, scale=wc.scale)
+                        w, scale=wc.scale, plan=plan)
         return bi, g
 
     for _ in range(warm):
@@ -414,18 +417,24 @@ def timed_workload(torch, ops, _lib, cfg, d, stream, steps, warmup, barrier=None
     group-sharded mode `cfg` and `d` are this rank's groups, `kl_weight` uses the global
     group count and `after_bwd` is the exchange (all-reduce of dk_idx and the KL)."""
     w = kl_weight if kl_weight is not None else cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N)
+    # one plan (inverted lists of the step's block_idx) serves the index LSE, forward and
+    # backward of each step: built by the index call, read by the other two
+    plan = ops.new_plan(cfg.B, cfg.N, cfg.H_q, cfg.H_kv, cfg.topk, d=cfg.d, d_idx=cfg.d_idx,
+                        device=d["q"].device)
 
     def step(t, phase_ev=None):
         if phase_ev:
             phase_ev[0].record(stream)
-        bi, li = ops.msa_index_topk(t["q_idx"], t["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d)
+        bi, li = ops.msa_index_topk(t["q_idx"], t["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d,
+                                    plan=plan)
         if phase_ev:
             phase_ev[1].record(stream)
-        o, lse = ops.msa_fwd(t["q"], t["k"], t["v"], bi, scale=cfg.scale, d_idx=cfg.d_idx)
+        o, lse = ops.msa_fwd(t["q"], t["k"], t["v"], bi, scale=cfg.scale, d_idx=cfg.d_idx,
+                             plan=plan)
         if phase_ev:
             phase_ev[2].record(stream)
         g = ops.msa_bwd(t["q"], t["k"], t["v"], o, lse, t["dO"], t["q_idx"], t["k_idx"], bi, li, w,
-                        scale=cfg.scale)
+                        scale=cfg.scale, plan=plan)
         if after_bwd is not None:
             g = after_bwd(g)
         if phase_ev:
@@ -495,12 +504,16 @@ def graph_step(torch, ops, cfg, d, kl_weight=None, replays=10):
     allocates nothing and queues only memsets and kernels on the caller's stream, so the
     captured calls are the eager ones.  Returns ms per replayed step."""
     w = kl_weight if kl_weight is not None else cfg.kl_coef / (cfg.B * cfg.H_kv * cfg.N)
+    plan = ops.new_plan(cfg.B, cfg.N, cfg.H_q, cfg.H_kv, cfg.topk, d=cfg.d, d_idx=cfg.d_idx,
+                        device=d["q"].device)
 
     def step():
-        bi, li = ops.msa_index_topk(d["q_idx"], d["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d)
-        o, lse = ops.msa_fwd(d["q"], d["k"], d["v"], bi, scale=cfg.scale, d_idx=cfg.d_idx)
+        bi, li = ops.msa_index_topk(d["q_idx"], d["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d,
+                                    plan=plan)
+        o, lse = ops.msa_fwd(d["q"], d["k"], d["v"], bi, scale=cfg.scale, d_idx=cfg.d_idx,
+                             plan=plan)
         return ops.msa_bwd(d["q"], d["k"], d["v"], o, lse, d["dO"], d["q_idx"], d["k_idx"], bi, li,
-                           w, scale=cfg.scale)
+                           w, scale=cfg.scale, plan=plan)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -652,6 +665,8 @@ def run_ours(args, cfg, rank, world):
     kl_host = torch.empty(e2e_steps, dtype=torch.float32).pin_memory()
     h2d = sum(pinned[n].numel() * 2 for n in names)
     copy_streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    plan = ops.new_plan(cfg.B, cfg.N, cfg.H_q, cfg.H_kv, cfg.topk, d=cfg.d, d_idx=cfg.d_idx,
+                        device=dev)
     lanes = {"q_idx": 0, "q": 0, "k": 0, "k_idx": 1, "v": 1, "dO": 1}  # about 1.4 GB each
     landed = [{n: torch.cuda.Event() for n in names} for _ in range(2)]  # per set, per input
     consumed = [torch.cuda.Event() for _ in range(2)]  # the step reading set i is done
@@ -673,15 +688,17 @@ def run_ours(args, cfg, rank, world):
         t = bufs[i]
         for n in ("q_idx", "k_idx"):
             stream.wait_event(landed[i][n])
-        bi, li = ops.msa_index_topk(t["q_idx"], t["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d)
+        bi, li = ops.msa_index_topk(t["q_idx"], t["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d,
+                                    plan=plan)
         for n in ("q", "k", "v"):
             stream.wait_event(landed[i][n])
-        o, lse = ops.msa_fwd(t["q"], t["k"], t["v"], bi, scale=cfg.scale, d_idx=cfg.d_idx)
+        o, lse = ops.msa_fwd(t["q"], t["k"], t["v"], bi, scale=cfg.scale, d_idx=cfg.d_idx,
+                             plan=plan)
         if after_fwd is not None:
             after_fwd()
         stream.wait_event(landed[i]["dO"])
         g = ops.msa_bwd(t["q"], t["k"], t["v"], o, lse, t["dO"], t["q_idx"], t["k_idx"], bi, li,
-                        w, scale=cfg.scale)
+                        w, scale=cfg.scale, plan=plan)
         return after_bwd(g) if after_bwd is not None else g
 
     torch.cuda.synchronize()

@@ -31,7 +31,8 @@ EXPORTS = ("msa_workspace_size", "msa_index_topk", "msa_fwd", "msa_bwd",
            "msa_noalloc_scratch_bytes", "msa_version", "msa_workspace_size_varlen",
            "msa_index_topk_varlen", "msa_fwd_varlen", "msa_bwd_varlen",
            "msa_decode_workspace_size", "msa_decode", "msa_quantize_kv_fp8",
-           "msa_decode_fp8", "msa_quantize_fwd_fp8", "msa_fwd_fp8")
+           "msa_decode_fp8", "msa_quantize_fwd_fp8", "msa_fwd_fp8", "msa_plan_size",
+           "msa_index_topk_plan", "msa_fwd_plan", "msa_bwd_plan")
 
 MSA_KERNEL_INDEX = 0
 MSA_KERNEL_FWD = 1
@@ -76,6 +77,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp,
                             vp, vp, sz, vp]
     lib.msa_bwd.restype = i32
+    lib.msa_plan_size.argtypes = [P]
+    lib.msa_plan_size.restype = sz
+    lib.msa_index_topk_plan.argtypes = [P, vp, vp, vp, vp, vp, sz, vp, sz, vp]
+    lib.msa_index_topk_plan.restype = i32
+    lib.msa_fwd_plan.argtypes = [P, vp, vp, vp, vp, vp, sz, vp, vp, vp, sz, vp]
+    lib.msa_fwd_plan.restype = i32
+    lib.msa_bwd_plan.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, f32, vp, vp,
+                                 vp, vp, vp, vp, vp, sz, vp]
+    lib.msa_bwd_plan.restype = i32
     lib.msa_get_device_status.argtypes = [vp, ctypes.POINTER(i32)]
     lib.msa_get_device_status.restype = i32
     lib.msa_status_string.argtypes = [i32]
@@ -144,6 +154,28 @@ def msa_bwd(prob, q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx, kl_weig
     return load().msa_bwd(ctypes.byref(prob), q, k, v, o, lse, dO, q_idx, k_idx, block_idx,
                           lse_idx, float(kl_weight), dq, dk, dv, dq_idx, dk_idx, kl_out, ws,
                           ws_bytes, stream)
+
+
+def msa_plan_size(prob) -> int:
+    return int(load().msa_plan_size(ctypes.byref(prob)))
+
+
+def msa_index_topk_plan(prob, q_idx, k_idx, block_idx, lse_idx, plan, plan_bytes, ws, ws_bytes,
+                        stream) -> int:
+    return load().msa_index_topk_plan(ctypes.byref(prob), q_idx, k_idx, block_idx, lse_idx, plan,
+                                      plan_bytes, ws, ws_bytes, stream)
+
+
+def msa_fwd_plan(prob, q, k, v, block_idx, plan, plan_bytes, o, lse, ws, ws_bytes, stream) -> int:
+    return load().msa_fwd_plan(ctypes.byref(prob), q, k, v, block_idx, plan, plan_bytes, o, lse,
+                               ws, ws_bytes, stream)
+
+
+def msa_bwd_plan(prob, q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx, plan, plan_bytes,
+                 kl_weight, dq, dk, dv, dq_idx, dk_idx, kl_out, ws, ws_bytes, stream) -> int:
+    return load().msa_bwd_plan(ctypes.byref(prob), q, k, v, o, lse, dO, q_idx, k_idx, block_idx,
+                               lse_idx, plan, plan_bytes, float(kl_weight), dq, dk, dv, dq_idx,
+                               dk_idx, kl_out, ws, ws_bytes, stream)
 
 
 def msa_index_topk_noalloc(prob, q_idx, k_idx, block_idx, lse_idx, stream) -> int:

@@ -183,10 +183,17 @@ cudaError_t run_bwd(const Shape& s, const void* q, const void* k, const void* v,
                     const float* lse, const void* dO, const void* q_idx, const void* k_idx,
                     const int32_t* block_idx, const float* lse_idx, float kl_weight, void* dq,
                     void* dk, void* dv, void* dq_idx, void* dk_idx, float* kl_out, void* ws,
-                    const Ctx& cx, cudaStream_t st) {
+                    const Ctx& cx, cudaStream_t st, void* plan) {
   BwdWs w;
   carve(s, ws, &w);
-  cudaError_t e = launch_plan(s, block_idx, 64 / s.G, w.pl, cx, st);
+  cudaError_t e;
+  if (plan) {  // the step's shared plan (the backward reads its CSR only)
+    const SharedPlan sp = shared_plan_carve(s, plan);
+    e = launch_shared_plan_check(s, sp, cx, st);
+    w.pl = sp.idx;
+  } else {
+    e = launch_plan(s, block_idx, 64 / s.G, w.pl, cx, st);
+  }
   if (e != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(w.counter, 0, 256, st)) != cudaSuccess) return e;  // counter + KL
   {

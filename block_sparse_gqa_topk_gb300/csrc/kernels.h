@@ -84,6 +84,28 @@ Plan plan_carve(const Shape& s, void* ws);
 cudaError_t launch_plan(const Shape& s, const int32_t* block_idx, int qpt, const Plan& pl,
                         const Ctx& cx, cudaStream_t st);
 
+// A plan shared by the calls of one step, in a caller-owned buffer: a header naming the
+// problem (written last by the build), the CSR with tiles of 128 queries (index LSE; the
+// backward reads only the CSR) and a second tile split of 128 / G queries (forward).
+constexpr int kPlanHeaderInts = 8;
+constexpr size_t kPlanHeaderBytes = 256;
+constexpr int kPlanMagic = 0x4D534150;
+struct PlanHeader {
+  int v[kPlanHeaderInts];
+};
+struct SharedPlan {
+  int* hdr;
+  Plan idx;  // tiles of 128 queries
+  Plan fwd;  // the same CSR, tiles of 128 / G queries
+};
+PlanHeader plan_header(const Shape& s);
+size_t shared_plan_bytes(const Shape& s);
+SharedPlan shared_plan_carve(const Shape& s, void* buf);
+cudaError_t launch_shared_plan(const Shape& s, const int32_t* block_idx, const SharedPlan& sp,
+                               const Ctx& cx, cudaStream_t st);
+cudaError_t launch_shared_plan_check(const Shape& s, const SharedPlan& sp, const Ctx& cx,
+                                     cudaStream_t st);
+
 // Index branch: tcgen05 scoring + block max-pool + register top-k -> block_idx.
 cudaError_t launch_index_topk(const Shape& s, const void* q_idx, const void* k_idx,
                               int32_t* block_idx, const Ctx& cx, cudaStream_t st);
@@ -167,16 +189,19 @@ int check_index_args(const Shape& s, const void* q_idx, const void* k_idx,
 int check_fwd_args(const void* q, const void* k, const void* v, const int32_t* block_idx,
                    const void* o, const float* lse);
 int check_bwd_args(const void* const* ptrs, int n);
+// With `plan` (a shared plan buffer), run_index builds it and the others read it (after
+// a header check) instead of building their own in the workspace.
 cudaError_t run_index(const Shape& s, const void* q_idx, const void* k_idx, int32_t* block_idx,
-                      float* lse_idx, void* ws, const Ctx& cx, cudaStream_t st);
+                      float* lse_idx, void* ws, const Ctx& cx, cudaStream_t st,
+                      void* plan = nullptr);
 cudaError_t run_fwd(const Shape& s, const void* q, const void* k, const void* v,
                     const int32_t* block_idx, void* o, float* lse, void* ws, const Ctx& cx,
-                    cudaStream_t st);
+                    cudaStream_t st, void* plan = nullptr);
 cudaError_t run_bwd(const Shape& s, const void* q, const void* k, const void* v, const void* o,
                     const float* lse, const void* dO, const void* q_idx, const void* k_idx,
                     const int32_t* block_idx, const float* lse_idx, float kl_weight, void* dq,
                     void* dk, void* dv, void* dq_idx, void* dk_idx, float* kl_out, void* ws,
-                    const Ctx& cx, cudaStream_t st);
+                    const Ctx& cx, cudaStream_t st, void* plan = nullptr);
 
 // Launch bookkeeping (msa_api.cu): counts launches and records the profiling
 // events of msa_set_kernel_events around the named kernels.

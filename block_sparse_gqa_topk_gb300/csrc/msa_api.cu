@@ -127,24 +127,41 @@ int check_bwd_args(const void* const* ptrs, int n) {
 }
 
 cudaError_t run_index(const Shape& s, const void* q_idx, const void* k_idx, int32_t* block_idx,
-                      float* lse_idx, void* ws, const Ctx& cx, cudaStream_t st) {
+                      float* lse_idx, void* ws, const Ctx& cx, cudaStream_t st, void* plan) {
   cudaError_t e = launch_index_topk(s, q_idx, k_idx, block_idx, cx, st);
-  if (e != cudaSuccess || !lse_idx) return e;
-  Plan pl = plan_carve(s, ws);
+  if (e != cudaSuccess) return e;
+  Plan pl;
+  if (plan) {  // the step's shared plan, built once here
+    const SharedPlan sp = shared_plan_carve(s, plan);
+    if ((e = launch_shared_plan(s, block_idx, sp, cx, st)) != cudaSuccess) return e;
+    pl = sp.idx;
+  }
+  if (!lse_idx) return cudaSuccess;
   float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + plan_bytes(s));
-  if ((e = launch_plan(s, block_idx, 128, pl, cx, st)) != cudaSuccess) return e;
+  if (!plan) {
+    pl = plan_carve(s, ws);
+    if ((e = launch_plan(s, block_idx, 128, pl, cx, st)) != cudaSuccess) return e;
+  }
   return launch_index_lse(s, q_idx, k_idx, block_idx, pl, lse_part, lse_idx, cx, st);
 }
 
 cudaError_t run_fwd(const Shape& s, const void* q, const void* k, const void* v,
                     const int32_t* block_idx, void* o, float* lse, void* ws, const Ctx& cx,
-                    cudaStream_t st) {
-  Plan pl = plan_carve(s, ws);
+                    cudaStream_t st, void* plan) {
   uint8_t* w = static_cast<uint8_t*>(ws) + plan_bytes(s);
   const size_t parts = (size_t)s.rows_kv() * s.topk * s.G;
   __nv_bfloat16* o_part = reinterpret_cast<__nv_bfloat16*>(w);
   float* lse_part = reinterpret_cast<float*>(w + align256(parts * s.d * 2));
-  cudaError_t e = launch_plan(s, block_idx, 128 / s.G, pl, cx, st);
+  Plan pl;
+  cudaError_t e;
+  if (plan) {
+    const SharedPlan sp = shared_plan_carve(s, plan);
+    e = launch_shared_plan_check(s, sp, cx, st);
+    pl = sp.fwd;
+  } else {
+    pl = plan_carve(s, ws);
+    e = launch_plan(s, block_idx, 128 / s.G, pl, cx, st);
+  }
   if (e != cudaSuccess) return e;
   return launch_attn_fwd(s, q, k, v, block_idx, pl, o_part, lse_part, o, lse, cx, st);
 }
@@ -337,6 +354,77 @@ int msa_bwd(const msa_problem_t* p, const void* q, const void* k, const void* v,
   if ((rc = make_ctx(&cx))) return rc;
   return finish(run_bwd(s, q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx, kl_weight, dq,
                         dk, dv, dq_idx, dk_idx, kl_out, workspace, cx, stream));
+}
+
+size_t msa_plan_size(const msa_problem_t* p) {
+  Shape s;
+  if (check_problem(p, &s)) return 0;
+  return shared_plan_bytes(s);
+}
+
+static int check_plan(const Shape& s, const void* plan, size_t plan_bytes) {
+  if (!plan || (reinterpret_cast<uintptr_t>(plan) & 255) != 0) return MSA_ERR_ARG;
+  if (plan_bytes < shared_plan_bytes(s)) return MSA_ERR_WORKSPACE;
+  return MSA_OK;
+}
+
+int msa_index_topk_plan(const msa_problem_t* p, const void* q_idx, const void* k_idx,
+                        int32_t* block_idx, float* lse_idx, void* plan, size_t plan_bytes,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Shape s;
+  int rc = check_problem(p, &s);
+  if (rc) return rc;
+  if (s.B == 0 || s.N == 0) return MSA_OK;
+  if ((rc = check_index_args(s, q_idx, k_idx, block_idx))) return rc;
+  if ((rc = check_plan(s, plan, plan_bytes))) return rc;
+  if (lse_idx) {
+    if (!workspace || workspace_bytes < ws_index(s)) return MSA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MSA_ERR_ARG;
+  }
+  Ctx cx;
+  if ((rc = make_ctx(&cx))) return rc;
+  return finish(run_index(s, q_idx, k_idx, block_idx, lse_idx, workspace, cx, stream, plan));
+}
+
+int msa_fwd_plan(const msa_problem_t* p, const void* q, const void* k, const void* v,
+                 const int32_t* block_idx, void* plan, size_t plan_bytes, void* o, float* lse,
+                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Shape s;
+  int rc = check_problem(p, &s);
+  if (rc) return rc;
+  if (s.B == 0 || s.N == 0) return MSA_OK;
+  if ((rc = check_fwd_args(q, k, v, block_idx, o, lse))) return rc;
+  if ((rc = check_plan(s, plan, plan_bytes))) return rc;
+  if (!workspace || workspace_bytes < ws_fwd(s)) return MSA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MSA_ERR_ARG;
+  Ctx cx;
+  if ((rc = make_ctx(&cx))) return rc;
+  return finish(run_fwd(s, q, k, v, block_idx, o, lse, workspace, cx, stream, plan));
+}
+
+int msa_bwd_plan(const msa_problem_t* p, const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dO, const void* q_idx, const void* k_idx,
+                 const int32_t* block_idx, const float* lse_idx, void* plan, size_t plan_bytes,
+                 float kl_weight, void* dq, void* dk, void* dv, void* dq_idx, void* dk_idx,
+                 float* kl_out, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Shape s;
+  int rc = check_problem(p, &s);
+  if (rc) return rc;
+  if (!isfinite(kl_weight)) return MSA_ERR_ARG;
+  if (s.B == 0 || s.N == 0) {
+    if (kl_out) return finish(cudaMemsetAsync(kl_out, 0, sizeof(float), stream));
+    return MSA_OK;
+  }
+  const void* ins[] = {q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx,
+                       dq, dk, dv, dq_idx, dk_idx};
+  if ((rc = check_bwd_args(ins, sizeof(ins) / sizeof(ins[0])))) return rc;
+  if ((rc = check_plan(s, plan, plan_bytes))) return rc;
+  if (!workspace || workspace_bytes < bwd_ws_bytes(s)) return MSA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MSA_ERR_ARG;
+  Ctx cx;
+  if ((rc = make_ctx(&cx))) return rc;
+  return finish(run_bwd(s, q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx, kl_weight, dq,
+                        dk, dv, dq_idx, dk_idx, kl_out, workspace, cx, stream, plan));
 }
 
 }  // extern "C"

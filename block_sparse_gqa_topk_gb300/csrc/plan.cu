@@ -14,6 +14,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <algorithm>
+
 namespace msa {
 namespace {
 
@@ -254,6 +256,77 @@ __global__ void __launch_bounds__(kFillThreads)
   }
 }
 
+// Tile offsets of an existing CSR for a second tile size (counts from the offsets), then
+// the shared plan's header, written last so that it marks a complete plan.  One block.
+__global__ void __launch_bounds__(1024) plan_retile_kernel(const int* __restrict__ off,
+                                                           int* __restrict__ toff, int64_t keys,
+                                                           int qpt, int* __restrict__ hdr,
+                                                           PlanHeader h) {
+  __shared__ int s_w[32];
+  __shared__ int carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t base = 0; base < keys; base += 1024) {
+    const int64_t k = base + threadIdx.x;
+    const int n = k < keys ? __ldg(&off[k + 1]) - __ldg(&off[k]) : 0;
+    int x = (n + qpt - 1) / qpt;  // inclusive warp scan of the tile counts
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_w[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = s_w[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      s_w[lane] = w;
+    }
+    __syncthreads();
+    const int before = carry + (warp > 0 ? s_w[warp - 1] : 0);
+    if (k < keys) toff[k + 1] = before + x;
+    if (k == 0) toff[0] = 0;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = before + x;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+#pragma unroll
+    for (int i = 0; i < kPlanHeaderInts; ++i) hdr[i] = h.v[i];
+  }
+}
+
+// A shared plan handed to a call: if its header does not name this problem, record
+// MSA_ERR_ARG, clear the header (the buffer no longer holds a plan) and empty its lists
+// (offsets and tile offsets all 0), so the kernels that read it do no work and never
+// index past its arrays.  A block that reads the header after block 0 cleared it sees a
+// mismatch too.
+__global__ void plan_check_kernel(int* hdr, PlanHeader want, int* off, int* toff, int* toff2,
+                                  int64_t n, int* status) {
+  bool same = true;
+#pragma unroll
+  for (int i = 0; i < kPlanHeaderInts; ++i)
+    same = same && (reinterpret_cast<volatile int*>(hdr)[i] == want.v[i]);
+  if (same) return;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    set_status(status, MSA_ERR_ARG);
+#pragma unroll
+    for (int i = 0; i < kPlanHeaderInts; ++i) hdr[i] = 0;
+  }
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    off[i] = 0;
+    toff[i] = 0;
+    toff2[i] = 0;
+  }
+}
+
 }  // namespace
 
 int varlen_chunk_rows(VarlenTable k, int topk) {
@@ -288,6 +361,55 @@ Plan plan_carve(const Shape& s, void* ws) {
   p += align256((keys + 1) * 4);
   pl.entries = reinterpret_cast<int*>(p);
   return pl;
+}
+
+PlanHeader plan_header(const Shape& s) {
+  PlanHeader h;
+  h.v[0] = kPlanMagic;
+  h.v[1] = s.B;
+  h.v[2] = s.N;
+  h.v[3] = s.H_kv;
+  h.v[4] = s.nb;
+  h.v[5] = s.topk;
+  h.v[6] = s.G;
+  h.v[7] = (int)(s.T & 0x7fffffff);
+  return h;
+}
+
+size_t shared_plan_bytes(const Shape& s) {
+  return kPlanHeaderBytes + plan_bytes(s) + align256(((size_t)s.keys() + 1) * 4);
+}
+
+SharedPlan shared_plan_carve(const Shape& s, void* buf) {
+  uint8_t* p = static_cast<uint8_t*>(buf);
+  SharedPlan sp;
+  sp.hdr = reinterpret_cast<int*>(p);
+  sp.idx = plan_carve(s, p + kPlanHeaderBytes);
+  sp.fwd = sp.idx;
+  sp.fwd.toff = reinterpret_cast<int*>(p + kPlanHeaderBytes + plan_bytes(s));
+  return sp;
+}
+
+cudaError_t launch_shared_plan(const Shape& s, const int32_t* block_idx, const SharedPlan& sp,
+                               const Ctx& cx, cudaStream_t st) {
+  // an interrupted build leaves no valid header behind
+  cudaError_t e = cudaMemsetAsync(sp.hdr, 0, kPlanHeaderInts * sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  if ((e = launch_plan(s, block_idx, 128, sp.idx, cx, st)) != cudaSuccess) return e;
+  plan_retile_kernel<<<1, 1024, 0, st>>>(sp.idx.off, sp.fwd.toff, s.keys(), 128 / s.G, sp.hdr,
+                                         plan_header(s));
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shared_plan_check(const Shape& s, const SharedPlan& sp, const Ctx& cx,
+                                     cudaStream_t st) {
+  const int64_t n = s.keys() + 1;
+  const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 4 * (int64_t)cx.num_sms);
+  plan_check_kernel<<<grid, 256, 0, st>>>(sp.hdr, plan_header(s), sp.idx.off, sp.idx.toff,
+                                          sp.fwd.toff, n, cx.status);
+  note_launch();
+  return cudaGetLastError();
 }
 
 cudaError_t launch_plan(const Shape& s, const int32_t* block_idx, int qpt, const Plan& pl,

@@ -62,9 +62,29 @@ def make_problem(B, N, H_q, H_kv, d, d_idx, topk, Bk=128, causal=True, scale=Non
                         scale_idx=float(scale_idx if scale_idx is not None else 0.0))
 
 
+def new_plan(B, N, H_q, H_kv, topk, *, d=128, d_idx=64, Bk: int = 128, causal: bool = True,
+             device="cuda") -> torch.Tensor:
+    """A buffer for one step's inverted lists ("plan").  Pass it as `plan=` to
+    msa_index_topk, which builds it, then to msa_fwd and msa_bwd of the same step, which
+    read it instead of each building their own (see include/msa.h)."""
+    prob = make_problem(B, N, H_q, H_kv, d, d_idx, topk, Bk, causal, None, None)
+    n = _lib.msa_plan_size(prob)
+    if n == 0:
+        raise ValueError("invalid problem for a plan")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _plan_arg(plan):
+    if plan.dtype != torch.uint8 or not plan.is_cuda or not plan.is_contiguous():
+        raise ValueError("plan must be a contiguous uint8 CUDA tensor from new_plan")
+    return _ptr(plan), plan.numel()
+
+
 def msa_index_topk(q_idx: torch.Tensor, k_idx: torch.Tensor, topk: int = 16, *, H_q=None, d=None,
-                   Bk: int = 128, causal: bool = True, scale_idx=None, with_lse: bool = True):
-    """Index branch: returns (block_idx [B,H_kv,N,topk] int32, lse_idx [B,H_kv,N] f32 or None)."""
+                   Bk: int = 128, causal: bool = True, scale_idx=None, with_lse: bool = True,
+                   plan=None):
+    """Index branch: returns (block_idx [B,H_kv,N,topk] int32, lse_idx [B,H_kv,N] f32 or None).
+    With `plan` (from new_plan) it also builds the step's shared plan there."""
     _need(q_idx, "q_idx", ndim=4)
     _need(k_idx, "k_idx", ndim=3)
     B, N, H_kv, d_idx = q_idx.shape
@@ -76,14 +96,21 @@ def msa_index_topk(q_idx: torch.Tensor, k_idx: torch.Tensor, topk: int = 16, *, 
     lse_idx = torch.empty((B, H_kv, N), dtype=torch.float32, device=dev) if with_lse else None
     nws = _lib.msa_workspace_size(prob, _lib.MSA_WS_INDEX) if with_lse else 0
     ws = _workspace(nws, dev) if with_lse else None
-    rc = _lib.msa_index_topk(prob, _ptr(q_idx), _ptr(k_idx), _ptr(block_idx), _ptr(lse_idx),
-                             _ptr(ws), nws, _stream(dev))
+    if plan is None:
+        rc = _lib.msa_index_topk(prob, _ptr(q_idx), _ptr(k_idx), _ptr(block_idx), _ptr(lse_idx),
+                                 _ptr(ws), nws, _stream(dev))
+    else:
+        pp, pn = _plan_arg(plan)
+        rc = _lib.msa_index_topk_plan(prob, _ptr(q_idx), _ptr(k_idx), _ptr(block_idx),
+                                      _ptr(lse_idx), pp, pn, _ptr(ws), nws, _stream(dev))
     _lib.check(rc, "msa_index_topk")
     return block_idx, lse_idx
 
 
-def msa_fwd(q, k, v, block_idx, *, scale=None, Bk: int = 128, causal: bool = True, d_idx=64):
-    """Main branch forward: returns (o [B,N,H_q,d] bf16, lse [B,H_q,N] f32)."""
+def msa_fwd(q, k, v, block_idx, *, scale=None, Bk: int = 128, causal: bool = True, d_idx=64,
+            plan=None):
+    """Main branch forward: returns (o [B,N,H_q,d] bf16, lse [B,H_q,N] f32).  With `plan`
+    it reads the step's shared plan (built by msa_index_topk for this block_idx)."""
     _need(q, "q", ndim=4)
     _need(k, "k", ndim=4)
     _need(v, "v", ndim=4)
@@ -101,15 +128,21 @@ def msa_fwd(q, k, v, block_idx, *, scale=None, Bk: int = 128, causal: bool = Tru
     lse = torch.empty((B, H_q, N), dtype=torch.float32, device=dev)
     nws = _lib.msa_workspace_size(prob, _lib.MSA_WS_FWD)
     ws = _workspace(nws, dev)
-    rc = _lib.msa_fwd(prob, _ptr(q), _ptr(k), _ptr(v), _ptr(block_idx), _ptr(o), _ptr(lse),
-                      _ptr(ws), nws, _stream(dev))
+    if plan is None:
+        rc = _lib.msa_fwd(prob, _ptr(q), _ptr(k), _ptr(v), _ptr(block_idx), _ptr(o), _ptr(lse),
+                          _ptr(ws), nws, _stream(dev))
+    else:
+        pp, pn = _plan_arg(plan)
+        rc = _lib.msa_fwd_plan(prob, _ptr(q), _ptr(k), _ptr(v), _ptr(block_idx), pp, pn, _ptr(o),
+                               _ptr(lse), _ptr(ws), nws, _stream(dev))
     _lib.check(rc, "msa_fwd")
     return o, lse
 
 
 def msa_bwd(q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx, kl_weight: float, *,
-            scale=None, scale_idx=None, Bk: int = 128, causal: bool = True):
-    """Fused backward: returns dict dq, dk, dv, dq_idx, dk_idx (bf16) and kl (f32 [1])."""
+            scale=None, scale_idx=None, Bk: int = 128, causal: bool = True, plan=None):
+    """Fused backward: returns dict dq, dk, dv, dq_idx, dk_idx (bf16) and kl (f32 [1]).
+    With `plan` it reads the step's shared plan (built by msa_index_topk)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (q_idx, "q_idx")):
         _need(t, n, ndim=4)
     _need(k_idx, "k_idx", ndim=3)
@@ -127,10 +160,14 @@ def msa_bwd(q, k, v, o, lse, dO, q_idx, k_idx, block_idx, lse_idx, kl_weight: fl
            "kl": torch.empty(1, dtype=torch.float32, device=dev)}
     nws = _lib.msa_workspace_size(prob, _lib.MSA_WS_BWD)
     ws = _workspace(nws, dev)
-    rc = _lib.msa_bwd(prob, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(q_idx),
-                      _ptr(k_idx), _ptr(block_idx), _ptr(lse_idx), kl_weight, _ptr(out["dq"]),
-                      _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dq_idx"]), _ptr(out["dk_idx"]),
-                      _ptr(out["kl"]), _ptr(ws), nws, _stream(dev))
+    outs = (_ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dq_idx"]),
+            _ptr(out["dk_idx"]), _ptr(out["kl"]), _ptr(ws), nws, _stream(dev))
+    ins = (prob, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(q_idx), _ptr(k_idx),
+           _ptr(block_idx), _ptr(lse_idx))
+    if plan is None:
+        rc = _lib.msa_bwd(*ins, kl_weight, *outs)
+    else:
+        rc = _lib.msa_bwd_plan(*ins, *_plan_arg(plan), kl_weight, *outs)
     _lib.check(rc, "msa_bwd")
     return out
 
@@ -150,23 +187,26 @@ class MSAFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, q_idx, k_idx, topk, Bk, scale, scale_idx, kl_coef):
         B, N, H_q, d = q.shape
+        # one plan (inverted lists of block_idx) serves the index LSE, forward and backward
+        plan = new_plan(B, N, H_q, k.shape[2], topk, d=d, d_idx=q_idx.shape[3], Bk=Bk,
+                        device=q.device)
         block_idx, lse_idx = msa_index_topk(q_idx, k_idx, topk, H_q=H_q, d=d, Bk=Bk,
-                                            scale_idx=scale_idx, with_lse=True)
-        o, lse = msa_fwd(q, k, v, block_idx, scale=scale, Bk=Bk, d_idx=q_idx.shape[3])
-        ctx.save_for_backward(q, k, v, q_idx, k_idx, o, lse, block_idx, lse_idx)
+                                            scale_idx=scale_idx, with_lse=True, plan=plan)
+        o, lse = msa_fwd(q, k, v, block_idx, scale=scale, Bk=Bk, d_idx=q_idx.shape[3], plan=plan)
+        ctx.save_for_backward(q, k, v, q_idx, k_idx, o, lse, block_idx, lse_idx, plan)
         ctx.cfg = (Bk, scale, scale_idx, kl_coef)
         ctx.mark_non_differentiable(block_idx)
         return o, block_idx
 
     @staticmethod
     def backward(ctx, dO, _dblock):
-        q, k, v, q_idx, k_idx, o, lse, block_idx, lse_idx = ctx.saved_tensors
+        q, k, v, q_idx, k_idx, o, lse, block_idx, lse_idx, plan = ctx.saved_tensors
         Bk, scale, scale_idx, kl_coef = ctx.cfg
         B, N, H_q, _ = q.shape
         H_kv = k.shape[2]
         w = kl_coef / float(B * H_kv * N)
         g = msa_bwd(q, k, v, o, lse, dO.contiguous(), q_idx, k_idx, block_idx, lse_idx, w,
-                    scale=scale, scale_idx=scale_idx, Bk=Bk)
+                    scale=scale, scale_idx=scale_idx, Bk=Bk, plan=plan)
         MSAFunction.last_kl = g["kl"]
         return g["dq"], g["dk"], g["dv"], g["dq_idx"], g["dk_idx"], None, None, None, None, None
 

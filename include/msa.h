@@ -140,6 +140,40 @@ int msa_bwd(const msa_problem_t* p, const void* q, const void* k, const void* v,
             size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * One plan per step.  msa_index_topk (for lse_idx), msa_fwd and msa_bwd each turn
+ * block_idx into the same inverted lists (for every key block, the (query, slot)
+ * pairs that selected it: the KV-outer query gather of "El codiseño del kernel").
+ * The _plan variants build them once, into a caller-owned buffer that lives from a
+ * layer's index call to its backward:
+ *   msa_plan_size(p)     bytes of the plan buffer for problem p (0 if p is invalid);
+ *   msa_index_topk_plan  as msa_index_topk, and writes the plan of the block_idx it
+ *                        computes (also when lse_idx is NULL);
+ *   msa_fwd_plan, msa_bwd_plan
+ *                        as msa_fwd, msa_bwd (same workspace sizes), reading that plan
+ *                        instead of building their own.
+ * The plan must be the one msa_index_topk_plan wrote for the same problem and the same
+ * block_idx, unchanged since.  plan must be 256-byte aligned and plan_bytes at least
+ * msa_plan_size(p) (else MSA_ERR_ARG / MSA_ERR_WORKSPACE).  The plan starts with a header
+ * naming its problem, written last by the build.  A reading call first checks that header
+ * on the device.  If it names another problem (or no complete build), the call records
+ * MSA_ERR_ARG in the device status (msa_get_device_status), empties the plan's lists, and
+ * computes nothing meaningful; it never reads outside the plan's arrays.
+ * Fixed-length batches only; the variable-length calls build their own plan.
+ */
+size_t msa_plan_size(const msa_problem_t* p);
+int msa_index_topk_plan(const msa_problem_t* p, const void* q_idx, const void* k_idx,
+                        int32_t* block_idx, float* lse_idx, void* plan, size_t plan_bytes,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+int msa_fwd_plan(const msa_problem_t* p, const void* q, const void* k, const void* v,
+                 const int32_t* block_idx, void* plan, size_t plan_bytes, void* o, float* lse,
+                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+int msa_bwd_plan(const msa_problem_t* p, const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dO, const void* q_idx, const void* k_idx,
+                 const int32_t* block_idx, const float* lse_idx, void* plan, size_t plan_bytes,
+                 float kl_weight, void* dq, void* dk, void* dv, void* dq_idx, void* dk_idx,
+                 float* kl_out, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Packed variable-length batches (the variable-length view of the sparse attention,
  * Flash-MSA article, tech.kuratif.com, ¶7).  num_seqs sequences share one token axis of
  * total_tokens tokens: sequence s holds tokens cu_seqlens[s] .. cu_seqlens[s+1]-1 of

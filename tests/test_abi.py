@@ -139,6 +139,38 @@ def test_varlen_arguments_are_checked_on_the_host():
         _lib.MSA_ERR_ARG  # workspace not 256-byte aligned
 
 
+def test_plan_arguments_are_checked_on_the_host():
+    # the shared plan's size grows with the problem; a null, short or misaligned plan
+    # buffer is refused before anything is queued (its contents are checked on the device)
+    small, big = _prob(N=1024), _prob(N=4096)
+    assert _lib.msa_plan_size(small) > 0
+    assert _lib.msa_plan_size(big) > _lib.msa_plan_size(small)
+    assert _lib.msa_plan_size(_prob(N=1024, H_q=24, H_kv=16)) == 0  # H_q % H_kv != 0
+    n = _lib.msa_plan_size(small)
+    ws = 1 << 34
+    assert _lib.msa_index_topk_plan(small, 16, 16, 16, None, None, n, None, 0, None) == \
+        _lib.MSA_ERR_ARG
+    assert _lib.msa_index_topk_plan(small, 16, 16, 16, None, 256, n - 1, None, 0, None) == \
+        _lib.MSA_ERR_WORKSPACE
+    assert _lib.msa_index_topk_plan(small, 16, 16, 16, None, 128, n, None, 0, None) == \
+        _lib.MSA_ERR_ARG  # not 256-byte aligned
+    assert _lib.msa_fwd_plan(small, 16, 16, 16, 16, None, n, 16, 16, 256, ws, None) == \
+        _lib.MSA_ERR_ARG
+    assert _lib.msa_fwd_plan(small, 16, 16, 16, 16, 256, n - 256, 16, 16, 256, ws, None) == \
+        _lib.MSA_ERR_WORKSPACE
+    args = [16] * 10
+    assert _lib.msa_bwd_plan(small, *args, None, n, 1.0, 16, 16, 16, 16, 16, None, 256, ws,
+                             None) == _lib.MSA_ERR_ARG
+    assert _lib.msa_bwd_plan(small, *args, 256, 16, 1.0, 16, 16, 16, 16, 16, None, 256, ws,
+                             None) == _lib.MSA_ERR_WORKSPACE
+    # empty problems are no-ops with or without a plan
+    p0 = _prob(N=0)
+    assert _lib.msa_index_topk_plan(p0, None, None, None, None, None, 0, None, 0, None) == \
+        _lib.MSA_OK
+    assert _lib.msa_fwd_plan(p0, None, None, None, None, None, 0, None, None, None, 0, None) == \
+        _lib.MSA_OK
+
+
 def test_empty_problem_is_a_no_op():
     p = _prob(N=0)
     assert _lib.msa_index_topk(p, None, None, None, None, None, 0, None) == _lib.MSA_OK
