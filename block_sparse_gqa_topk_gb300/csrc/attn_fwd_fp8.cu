@@ -242,11 +242,9 @@ __global__ void __launch_bounds__(kThreads8, 1)
           cp_async_16(dq + sw_row(r, chf), qg + i * qrow + h * kD8, ok);
         }
         cp_async_commit();
-        if (u >= 1) {  // the previous tile's copies have landed: publish them
-          cp_async_wait<1>();
-          fence_async();
-          mbar_arrive(&qfull[(u - 1) % kStages8]);
-        }
+        // this thread's copies count toward the tile's stage as soon as they land (the
+        // MMA thread orders them before the tensor core's reads with a proxy fence)
+        cp_async_mbar_arrive(&qfull[st]);
         if (key != prev_key) {
           if (lt == 0) {
             if (kv_loads > 0 && !mbar_wait(kvempty, (kv_loads - 1) & 1, p.wait_ns, abort_flag))
@@ -265,9 +263,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
 #pragma unroll
         for (int m = 0; m < NE; ++m) my_ent[m] = nxt_ent[m];
       }
-      cp_async_wait<0>();
-      fence_async();
-      if (!*abort_flag) mbar_arrive(&qfull[(n_tiles - 1) % kStages8]);
+      cp_async_wait<0>();  // nothing may still be landing when the CTA exits
       if (lt == 0 && kv_issued > 0) mbar_wait(kvfull, (kv_issued - 1) & 1, 1000000000ull);
     } else if (warp == 11) {
       // ============================== MMA issuer ================================
@@ -280,6 +276,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
         auto issue_s = [&](int u) -> bool {
           const int st = u % kStages8, b = u & 1;
           if (!mbar_wait(&qfull[st], (u / kStages8) & 1, p.wait_ns, abort_flag)) return false;
+          fence_async();  // the q rows came by cp.async (generic proxy)
           if (!mbar_wait(&sfree[b], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag)) return false;
           tc_fence_after();
           const uint32_t aQ = smem_u32(sQ + st * L::kTile);

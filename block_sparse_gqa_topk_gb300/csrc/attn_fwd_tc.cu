@@ -10,8 +10,9 @@
 // A tile is one key block c of one (batch, group) and 128 rows = 128/G gathered
 // queries x G heads.  Per CTA (persistent, a contiguous range of tiles):
 //   warps 8-10 loaders: gather the tile's q rows with cp.async into a 3-stage ring
-//              in the 128-byte-swizzled K-major layout tcgen05 reads; one thread
-//              TMA-loads K and V of the block when the key changes;
+//              in the 128-byte-swizzled K-major layout tcgen05 reads (a stage completes
+//              through cp.async arrivals as its rows land); one thread TMA-loads K and V
+//              of the block when the key changes;
 //   warp 11    TMEM owner + one MMA thread: S = Q K^T (M=N=128, K=d) into a 2-deep
 //              TMEM ring, then O = P V with V as an MN-major operand;
 //   warps 0-7  two softmax warpgroups taking alternate tiles (thread = row = TMEM
@@ -193,9 +194,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (n_tiles > 0) {
     if (warp >= 8 && warp < 11) {
       // ================================ loaders =================================
-      // Order per tile: gather q(u) -> publish q(u-1) -> (new block) swap K/V.  The
-      // swap waits for the previous block's last PV MMA, which needs q(u-1)
-      // published first.
+      // Order per tile: gather q(u), whose stage completes through cp.async arrivals as
+      // the rows land -> (new block) swap K/V once the previous block's last PV MMA is
+      // done.
       const int lt = threadIdx.x - 256;  // 0 .. kLoadThreads-1
       KeyCursor kc;
       int prev_key = -1, kv_loads = 0, kv_issued = 0;
@@ -252,11 +253,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           cp_async_16(dcol + r * 128 + (((chf & 7) ^ (r & 7)) << 4), qg + i * qrow + h * D, ok);
         }
         cp_async_commit();
-        if (u >= 1) {  // the previous tile's copies have landed: publish them
-          cp_async_wait<1>();
-          fence_proxy_async_smem();
-          mbar_arrive(&qfull[(u - 1) % kQStages]);
-        }
+        // this thread's copies count toward the tile's stage as soon as they land (the
+        // MMA thread makes them visible to the tensor core with a proxy fence)
+        cp_async_mbar_arrive(&qfull[st]);
         if (key != prev_key) {
           if (lt == 0) {
             // the previous block's MMAs must be done with K/V before they are replaced
@@ -279,9 +278,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int m = 0; m < NE; ++m) my_ent[m] = nxt_ent[m];
       }
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      if (!*abort_flag) mbar_arrive(&qfull[(n_tiles - 1) % kQStages]);
+      cp_async_wait<0>();  // nothing may still be landing when the CTA exits
       // teardown: the last K/V TMA issued must have landed
       if (lt == 0 && kv_issued > 0) mbar_wait(kvfull, (kv_issued - 1) & 1, 1000000000ull);
     } else if (warp == 11) {
@@ -297,6 +294,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         auto issue_s = [&](int u) -> bool {
           const int st = u % kQStages, b = u & 1;
           if (!mbar_wait(&qfull[st], (u / kQStages) & 1, p.wait_ns, abort_flag)) return false;
+          // the gathered rows were written by cp.async (generic proxy): order them before
+          // the tensor core's reads
+          fence_proxy_async_smem();
           if (!mbar_wait(&sfree[b], ((u >> 1) & 1) ^ 1, p.wait_ns, abort_flag)) return false;
           tc_fence_after();
           const uint32_t aQ = smem_u32(sQ + st * L::kTile);

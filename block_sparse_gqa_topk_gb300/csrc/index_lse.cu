@@ -155,10 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_tiles > 0) {
     if (warp >= kLoadWarp0 && warp < kMmaWarp) {
       // ================================ loaders =================================
-      // Per tile: (new block) TMA its k_idx tile -> gather q(u) -> publish q(u-1).
-      // The k_idx wait is on the block two keys back: its last tile is at most u-2,
-      // published in an earlier iteration, and the MMA thread releases the buffer
-      // right after that tile's MMA.
+      // Per tile: (new block) TMA its k_idx tile -> gather q(u), whose stage completes
+      // through cp.async arrivals as the rows land.  The k_idx wait is on the block two
+      // keys back: its last tile is at most u-2, whose rows were issued in an earlier
+      // iteration, and the MMA thread releases the buffer right after that tile's MMA.
       const int lt = threadIdx.x - 32 * kLoadWarp0;
       Cursor kc;
       int prev_key = -1, k_loads = 0, k_issued = 0;
@@ -218,18 +218,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           cp_async_16(dq + swz<RB>(r, chf), qg + (int64_t)i * p.H_kv * DI, ok);
         }
         cp_async_commit();
-        if (u >= 1) {
-          cp_async_wait<1>();
-          fence_proxy_async_smem();
-          mbar_arrive(&qfull[(u - 1) % kQStages]);
-        }
+        // this thread's copies count toward the tile's stage as soon as they land (the
+        // MMA thread orders them before the tensor core's reads with a proxy fence)
+        cp_async_mbar_arrive(&qfull[st]);
         cur_key = nxt_key;
 #pragma unroll
         for (int k = 0; k < NR; ++k) cur_ent[k] = nxt_ent[k];
       }
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      if (!*abort_flag) mbar_arrive(&qfull[(n_tiles - 1) % kQStages]);
+      cp_async_wait<0>();  // nothing may still be landing when the CTA exits
       // teardown: every k_idx TMA issued must have landed before the CTA exits
       if (lt == 0)
         for (int n = max(0, k_issued - 2); n < k_issued; ++n)
@@ -257,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          fence_proxy_async_smem();  // the q_idx rows came by cp.async (generic proxy)
           tc_fence_after();
           const uint64_t qd = umma_desc_kmajor<RB>(smem_u32(sQ + st * L::kTile));
           const uint64_t kd = umma_desc_kmajor<RB>(smem_u32(sK + ((k_uses - 1) & 1) * L::kTile));
