@@ -230,27 +230,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         uint8_t* dq = sQ + st * L::kTile;
-        // Each thread copies one fixed 16-byte column (chf) of the rows r0, r0 + RS, ...:
-        // the per-copy work is a shuffle for the row's entry, one multiply-add for the
-        // source and the swizzled destination.
+        // Each thread copies one fixed 16-byte column (chf) of the G head rows of the
+        // queries q0, q0 + QS, ...: one shuffle for the query's entry and one source
+        // address per query, then G copies at a fixed stride.
         static_assert(kLoadThreads % CH == 0, "loader threads cover whole rows");
-        constexpr int RS = kLoadThreads / CH;  // rows per pass
+        constexpr int QS = kLoadThreads / CH;          // queries per pass
+        constexpr int NPASS = (QPT + QS - 1) / QS;     // passes (the same for every lane)
         const int chf = lt % CH;
         const __nv_bfloat16* qg = p.q + (sp.t0 * p.H_kv * G + (int64_t)g * G) * D + chf * 8;
         const int64_t qrow = (int64_t)p.H_kv * G * D;  // elements between consecutive queries
         uint8_t* dcol = dq + (chf >> 3) * L::kHalf;
-#pragma unroll 4
-        for (int r = lt / CH; r < 128; r += RS) {
-          const int qi = r / G, h = r % G;
+#pragma unroll 2
+        for (int pass = 0; pass < NPASS; ++pass) {
+          const int qi = lt / CH + QS * pass;
           int ent = -1;
 #pragma unroll
           for (int m = 0; m < NE; ++m) {
             const int v = __shfl_sync(0xffffffffu, my_ent[m], qi & 31);
             if ((qi >> 5) == m) ent = v;
           }
-          const bool ok = ent >= 0;
-          const int i = ok ? (ent >> kSlotBits) : 0;
-          cp_async_16(dcol + r * 128 + (((chf & 7) ^ (r & 7)) << 4), qg + i * qrow + h * D, ok);
+          if (qi < QPT) {
+            const bool ok = ent >= 0;
+            const __nv_bfloat16* src = qg + (ok ? (int64_t)(ent >> kSlotBits) * qrow : 0);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const int r = qi * G + h;
+              cp_async_16(dcol + r * 128 + (((chf & 7) ^ (r & 7)) << 4), src + h * D, ok);
+            }
+          }
         }
         cp_async_commit();
         // this thread's copies count toward the tile's stage as soon as they land (the
