@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
       // ================================ loaders =================================
       const int lt = threadIdx.x - 256;
       static_assert(kLoad8 % CH == 0, "loader threads cover whole rows");
-      constexpr int RS = kLoad8 / CH;  // rows per pass
+      constexpr int RS = kLoad8 / CH;  // queries per pass
       const int chf = lt % CH;
       Cursor8 kc;
       int prev_key = -1, kv_loads = 0, kv_issued = 0;
@@ -228,18 +228,25 @@ __global__ void __launch_bounds__(kThreads8, 1)
         uint8_t* dq = sQ + st * L::kTile;
         const uint8_t* qg = p.q8 + ((int64_t)b * p.N * p.H_kv * G + (int64_t)g * G) * kD8 + chf * 16;
         const int64_t qrow = (int64_t)p.H_kv * G * kD8;  // bytes between consecutive queries
-#pragma unroll 4
-        for (int r = lt / CH; r < 128; r += RS) {
-          const int qi = r / G, h = r % G;
+        // whole queries per thread: one shuffle and one source address per query, then
+        // its G head rows at a fixed stride (RS queries per pass, the same passes for
+        // every lane)
+        constexpr int NPASS = (QPT + RS - 1) / RS;
+#pragma unroll 2
+        for (int pass = 0; pass < NPASS; ++pass) {
+          const int qi = lt / CH + RS * pass;
           int ent = -1;
 #pragma unroll
           for (int m = 0; m < NE; ++m) {
             const int v = __shfl_sync(0xffffffffu, my_ent[m], qi & 31);
             if ((qi >> 5) == m) ent = v;
           }
-          const bool ok = ent >= 0;
-          const int i = ok ? (ent >> kSlotBits) : 0;
-          cp_async_16(dq + sw_row(r, chf), qg + i * qrow + h * kD8, ok);
+          if (qi < QPT) {
+            const bool ok = ent >= 0;
+            const uint8_t* src = qg + (ok ? (int64_t)(ent >> kSlotBits) * qrow : 0);
+#pragma unroll
+            for (int h = 0; h < G; ++h) cp_async_16(dq + sw_row(qi * G + h, chf), src + h * kD8, ok);
+          }
         }
         cp_async_commit();
         // this thread's copies count toward the tile's stage as soon as they land (the
