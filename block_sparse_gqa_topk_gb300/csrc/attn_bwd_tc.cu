@@ -133,7 +133,7 @@ constexpr uint32_t cDK = 0, cDV = 128, cST = 256, cDPT = 320, cDQT = 384, cDKI =
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_qi, const __grid_constant__ CUtensorMap tm_ki,
                   const BwdTcParams p) {
   constexpr int R = rows_per_chunk(G);  // rows per chunk
@@ -721,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct BwdMaps {
-  CUtensorMap k, v, q, dO, qi, ki;
+  CUtensorMap k, v, q, qi, ki;
 };
 
 template <int D, int G>
@@ -731,7 +731,7 @@ cudaError_t launch_dg(const BwdTcParams& prm, const BwdMaps& m, const Ctx& cx, c
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   kernel_event(MSA_KERNEL_BWD, true, st);
-  kern<<<cx.num_sms, kThreads, L::kAlloc, st>>>(m.k, m.v, m.q, m.dO, m.qi, m.ki, prm);
+  kern<<<cx.num_sms, kThreads, L::kAlloc, st>>>(m.k, m.v, m.q, m.qi, m.ki, prm);
   kernel_event(MSA_KERNEL_BWD, false, st);
   note_launch();
   return cudaGetLastError();
@@ -746,7 +746,8 @@ cudaError_t launch_attn_bwd_tc(const Shape& s, const void* q, const void* k, con
                                __nv_bfloat16* dqi_part, float* dki_part, double* kl_acc, void* dk,
                                void* dv, const Ctx& cx, cudaStream_t st) {
   // K, V: [tokens][H_kv][d] per batch, one (64-column, 128-key) box per half.
-  // q, dO: [T][H_q][d], one (64-column, G-head) box per query and half.
+  // q: [T][H_q][d], one (64-column, G-head) box per query and half (dO is gathered by
+  // cp.async).
   // q_idx: [T][H_kv][d_idx], one row box per query slot; k_idx: [tokens][d_idx] per
   // batch, one 128-key box.  All 128-byte swizzled; the q_idx and k_idx boxes are 64
   // columns wide whatever d_idx is, so with d_idx = 32 the upper half lands as zeros.
@@ -769,7 +770,7 @@ cudaError_t launch_attn_bwd_tc(const Shape& s, const void* q, const void* k, con
   const uint64_t ski[2] = {DI * 2, s.tma_tokens() * DI * 2};
   const uint32_t bki[3] = {64, 128, 1};
   if (!encode_tiled(&m.k, bf, 4, k, dkv, skv, bkv, sw) || !encode_tiled(&m.v, bf, 4, v, dkv, skv, bkv, sw) ||
-      !encode_tiled(&m.q, bf, 3, q, dq, sq, bq, sw) || !encode_tiled(&m.dO, bf, 3, dO, dq, sq, bq, sw) ||
+      !encode_tiled(&m.q, bf, 3, q, dq, sq, bq, sw) ||
       !encode_tiled(&m.qi, bf, 3, q_idx, dqi, sqi, bqi, sw) ||
       !encode_tiled(&m.ki, bf, 3, k_idx, dki, ski, bki, sw))
     return cudaErrorInvalidValue;
