@@ -5,8 +5,9 @@ forward and the backward read them instead of each building their own.
 The chain with the shared plan gives the same selection, index LSE, o and lse bit for
 bit (every row is computed on its own, whatever tile it lands in), and the same gradients
 to the rounding of the backward's accumulation order (the order of a key block's list
-comes from a parallel fill).  A plan buffer that names another problem, or holds no
-complete build, is reported through the device status and read as empty lists."""
+comes from a parallel fill), at G = 1, 4, 8 and 16.  A plan buffer that names another
+problem, or holds no complete build, is reported through the device status and read as
+empty lists."""
 import numpy as np
 import pytest
 import torch
@@ -17,6 +18,9 @@ from gpu_inputs import device_inputs
 pytestmark = pytest.mark.gpu
 
 CFG_G8 = synth.CONFIGS["8k"].with_(name="plan-g8", B=1, N=4096, H_q=16, H_kv=2, seed=81)
+# G = 16 (8-query forward tiles, ragged N) and G = 1 with d = 64 (128-query tiles)
+CFG_G16 = synth.CONFIGS["8k"].with_(name="plan-g16", B=1, N=3000, H_q=32, H_kv=2, topk=8, seed=82)
+CFG_G1 = synth.CONFIGS["tiny"].with_(name="plan-g1", N=2200, H_q=4, H_kv=4, topk=3, seed=83)
 
 
 def _step(cfg, d, plan):
@@ -32,8 +36,8 @@ def _plan_for(cfg):
     return ops.new_plan(cfg.B, cfg.N, cfg.H_q, cfg.H_kv, cfg.topk, d=cfg.d, d_idx=cfg.d_idx)
 
 
-@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], synth.CONFIGS["8k"], CFG_G8],
-                         ids=["tiny", "8k", "g8"])
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], synth.CONFIGS["8k"], CFG_G8, CFG_G16, CFG_G1],
+                         ids=["tiny", "8k", "g8", "g16", "g1_d64"])
 def test_shared_plan_matches_per_call_plans(cfg):
     _, d = device_inputs(cfg)
     ref = _step(cfg, d, None)
