@@ -355,6 +355,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
+// The 32x32b.x32 load with a max reduction (sm_103a): r as tmem_ld_32x32b_x32, and m the
+// largest of this lane's 32 values.  Both are valid after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld_max_32x32b_x32(uint32_t taddr, uint32_t (&r)[32], float& m) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+      : MSA_R8(0), MSA_R8(8), MSA_R8(16), MSA_R8(24), "=f"(m)
+      : "r"(taddr)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA with
 // a 128-byte (rows of 64 bf16) or 64-byte (rows of 32 bf16) swizzle: 8-row atoms,
 // SBO = 8 * row bytes, LBO unused, descriptor version 1 (bit 46).

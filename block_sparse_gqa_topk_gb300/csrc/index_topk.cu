@@ -15,9 +15,10 @@
 //     (SWIZZLE_128B / 64B, the layout tcgen05 reads directly);
 //   - one thread issues tcgen05.mma: S_g = Q_idx,g (128 x d_idx) . K^T for both
 //     groups into a 2-slot TMEM ring (2 slots x 2 groups x 128 fp32 columns);
-//   - 8 epilogue warps (one thread per query row and group) tcgen05.ld the row's
-//     128 scores, max-reduce them to the block score and update a sorted top-(k-1)
-//     list in registers.
+//   - 8 epilogue warps (one thread per query row and group) read the row's 128
+//     scores with max-reducing TMEM loads (tcgen05.ld.red, four of 32 columns), so
+//     the block score needs no max chain, and update a sorted top-(k-1) list in
+//     registers.
 // The local (diagonal) block is never scored: it is always selected.  Nothing but
 // block_idx is written: the pooled scores never leave the SM.
 #include <cudaTypedefs.h>
@@ -279,15 +280,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + a * 256 + gi * 128;
+          // the block score: each 32-column load returns its own max (the reducing
+          // TMEM load of sm_103a), so no max chain runs over the loaded registers
           float m = -INFINITY;
-#pragma unroll
+#pragma unroll 1
           for (int h = 0; h < 4; ++h) {
             uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + h * 32, r);
+            float mh;
+            tmem_ld_max_32x32b_x32(taddr + h * 32, r, mh);
             tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; c += 2)
-              m = fmax3(m, __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+            m = fmaxf(m, mh);
           }
           tc_fence_before();
           __syncwarp();
