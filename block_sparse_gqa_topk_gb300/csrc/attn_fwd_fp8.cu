@@ -381,11 +381,11 @@ __global__ void __launch_bounds__(kThreads8, 1)
 #pragma unroll 1
         for (int h = 0; h < 4; ++h) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(srow + 32 * h, r);
+          float mh;
+          tmem_ld_max_32x32b_x32(srow + 32 * h, r, mh);
           tmem_wait_ld();
           if (full) {
-#pragma unroll
-            for (int x = 0; x < 32; x += 2) m = fmax3(m, __uint_as_float(r[x]), __uint_as_float(r[x + 1]));
+            m = fmaxf(m, mh);
           } else {
 #pragma unroll
             for (int x = 0; x < 32; ++x) m = fmaxf(m, 32 * h + x <= jlim ? __uint_as_float(r[x]) : -INFINITY);

@@ -341,12 +341,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 acc = make_float2(0.f, 0.f);
         {
           uint32_t r[64];
-          load64(r, 0);
-          float m0 = -INFINITY;
+          float m0;
+          tmem_ld_max_32x32b_x32(srow, *reinterpret_cast<uint32_t(*)[32]>(&r[0]), m0);
+          tmem_ld_32x32b_x32(srow + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+          tmem_wait_ld();
+          if (!full) {
+            m0 = -INFINITY;
 #pragma unroll
-          for (int x = 0; x < 32; x += 2)
-            m0 = fmax3(m0, full || x <= jlim ? __uint_as_float(r[x]) : -INFINITY,
-                       full || x + 1 <= jlim ? __uint_as_float(r[x + 1]) : -INFINITY);
+            for (int x = 0; x < 32; x += 2)
+              m0 = fmax3(m0, x <= jlim ? __uint_as_float(r[x]) : -INFINITY,
+                         x + 1 <= jlim ? __uint_as_float(r[x + 1]) : -INFINITY);
+          }
           ms = m0 == -INFINITY ? 0.f : m0 * sl2;
           exp_sum(r, 0, ms, acc);
           load64(r, 64);
