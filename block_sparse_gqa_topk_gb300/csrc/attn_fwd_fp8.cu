@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
         for (int h = 0; h < 4; ++h) {
           uint32_t r[32];
           float mh;
-          tmem_ld_max_32x32b_x32(srow + 32 * h, r, mh);
+          tmem_ld_max_32x32b_x32(srow + 32 * h, r, mh);  // mh: max of the 32 columns
           tmem_wait_ld();
           if (full) {
             m = fmaxf(m, mh);

@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           uint32_t r[64];
           float m0;
+          // a full tile takes the offset from the first load's own max reduction
           tmem_ld_max_32x32b_x32(srow, *reinterpret_cast<uint32_t(*)[32]>(&r[0]), m0);
           tmem_ld_32x32b_x32(srow + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
           tmem_wait_ld();

@@ -294,20 +294,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&accempty[a]);
-          // sorted insert of (m, t); equal scores keep the earlier (lower) block
+          // sorted insert of (m, t).  The first M slots stay ordered by (score
+          // descending, block ascending): m lands in the first slot whose score it
+          // beats strictly (after every equal score, which came from a lower block)
+          // and the slots after it shift down by one.  When the list overflows, the
+          // entry dropped has the lowest score and, among equal scores, the highest
+          // block, as the selection rule wants.  Each slot's new value depends on the
+          // old list only, so there is no carry from slot to slot.
           if (!exact || m > val[KM - 1]) {
-            float cv = m;
-            int ci = t;
+            bool gt[KM];
 #pragma unroll
-            for (int s = 0; s < KM; ++s) {
-              const bool gt = cv > val[s];
-              const float tv = gt ? cv : val[s];
-              const int ti = gt ? ci : id[s];
-              cv = gt ? val[s] : cv;
-              ci = gt ? id[s] : ci;
-              val[s] = tv;
-              id[s] = ti;
+            for (int s = 0; s < KM; ++s) gt[s] = m > val[s];
+#pragma unroll
+            for (int s = KM - 1; s > 0; --s) {
+              val[s] = gt[s] ? (gt[s - 1] ? val[s - 1] : m) : val[s];
+              id[s] = gt[s] ? (gt[s - 1] ? id[s - 1] : t) : id[s];
             }
+            val[0] = gt[0] ? m : val[0];
+            id[0] = gt[0] ? t : id[0];
           }
         }
         if (__any_sync(0xffffffffu, !ok || *abort_flag)) break;  // warp-uniform exit

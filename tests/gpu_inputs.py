@@ -22,3 +22,20 @@ def rows_for(cfg, n_rows, seed=77):
         return None, np.arange(cfg.B * cfg.N, dtype=np.int64)
     r = synth.sample_rows(cfg, n_rows, seed)
     return r, r
+
+
+def tie_inputs(cfg, seed=46):
+    """Host inputs whose key blocks are copies of block 0 scaled by 1, 2 or 4 (seeded).
+
+    Scaling bf16 values by a power of two is exact, and so is every partial sum of the
+    scores, in float32 as in float64: a query's pooled block scores are its block-0
+    score times 1, 2 or 4, exactly.  Each query therefore sees runs of exactly equal
+    scores, which only the lower-block tie rule orders.
+    """
+    h = dict(synth.make_inputs(cfg, names=("q_idx", "k_idx")))
+    nb = cfg.N // cfg.Bk
+    ki = synth.bf16_bits_to_f32(h["k_idx"]).reshape(cfg.B, nb, cfg.Bk, cfg.d_idx)
+    scale = 2.0 ** np.random.default_rng(seed).integers(0, 3, size=nb)
+    ki = ki[:, :1] * scale[None, :, None, None]
+    h["k_idx"] = synth.f32_to_bf16_bits(ki.reshape(cfg.B, cfg.N, cfg.d_idx).astype(np.float32))
+    return h, scale

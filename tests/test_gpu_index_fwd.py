@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from block_sparse_gqa_topk_gb300 import ops, synth
-from gpu_inputs import device_inputs, host_inputs, rows_for
+from gpu_inputs import device_inputs, host_inputs, rows_for, tie_inputs
 from parity import LSE_TOL, O_TOL, check_selection, f64, gpu_sel_rows, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -56,6 +56,26 @@ def test_index_topk_matches_oracle(name, n_rows):
     assert err <= LSE_TOL, f"lse_idx max err {err}"
     print(f"{name}: rows {len(rows_arr)} same {n_same} near-tie {n_near} "
           f"differing {int(diff.sum())} lse_idx err {err:.2e}")
+
+
+@pytest.mark.parametrize("topk", [4, 6])
+def test_exact_ties_keep_the_lower_block(topk):
+    """Key blocks that are block 0 scaled by 1, 2 or 4 score exactly that multiple of the
+    query's block-0 score in the kernel's float32 as in the oracle's float64, so rows see
+    runs of equal block scores longer than the k - 1 free slots.  The lower-block rule
+    then fixes the set, with no near-tie freedom: the GPU's must be the oracle's on every
+    row.  k = 4 fills a 3-slot list exactly, k = 6 uses 5 slots of a 7-slot list."""
+    cfg = T.with_(name=f"ties-k{topk}", N=4096, topk=topk, seed=45)
+    h, _ = tie_inputs(cfg)
+    bi, _ = ops.msa_index_topk(to_dev(h["q_idx"]), to_dev(h["k_idx"]), cfg.topk, H_q=cfg.H_q,
+                               d=cfg.d)
+    assert ops.device_status() == 0
+    rows = np.arange(cfg.B * cfg.N, dtype=np.int64)
+    bi_ref, _, _ = oracle.select(cfg, h, rows=None)
+    gsel = gpu_sel_rows(cfg, bi.cpu().numpy(), rows)
+    bad = np.argwhere(np.any(gsel != bi_ref, axis=-1))
+    assert len(bad) == 0, (f"{len(bad)} (row, group) sets differ, e.g. {bad[0]}: gpu "
+                           f"{gsel[tuple(bad[0])]} oracle {bi_ref[tuple(bad[0])]}")
 
 
 @pytest.mark.parametrize("name,n_rows", FULL + SAMPLED)
