@@ -24,7 +24,7 @@ def rows_for(cfg, n_rows, seed=77):
     return r, r
 
 
-def tie_inputs(cfg, seed=46):
+def tie_inputs(cfg, seed=46, names=("q_idx", "k_idx")):
     """Host inputs whose key blocks are copies of block 0 scaled by 1, 2 or 4 (seeded).
 
     Scaling bf16 values by a power of two is exact, and so is every partial sum of the
@@ -32,7 +32,7 @@ def tie_inputs(cfg, seed=46):
     score times 1, 2 or 4, exactly.  Each query therefore sees runs of exactly equal
     scores, which only the lower-block tie rule orders.
     """
-    h = dict(synth.make_inputs(cfg, names=("q_idx", "k_idx")))
+    h = dict(synth.make_inputs(cfg, names=tuple(names)))
     nb = cfg.N // cfg.Bk
     ki = synth.bf16_bits_to_f32(h["k_idx"]).reshape(cfg.B, nb, cfg.Bk, cfg.d_idx)
     scale = 2.0 ** np.random.default_rng(seed).integers(0, 3, size=nb)

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from block_sparse_gqa_topk_gb300 import ops, synth
-from gpu_inputs import host_inputs
+from gpu_inputs import host_inputs, tie_inputs
 from parity import LSE_TOL, O_TOL, check_selection, f64, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -51,6 +51,29 @@ def test_decode_matches_oracle_last_row(name):
         eo = np.abs(o[b] - o_ref[0]).max()
         el = np.abs(lse[b] - lse_ref[0]).max()
         assert eo <= O_TOL and el <= LSE_TOL, (name, b, eo, el)
+
+
+def test_decode_exact_ties_keep_the_lower_block():
+    """Key blocks that are block 0 scaled by 1, 2 or 4 pool to exact multiples of one
+    another on the decode path's mma.sync pooling as in the oracle, so the last row sees
+    runs of equal block scores longer than the k - 1 free slots: the decode selection
+    (ranked on (score, -block) keys) must take the oracle's set exactly."""
+    cfg = T.with_(name="dec-ties", B=2, N=4096, topk=6, seed=66)
+    h, _ = tie_inputs(cfg, names=("q", "k", "v", "q_idx", "k_idx"))
+    d = {n: to_dev(h[n]) for n in ("q", "k", "v", "q_idx", "k_idx")}
+    lens = [4096, 3001]
+    bsel = torch.arange(cfg.B, device="cuda")
+    last = torch.tensor([L - 1 for L in lens], device="cuda")
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    bi, _, _ = ops.msa_decode(d["q"][bsel, last].contiguous(), d["q_idx"][bsel, last].contiguous(),
+                              d["k"], d["v"], d["k_idx"], lens_t, cfg.topk, scale=cfg.scale)
+    assert ops.device_status() == 0
+    bi = bi.cpu().numpy()
+    for b, L in enumerate(lens):
+        cb = cfg.with_(B=1, N=L)
+        hb = {n: np.ascontiguousarray(h[n][b:b + 1, :L]) for n in h}
+        bi_ref, _, _ = oracle.select(cb, hb, rows=np.array([L - 1], dtype=np.int64))
+        assert np.array_equal(bi[b], bi_ref[0]), (b, bi[b], bi_ref[0])
 
 
 def test_decode_invalid_length_is_reported_and_bounded():
