@@ -411,10 +411,13 @@ __device__ __forceinline__ void lse_merge(float& m, float& l, float m2, float l2
   m = mm;
 }
 
+template <int V>
 __global__ void lse_combine_kernel(const float* __restrict__ lse_part,
                                    const int32_t* __restrict__ block_idx,
                                    float* __restrict__ lse_idx, const int2* __restrict__ spans,
                                    int B, int N, int H_kv, int64_t rows, int topk, int nb, int W) {
+  // W lanes per row, V consecutive slots per lane and load (V = 4: 16-byte loads of the
+  // row's block ids and partials, so that enough bytes are in flight to stream them)
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t r = warp * (32 / W) + lane / W;
@@ -426,10 +429,21 @@ __global__ void lse_combine_kernel(const float* __restrict__ lse_part,
   }
   float m = -INFINITY, l = 0.f;
   if (live) {
-    for (int s = sl; s < topk; s += W) {
-      const int c = __ldg(&block_idx[r * topk + s]);
-      if (c < 0 || c >= nb) continue;
-      lse_merge(m, l, __ldg(&lse_part[r * topk + s]), 1.f);
+    for (int s = V * sl; s < topk; s += V * W) {
+      int c[V];
+      float v[V];
+      if constexpr (V == 4) {
+        const int4 c4 = __ldg(reinterpret_cast<const int4*>(block_idx + r * topk + s));
+        const float4 v4 = __ldg(reinterpret_cast<const float4*>(lse_part + r * topk + s));
+        c[0] = c4.x, c[1] = c4.y, c[2] = c4.z, c[3] = c4.w;
+        v[0] = v4.x, v[1] = v4.y, v[2] = v4.z, v[3] = v4.w;
+      } else {
+        c[0] = __ldg(&block_idx[r * topk + s]);
+        v[0] = __ldg(&lse_part[r * topk + s]);
+      }
+#pragma unroll
+      for (int e = 0; e < V; ++e)
+        if (c[e] >= 0 && c[e] < nb) lse_merge(m, l, v[e], 1.f);
     }
   }
   for (int o = W / 2; o > 0; o >>= 1) {
@@ -485,11 +499,19 @@ cudaError_t launch_index_lse(const Shape& s, const void* q_idx, const void* k_id
   cudaError_t e = DI == 64 ? launch_lse_tc<64>(tk, prm, cx, st) : launch_lse_tc<32>(tk, prm, cx, st);
   if (e != cudaSuccess) return e;
   const int64_t rows = s.rows_kv();
+  // rows of whole 16-byte groups of slots, both arrays 16-byte aligned: 4 slots a load
+  const bool vec = (s.topk & 3) == 0 && (reinterpret_cast<uintptr_t>(block_idx) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(lse_part) & 15) == 0;
+  const int per_lane = vec ? 4 : 1;
   int W = 1;
-  while (W < s.topk && W < 32) W <<= 1;
+  while (W * per_lane < s.topk && W < 32) W <<= 1;
   const int64_t warps = (rows + (32 / W) - 1) / (32 / W);
-  lse_combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
-      lse_part, block_idx, lse_idx, s.spans, s.B, s.N, s.H_kv, rows, s.topk, s.nb, W);
+  if (vec)
+    lse_combine_kernel<4><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+        lse_part, block_idx, lse_idx, s.spans, s.B, s.N, s.H_kv, rows, s.topk, s.nb, W);
+  else
+    lse_combine_kernel<1><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+        lse_part, block_idx, lse_idx, s.spans, s.B, s.N, s.H_kv, rows, s.topk, s.nb, W);
   note_launch();
   return cudaGetLastError();
 }
