@@ -53,6 +53,9 @@ struct IdxParams {
   const int* units;   // packed batches: prefix counts of ceil(len / 256) per sequence
   int B, N, H_kv, nb, topk;
   int n_units;  // fixed layout: ceil(nb / 2) query-block pairs per sequence
+  // fixed layout: units from split_from on (the last wave's) are split in two CTAs, one
+  // group of the pair each, so that the last wave's CTAs are shorter
+  int split_from;
   int n_gp;     // ceil(H_kv / 2) group pairs
   uint64_t wait_ns;
   int debug;
@@ -122,18 +125,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // CTA -> (sequence, group pair, query-block pair); the pair (u, nbs-1-u) of a
   // sequence of nbs blocks
-  int b, u, gp;
+  int b, u, gp, half = -1;  // half >= 0: this CTA takes group 2 gp + half of a split unit
   if (!p.units) {
-    u = blockIdx.x % p.n_units;
-    gp = (blockIdx.x / p.n_units) % p.n_gp;
-    b = blockIdx.x / (p.n_units * p.n_gp);
+    int x = blockIdx.x;
+    if (x >= p.split_from) {
+      half = (x - p.split_from) & 1;
+      x = p.split_from + (x - p.split_from) / 2;
+    }
+    u = x % p.n_units;
+    gp = (x / p.n_units) % p.n_gp;
+    b = x / (p.n_units * p.n_gp);
   } else {
     gp = blockIdx.x % p.n_gp;
     if (!chunk_item(p.units, p.B, 0, blockIdx.x / p.n_gp, &b, &u)) return;  // whole CTA
   }
   const SeqSpan sp = seq_span(p.spans, b, p.N);
-  const int g0 = 2 * gp;
-  const int ng = min(2, p.H_kv - g0);
+  const int g0 = 2 * gp + (half > 0 ? 1 : 0);
+  const int ng = half >= 0 ? 1 : min(2, p.H_kv - g0);
   const int qa = (sp.len + 127) / 128 - 1 - u;  // heavy block first
   const int nq = (u < qa) ? 2 : 1;
   const int M = p.topk - 1;     // non-local slots
@@ -418,8 +426,17 @@ cudaError_t launch_index_topk(const Shape& s, const void* q_idx, const void* k_i
   p.wait_ns = cx.wait_ns;
   p.debug = cx.debug;
   p.status = cx.status;
-  const int64_t grid = (int64_t)p.n_gp * (s.packed() ? varlen_grid_items(s, kTabIndexUnit)
-                                                      : (int64_t)s.B * p.n_units);
+  int64_t grid = (int64_t)p.n_gp * (s.packed() ? varlen_grid_items(s, kTabIndexUnit)
+                                                : (int64_t)s.B * p.n_units);
+  // One CTA per SM.  Every unit of the fixed layout scores the same number of key tiles,
+  // so a last wave of at most half the SMs would leave the rest idle: its units go to two
+  // CTAs each, one group apiece (only when every pair holds two groups).
+  p.split_from = 0x7fffffff;
+  const int64_t rem = grid % cx.num_sms;
+  if (!s.packed() && s.H_kv % 2 == 0 && grid > cx.num_sms && rem > 0 && 2 * rem <= cx.num_sms) {
+    p.split_from = (int)(grid - rem);
+    grid += rem;
+  }
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   if (DI == 64) return launch_di<64>(s, tq, tk, p, (int)grid, st);
   return launch_di<32>(s, tq, tk, p, (int)grid, st);

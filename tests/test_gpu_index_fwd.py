@@ -58,6 +58,24 @@ def test_index_topk_matches_oracle(name, n_rows):
           f"differing {int(diff.sum())} lse_idx err {err:.2e}")
 
 
+def test_index_topk_split_last_wave_matches_oracle():
+    """B = 2, H_kv = 4, 80 blocks: 160 units (2 group pairs x 40 query-block pairs x 2
+    sequences) on a GPU of at most 160 SMs.  On 152 SMs the last 8 units (the second
+    sequence's second group pair, query blocks 32..47) run as two one-group CTAs each.
+    Every row is compared with the oracle, whichever way the grid was cut."""
+    cfg = T.with_(name="split-tail", B=2, N=10240, H_q=8, H_kv=4, seed=47)
+    h, d = device_inputs(cfg, names=("q_idx", "k_idx"))
+    bi, lse_idx = ops.msa_index_topk(d["q_idx"], d["k_idx"], cfg.topk, H_q=cfg.H_q, d=cfg.d)
+    assert ops.device_status() == 0
+    rows = np.arange(cfg.B * cfg.N, dtype=np.int64)
+    bi_ref, kth, _ = oracle.select(cfg, h, rows=None)
+    gsel = gpu_sel_rows(cfg, bi.cpu().numpy(), rows)
+    # every (row, group) set equal to the oracle's, or valid inside the near-tie band
+    n_same, n_near, diff = check_selection(cfg, h, gsel, rows, bi_ref, kth)
+    print(f"split-tail: (row, group) sets equal {n_same} of {gsel.shape[0] * gsel.shape[1]}, "
+          f"near-tie {n_near}, differing {int(diff.sum())}")
+
+
 @pytest.mark.parametrize("topk", [4, 6])
 def test_exact_ties_keep_the_lower_block(topk):
     """Key blocks that are block 0 scaled by 1, 2 or 4 score exactly that multiple of the
