@@ -45,6 +45,11 @@ WORKLOAD_STEPS = {"tiny": 20, "8k": 20, "32k": 10, "128k": 10, "1m": 3}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def cfg_label(cfg):
+    """The workload's short name as the text writes it: 128K, 1M, tiny."""
+    return cfg.name.upper() if cfg.name[:1].isdigit() else cfg.name
+
+
 def workload_name(cfg):
     return (f"MSA fwd+bwd: B={cfg.B} N={cfg.N} H_q={cfg.H_q} H_kv={cfg.H_kv} d={cfg.d} "
             f"d_idx={cfg.d_idx} Bk={cfg.Bk} k={cfg.topk} causal bf16, N(0,1) + "
@@ -388,7 +393,7 @@ def run_reference(args, cfg, rank):
         total_t += dt
     v = total_rows / total_t
     cores = os.cpu_count()
-    sample = (f"{rows_per_step} seeded query rows (+ first/last) of the 128K workload per step, "
+    sample = (f"{rows_per_step} seeded query rows (+ first/last) of the {cfg_label(cfg)} workload per step, "
               f"all {cfg.H_kv} groups: index top-k, forward, backward in float64")
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
@@ -759,7 +764,7 @@ def run_ours(args, cfg, rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n_rows, dt = oracle_sample(cfg, host, args.cpu_rows, seed=900)
         cpu = {"value": n_rows / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": (f"{n_rows} seeded query rows of the 128K workload, all {cfg.H_kv} groups: "
+               "sample": (f"{n_rows} seeded query rows of the {cfg_label(cfg)} workload, all {cfg.H_kv} groups: "
                           f"index top-k, forward, backward in float64 ({dt:.1f} s)")}
 
     # ---- every other seeded workload: the same step timed on its own inputs ----
